@@ -1,0 +1,164 @@
+/*
+ * icp.h - C ABI of the GB300 (sm_103a) decode-time ICP block indexer.
+ *
+ * The operations are the ones documented by FlashInfer's experimental
+ * MiniMax-M3 ICP indexer API pages (flashinfer.msa_ops):
+ *   msa_icp_decode_index_score_sharded  -> icp_score
+ *   msa_icp_topk_select_publish         -> icp_top16_select (select only) and
+ *                                          icp_publish_rows (select + legacy receive rows)
+ *   prepare_msa_icp_indexer, decode()   -> icp_merge (owner merge of the chain
+ *                                          "score plane -> select and publish -> owner merge")
+ *                                          and icp_score_select (fused scorer + select)
+ *
+ * Conventions for every entry point:
+ *   - All tensor pointers are DEVICE pointers owned by the caller, on the
+ *     current CUDA device; the library never frees or keeps them.
+ *   - `stream` is a cudaStream_t passed as void* (NULL = legacy default stream).
+ *     Calls only enqueue work: they allocate nothing and never synchronize,
+ *     so they may be recorded into a CUDA graph.
+ *   - fp8 tensors are float8_e4m3fn bit patterns passed as uint8_t; no scale.
+ *   - Return value: ICP_OK, or ICP_ERR_INVALID_ARG when a host-side check
+ *     fails (nothing is launched), ICP_ERR_UNSUPPORTED when the current device
+ *     is not an sm_103 GPU, ICP_ERR_CUDA when a CUDA call or launch fails.
+ *   - Device-side waits are bounded; a wait that runs out adds 1 to errors[0]
+ *     (when `errors` is not NULL) and the kernel returns without trapping.
+ *     The caller reads errors[0] after its own synchronization.
+ */
+#ifndef ICP_H
+#define ICP_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define ICP_OK 0
+#define ICP_ERR_INVALID_ARG 1
+#define ICP_ERR_CUDA 2
+#define ICP_ERR_UNSUPPORTED 3
+
+#define ICP_HEADS 4        /* index heads (prepare_msa_icp_indexer: num_index_heads must be 4) */
+#define ICP_DIM 128        /* fp8 values per index query / key row */
+#define ICP_TOPK 16        /* blocks kept per (token, head) row */
+#define ICP_ROW_WORDS 33   /* legacy receive row: 16 scores, 16 ids, ready flag */
+#define ICP_MAX_COLS 8192  /* msa_icp_decode_index_score_sharded: 0 < cols <= 8192 */
+#define ICP_MAX_K 12287    /* msa_icp_topk_select_publish: 0 < K < 12288 */
+#define ICP_MAX_BATCH 4096 /* requests per icp_score / icp_score_select call */
+
+/* Human-readable name of a status code (static string). */
+const char *icp_status_string(int status);
+
+/*
+ * Plane width for the longest request (msa_icp_decode_index_score_sharded,
+ * parameter score_out, which defers to msa_icp_decode_score_columns()):
+ * the number of columns of a request of max_seq_len tokens, rounded up to a
+ * multiple of four.  A column is a global B128 block at page_size 128, a
+ * local page at page_size 256 with world_size 2 or 4, and a B128 block at
+ * page_size 256 with world_size 1.  Returns the width, or -1 when the
+ * arguments are invalid or the width would exceed ICP_MAX_COLS.  Host only.
+ */
+int icp_score_columns(int max_seq_len, int page_size, int world_size);
+
+/*
+ * Decode index scores (msa_icp_decode_index_score_sharded).
+ *   index_q      [batch * decode_query_len, 4, 128] fp8, contiguous, 16-byte aligned;
+ *                token j of request b is row b * decode_query_len + j and sits at
+ *                position seq_lens[b] - decode_query_len + j.
+ *   index_k      [num_pages, page_size / world_size, 128] fp8 shard, contiguous,
+ *                16-byte aligned; this rank holds rows
+ *                [rank * page_size / world_size, (rank + 1) * page_size / world_size)
+ *                of every page.
+ *   block_table  int32 [batch, >= ceil(seq_len / page_size)], unit last stride,
+ *                row stride block_table_stride (elements); entries must lie in
+ *                [0, num_pages) (an entry outside reads as zero keys).
+ *   seq_lens     int32 [batch].
+ *   score_out    float32 [batch * decode_query_len, 4, cols], contiguous.  For
+ *                each request only columns c < round_up(n, 4) are written, n
+ *                being the request's column count (see icp_score_columns); the
+ *                other columns are not touched.  Written value: the maximum over
+ *                the column's keys at positions <= the token's position of the
+ *                fp32 dot product of the 128 dequantised values, -inf when no
+ *                key is visible.
+ *   Limits: 0 < cols <= 8192, cols % 4 == 0; page_size 128 or 256; world_size
+ *   1, 2 or 4 (1 is an extension of the documented 2 or 4); 0 <= rank <
+ *   world_size; 1 <= decode_query_len <= max_decode_query_len,
+ *   4 * max_decode_query_len <= 32; 0 <= batch <= ICP_MAX_BATCH.
+ *   errors: optional int32 [>= 1] counter for timed-out internal waits.
+ */
+int icp_score(const uint8_t *index_q, const uint8_t *index_k, int64_t num_pages,
+              const int32_t *block_table, int64_t block_table_stride, const int32_t *seq_lens,
+              float *score_out, int batch, int cols, int rank, int world_size, int page_size,
+              int decode_query_len, int max_decode_query_len, int32_t *errors, void *stream);
+
+/*
+ * Top16 select of every (token, head) row of a score plane (the selection
+ * half of msa_icp_topk_select_publish, written to plain output arrays).
+ *   scores           float32 [T, 4, K], contiguous, 0 < K <= 12287.
+ *   num_valid_pages  int32 [T]: global B128 block count of each token.
+ *   Column c carries global id c * index_scale + index_offset (index_scale
+ *   >= 1, index_offset >= 0); valid ids are those below num_valid_pages[t].
+ *   If num_valid_pages[t] <= 16 every valid id is kept.  Otherwise the ids
+ *   in [0, init_blocks) and [nvp - local_blocks, nvp) are forced and the
+ *   remaining slots take the best other valid ids by (score descending, id
+ *   ascending).  init_blocks + local_blocks <= 16.
+ *   out_scores float32 [T, 4, 16], out_ids int32 [T, 4, 16]: ids ascending,
+ *   each with its raw score, then padding id -1 / score -inf.  Every row is
+ *   written.
+ */
+int icp_top16_select(const float *scores, int T, int K, const int32_t *num_valid_pages,
+                     int init_blocks, int local_blocks, int index_scale, int index_offset,
+                     float *out_scores, int32_t *out_ids, void *stream);
+
+/*
+ * Top16 select and publish into legacy receive rows
+ * (msa_icp_topk_select_publish, legacy mode).
+ *   scores [T, world_size * heads_per_rank, K] (world_size * heads_per_rank
+ *   must be 4), num_valid_pages, index_scale, index_offset,
+ *   force_begin_blocks / force_end_blocks: as icp_top16_select.
+ *   recv_bases  int64 [world_size] DEVICE array of device addresses: the
+ *               receive storage of every owner rank, each int32
+ *               [3][world_size][heads_per_rank][capacity][33] (row-major) and
+ *               8-byte aligned.  On one GPU these are ws buffers of the device.
+ *   Row (t, h) goes to owner h / heads_per_rank, row
+ *   ((slot * world_size + rank) * heads_per_rank + h % heads_per_rank) * capacity + t:
+ *   words 0-15 the fp32 bits of the scores, 16-31 the ascending ids, word 32
+ *   the ready flag.  Before writing, the kernel polls the flag (acquire) until
+ *   it reads 0 (free), at most spin_limit polls and at most about two seconds;
+ *   it then stores the 32 data words and release-stores flag = 1.  A row
+ *   whose wait runs out is skipped and adds 1 to errors[0] (no trap).
+ *   Every row t < T, padding rows included, is written on every call.
+ *   Limits: slot 0..2; world_size 1, 2 or 4; 0 <= rank < world_size;
+ *   1 <= T <= capacity; spin_limit >= 1.  errors: int32 [>= 1], required.
+ */
+int icp_publish_rows(const float *scores, int T, int K, const int32_t *num_valid_pages,
+                     const int64_t *recv_bases, int32_t *errors, int slot, int rank,
+                     int world_size, int heads_per_rank, int capacity, int force_begin_blocks,
+                     int force_end_blocks, int64_t spin_limit, int index_scale,
+                     int index_offset, void *stream);
+
+/*
+ * Owner merge of the decode chain (prepare_msa_icp_indexer, decode():
+ * "score plane -> Top16 select and publish -> owner merge"; the merge rule is
+ * this library's reading: union of the world_size published lists, maximum
+ * score per id, then the icp_top16_select rule with num_valid_pages[t]).
+ *   recv   this owner's receive storage, int32 [3][world_size][heads_per_rank][capacity][33].
+ *   For each token t < T and owned head hl < heads_per_rank it waits (acquire,
+ *   at most spin_limit polls / about two seconds) for the flag of each source
+ *   row of slot `slot` to read 1, merges, and then clears the flags it read
+ *   back to 0 (rows free).  A source whose wait runs out is left out of the
+ *   merge and adds 1 to errors[0].
+ *   out_scores float32 [T, heads_per_rank, 16], out_ids int32 [T, heads_per_rank, 16].
+ *   Limits as icp_publish_rows.  errors: required.
+ */
+int icp_merge(int32_t *recv, const int32_t *num_valid_pages, int T, int slot, int world_size,
+              int heads_per_rank, int capacity, int init_blocks, int local_blocks,
+              int64_t spin_limit, int32_t *errors, float *out_scores, int32_t *out_ids,
+              void *stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* ICP_H */

@@ -1,0 +1,64 @@
+// icp_internal.h - host-side declarations shared by the library's .cu files.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace icp {
+
+// Geometry of one scoring call, derived on the host from the layout
+// arguments of msa_icp_decode_index_score_sharded.
+struct ScoreGeom {
+  int rows_per_page;  // K rows of one page held by this rank: page_size / world_size
+  int R;              // K rows feeding one plane column (32, 64 or 128)
+  int cpt;            // plane columns per 128-row MMA tile: 128 / R
+  int split;          // 1 when a column is one half of a 256-row page (P256, world_size 1)
+  int nq;             // MMA N: query rows of a request (4 * dql) rounded up to 16 or 32
+};
+
+struct ScoreArgs {
+  const int32_t *block_table;
+  int64_t bt_stride;
+  const int32_t *seq_lens;
+  float *score_out;
+  int32_t *errors;
+  int batch, cols, rank, world_size, page_size, dql;
+  ScoreGeom g;
+};
+
+struct SelectArgs {
+  const float *scores;
+  int T, K;
+  const int32_t *nvp;
+  int init_blocks, local_blocks, index_scale, index_offset;
+  // plain output
+  float *out_scores;
+  int32_t *out_ids;
+  // publish
+  const int64_t *recv_bases;
+  int32_t *errors;
+  int slot, rank, world_size, heads_per_rank, capacity;
+  long long spin_limit;
+};
+
+struct MergeArgs {
+  int32_t *recv;
+  const int32_t *nvp;
+  int T, slot, world_size, heads_per_rank, capacity, init_blocks, local_blocks;
+  long long spin_limit;
+  int32_t *errors;
+  float *out_scores;
+  int32_t *out_ids;
+};
+
+// Launchers (return a cudaError_t from the launch).
+cudaError_t launch_score(const CUtensorMap &tmk, const CUtensorMap &tmq, const ScoreArgs &a,
+                         int grid, cudaStream_t stream);
+size_t score_smem_bytes(int batch);
+cudaError_t score_prepare(int device);  // one-time per-device kernel attributes
+
+cudaError_t launch_select(const SelectArgs &a, bool publish, cudaStream_t stream);
+cudaError_t launch_merge(const MergeArgs &a, cudaStream_t stream);
+
+}  // namespace icp

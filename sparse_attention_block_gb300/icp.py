@@ -1,0 +1,177 @@
+"""ctypes binding to libicp.so: same names and argument order as include/icp.h.
+
+Marshalling only: each function checks dtypes, shapes, devices and
+contiguity of the torch tensors, then passes ``data_ptr()`` values and the
+current CUDA stream to the C entry point.  Every step of the computation runs
+in the library's CUDA kernels.  Importing this module fails loudly when the
+library has not been built (``python -m sparse_attention_block_gb300.build``);
+there is no fallback.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "_lib", "libicp.so")
+
+if not os.path.exists(LIB_PATH):
+    raise ImportError(
+        f"{LIB_PATH} is missing: build it with `python -m sparse_attention_block_gb300.build`")
+
+lib = ctypes.CDLL(LIB_PATH)
+
+HEADS, DIM, TOPK, ROW_WORDS = 4, 128, 16, 33
+MAX_COLS, MAX_K, MAX_BATCH = 8192, 12287, 4096
+DEFAULT_SPIN_LIMIT = 67108864
+
+OK, ERR_INVALID_ARG, ERR_CUDA, ERR_UNSUPPORTED = 0, 1, 2, 3
+
+_P, _I32, _I64, _SZ = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_size_t
+
+lib.icp_status_string.restype = ctypes.c_char_p
+lib.icp_status_string.argtypes = [_I32]
+lib.icp_score_columns.restype = _I32
+lib.icp_score_columns.argtypes = [_I32, _I32, _I32]
+lib.icp_score.restype = _I32
+lib.icp_score.argtypes = [_P, _P, _I64, _P, _I64, _P, _P, _I32, _I32, _I32, _I32, _I32, _I32,
+                          _I32, _P, _P]
+lib.icp_top16_select.restype = _I32
+lib.icp_top16_select.argtypes = [_P, _I32, _I32, _P, _I32, _I32, _I32, _I32, _P, _P, _P]
+lib.icp_publish_rows.restype = _I32
+lib.icp_publish_rows.argtypes = [_P, _I32, _I32, _P, _P, _P, _I32, _I32, _I32, _I32, _I32, _I32,
+                                 _I32, _I64, _I32, _I32, _P]
+lib.icp_merge.restype = _I32
+lib.icp_merge.argtypes = [_P, _P, _I32, _I32, _I32, _I32, _I32, _I32, _I32, _I64, _P, _P, _P, _P]
+
+
+class IcpError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        super().__init__(f"{where}: {lib.icp_status_string(status).decode()} (status {status})")
+
+
+def _check(status: int, where: str):
+    if status != OK:
+        raise IcpError(status, where)
+
+
+def _stream(stream):
+    if stream is None:
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, torch.cuda.Stream):
+        return stream.cuda_stream
+    return int(stream)
+
+
+def _dev(t: torch.Tensor, name: str, dtypes, ndim=None, contiguous=True):
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if t.device.type != "cuda":
+        raise ValueError(f"{name} must be on a CUDA device")
+    if t.dtype not in dtypes:
+        raise TypeError(f"{name} must have dtype in {dtypes}, got {t.dtype}")
+    if ndim is not None and t.dim() != ndim:
+        raise ValueError(f"{name} must have {ndim} dims, got shape {tuple(t.shape)}")
+    if contiguous and not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    return t.data_ptr()
+
+
+_FP8 = (torch.uint8, torch.float8_e4m3fn)
+
+
+def icp_score_columns(max_seq_len: int, page_size: int, world_size: int) -> int:
+    cols = lib.icp_score_columns(int(max_seq_len), int(page_size), int(world_size))
+    if cols < 0:
+        raise ValueError("invalid arguments for icp_score_columns")
+    return cols
+
+
+def icp_score(index_q, index_k, block_table, seq_lens, score_out, *, rank: int, world_size: int,
+              page_size: int, decode_query_len: int, max_decode_query_len: int, errors=None,
+              stream=None):
+    """Decode index scores into score_out [T, 4, cols] (msa_icp_decode_index_score_sharded)."""
+    B = seq_lens.shape[0]
+    T = B * decode_query_len
+    qp = _dev(index_q, "index_q", _FP8, 3)
+    kp = _dev(index_k, "index_k", _FP8, 3)
+    if tuple(index_q.shape) != (T, HEADS, DIM):
+        raise ValueError(f"index_q must be [{T}, 4, 128], got {tuple(index_q.shape)}")
+    if tuple(index_k.shape[1:]) != (page_size // world_size, DIM):
+        raise ValueError(f"index_k must be [pages, {page_size // world_size}, 128]")
+    if block_table.dim() != 2 or block_table.stride(1) != 1:
+        raise ValueError("block_table must be 2-D with unit last stride")
+    btp = _dev(block_table, "block_table", (torch.int32,), 2, contiguous=False)
+    slp = _dev(seq_lens, "seq_lens", (torch.int32,), 1)
+    sop = _dev(score_out, "score_out", (torch.float32,), 3)
+    if score_out.shape[0] != T or score_out.shape[1] != HEADS:
+        raise ValueError(f"score_out must be [{T}, 4, cols]")
+    ep = 0 if errors is None else _dev(errors, "errors", (torch.int32,), 1)
+    _check(lib.icp_score(qp, kp, index_k.shape[0], btp, block_table.stride(0), slp, sop, B,
+                         score_out.shape[2], rank, world_size, page_size, decode_query_len,
+                         max_decode_query_len, ep, _stream(stream)), "icp_score")
+
+
+def icp_top16_select(scores, num_valid_pages, out_scores, out_ids, *, init_blocks: int,
+                     local_blocks: int, index_scale: int = 1, index_offset: int = 0,
+                     stream=None):
+    """Top16 of every (token, head) row of scores [T, 4, K] into out_* [T, 4, 16]."""
+    sp = _dev(scores, "scores", (torch.float32,), 3)
+    T, H, K = scores.shape
+    if H != HEADS:
+        raise ValueError("scores must have 4 heads")
+    np_ = _dev(num_valid_pages, "num_valid_pages", (torch.int32,), 1)
+    if num_valid_pages.shape[0] != T:
+        raise ValueError("num_valid_pages must be [T]")
+    osp = _dev(out_scores, "out_scores", (torch.float32,), 3)
+    oip = _dev(out_ids, "out_ids", (torch.int32,), 3)
+    if tuple(out_scores.shape) != (T, HEADS, TOPK) or tuple(out_ids.shape) != (T, HEADS, TOPK):
+        raise ValueError("out_scores / out_ids must be [T, 4, 16]")
+    _check(lib.icp_top16_select(sp, T, K, np_, init_blocks, local_blocks, index_scale,
+                                index_offset, osp, oip, _stream(stream)), "icp_top16_select")
+
+
+def recv_rows(world_size: int, heads_per_rank: int, capacity: int) -> int:
+    """Rows of one owner's legacy receive storage: [3][ws][hpr][capacity]."""
+    return 3 * world_size * heads_per_rank * capacity
+
+
+def icp_publish_rows(scores, num_valid_pages, recv_bases, errors, *, slot: int, rank: int,
+                     world_size: int, heads_per_rank: int, capacity: int,
+                     force_begin_blocks: int, force_end_blocks: int,
+                     spin_limit: int = DEFAULT_SPIN_LIMIT, index_scale: int = 1,
+                     index_offset: int = 0, stream=None):
+    """Top16 select + publish into legacy receive rows (msa_icp_topk_select_publish)."""
+    sp = _dev(scores, "scores", (torch.float32,), 3)
+    T, H, K = scores.shape
+    if H != world_size * heads_per_rank:
+        raise ValueError("scores must have world_size * heads_per_rank heads")
+    np_ = _dev(num_valid_pages, "num_valid_pages", (torch.int32,), 1)
+    rbp = _dev(recv_bases, "recv_bases", (torch.int64,), 1)
+    if recv_bases.shape[0] != world_size:
+        raise ValueError("recv_bases must be [world_size]")
+    ep = _dev(errors, "errors", (torch.int32,), 1)
+    _check(lib.icp_publish_rows(sp, T, K, np_, rbp, ep, slot, rank, world_size, heads_per_rank,
+                                capacity, force_begin_blocks, force_end_blocks, spin_limit,
+                                index_scale, index_offset, _stream(stream)), "icp_publish_rows")
+
+
+def icp_merge(recv, num_valid_pages, out_scores, out_ids, errors, *, T: int, slot: int,
+              world_size: int, heads_per_rank: int, capacity: int, init_blocks: int,
+              local_blocks: int, spin_limit: int = DEFAULT_SPIN_LIMIT, stream=None):
+    """Owner merge of this owner's receive rows into out_* [T, heads_per_rank, 16]."""
+    rp = _dev(recv, "recv", (torch.int32,), None)
+    if recv.numel() < recv_rows(world_size, heads_per_rank, capacity) * ROW_WORDS:
+        raise ValueError("recv is smaller than [3][ws][hpr][capacity][33]")
+    np_ = _dev(num_valid_pages, "num_valid_pages", (torch.int32,), 1)
+    osp = _dev(out_scores, "out_scores", (torch.float32,), 3)
+    oip = _dev(out_ids, "out_ids", (torch.int32,), 3)
+    if tuple(out_scores.shape) != (T, heads_per_rank, TOPK) or \
+            tuple(out_ids.shape) != (T, heads_per_rank, TOPK):
+        raise ValueError("out_scores / out_ids must be [T, heads_per_rank, 16]")
+    ep = _dev(errors, "errors", (torch.int32,), 1)
+    _check(lib.icp_merge(rp, np_, T, slot, world_size, heads_per_rank, capacity, init_blocks,
+                         local_blocks, spin_limit, ep, osp, oip, _stream(stream)), "icp_merge")

@@ -1,0 +1,93 @@
+"""The C ABI library loads on a machine without a GPU, exports every entry
+point include/icp.h declares, and rejects bad arguments on the host before
+touching CUDA (no compute call is made here)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "icp.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from sparse_attention_block_gb300 import build
+    return ctypes.CDLL(build.build())
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"^\s*(?:const\s+)?\w+\s*\*?\s*(icp_\w+)\s*\(", text, flags=re.M)))
+
+
+def test_header_declares_the_entry_points():
+    names = declared_functions()
+    for n in ["icp_score", "icp_top16_select", "icp_publish_rows", "icp_merge",
+              "icp_score_columns", "icp_status_string"]:
+        assert n in names
+
+
+def test_every_declared_symbol_is_exported(lib):
+    for n in declared_functions():
+        assert hasattr(lib, n), n
+
+
+def test_only_the_c_abi_is_exported():
+    from sparse_attention_block_gb300 import build
+    out = os.popen(f"nm -D --defined-only {build.LIB_PATH}").read()
+    syms = [l.split()[-1] for l in out.splitlines() if " T " in l]
+    assert syms and all(s.startswith("icp_") for s in syms), syms
+
+
+def test_score_columns_host_helper(lib):
+    f = lib.icp_score_columns
+    assert f(1000, 128, 1) == 8
+    assert f(1_000_000, 128, 1) == 7816
+    assert f(131072, 256, 1) == 1024
+    assert f(131072, 256, 2) == 512
+    assert f(0, 128, 4) == 4
+    assert f(2_000_000, 128, 1) == -1      # beyond 8192 columns
+    assert f(100, 64, 1) == -1
+
+
+def test_invalid_arguments_are_rejected_before_any_launch(lib):
+    P = ctypes.c_void_p
+    buf = ctypes.create_string_buffer(1 << 16)
+    a = ctypes.cast(ctypes.addressof(buf) + (-ctypes.addressof(buf) % 256), P)
+    lib.icp_score.argtypes = [P, P, ctypes.c_int64, P, ctypes.c_int64, P, P] + \
+        [ctypes.c_int] * 7 + [P, P]
+    good = dict(q=a, k=a, n=4, bt=a, st=4, sl=a, out=a, B=1, cols=8, rank=0, ws=1, ps=128,
+                dql=1, maxdql=1)
+
+    def call(**kw):
+        d = dict(good, **kw)
+        return lib.icp_score(d["q"], d["k"], d["n"], d["bt"], d["st"], d["sl"], d["out"], d["B"],
+                             d["cols"], d["rank"], d["ws"], d["ps"], d["dql"], d["maxdql"],
+                             None, None)
+    INVALID = 1
+    assert call(cols=6) == INVALID            # cols % 4 != 0
+    assert call(cols=8196) == INVALID         # cols > 8192
+    assert call(ps=64) == INVALID
+    assert call(ws=3) == INVALID
+    assert call(rank=1) == INVALID
+    assert call(dql=2, maxdql=1) == INVALID
+    assert call(dql=1, maxdql=9) == INVALID   # 4 * max_decode_query_len > 32
+    assert call(B=-1) == INVALID
+    assert call(q=ctypes.c_void_p(a.value + 8)) == INVALID   # TMA needs 16-byte alignment
+    assert call(B=0) == 0                     # empty batch: nothing to do
+    lib.icp_top16_select.argtypes = [P, ctypes.c_int, ctypes.c_int, P] + [ctypes.c_int] * 4 + \
+        [P, P, P]
+    assert lib.icp_top16_select(a, 1, 12288, a, 1, 2, 1, 0, a, a, None) == INVALID  # K >= 12288
+    assert lib.icp_top16_select(a, 1, 100, a, 9, 8, 1, 0, a, a, None) == INVALID   # init+local > 16
+    assert lib.icp_top16_select(a, 1, 100, a, 1, 2, 0, 0, a, a, None) == INVALID   # scale 0
+    lib.icp_publish_rows.argtypes = [P, ctypes.c_int, ctypes.c_int, P, P, P] + \
+        [ctypes.c_int] * 7 + [ctypes.c_int64, ctypes.c_int, ctypes.c_int, P]
+    # T > capacity, slot 3, hpr * ws != 4
+    assert lib.icp_publish_rows(a, 5, 10, a, a, a, 0, 0, 1, 4, 4, 1, 2, 100, 1, 0, None) == INVALID
+    assert lib.icp_publish_rows(a, 4, 10, a, a, a, 3, 0, 1, 4, 4, 1, 2, 100, 1, 0, None) == INVALID
+    assert lib.icp_publish_rows(a, 4, 10, a, a, a, 0, 0, 2, 1, 4, 1, 2, 100, 1, 0, None) == INVALID
+    lib.icp_status_string.restype = ctypes.c_char_p
+    assert lib.icp_status_string(1) == b"invalid argument"

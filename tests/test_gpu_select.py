@@ -1,0 +1,85 @@
+"""icp_top16_select (CUDA) against the oracle's select run on the same plane:
+ids and score bits must be identical."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from sparse_attention_block_gb300 import workloads as W
+
+from gpu_util import assert_select_equal, gpu_select
+
+pytestmark = pytest.mark.gpu
+
+
+def _check(plane, nvp, init, local, scale=1, offset=0, what=""):
+    p = plane.cuda()
+    n = nvp.cuda()
+    gs, gi = gpu_select(p, n, init=init, local=local, scale=scale, offset=offset)
+    torch.cuda.synchronize()
+    os_, oi = oracle.select(plane.numpy(), nvp.numpy(), init_blocks=init, local_blocks=local,
+                            index_scale=scale, index_offset=offset)
+    assert_select_equal(gs, gi, os_, oi, what)
+
+
+def test_standalone_plane_full_size():
+    plane, nvp = W.make_select_plane(seed=0)
+    _check(plane, nvp, W.SELECT_INIT, W.SELECT_LOCAL, what="[256,4,12284]")
+
+
+@pytest.mark.parametrize("K", [1, 3, 16, 17, 100, 1024, 1025, 4096, 4097, 12287])
+def test_widths_across_kernel_variants(K):
+    plane, nvp = W.make_select_plane(T=8, K=K, seed=K)
+    nvp = torch.tensor([1, 2, 16, 17, max(1, K // 2), K, K + 5, 1 << 30], dtype=torch.int32)
+    for init, local in [(0, 0), (1, 2), (4, 8), (16, 0), (0, 16)]:
+        _check(plane, nvp, init, local, what=f"K={K} init={init} local={local}")
+
+
+def test_all_equal_and_minus_inf_rows():
+    T, K = 4, 3000
+    plane = torch.zeros((T, 4, K))
+    plane[1] = -float("inf")
+    plane[2, :, ::7] = 1.0
+    plane[3] = torch.randn(4, K).round()            # heavy ties
+    nvp = torch.tensor([K, K, K, 40], dtype=torch.int32)
+    _check(plane, nvp, 1, 2, what="ties")
+
+
+def test_adversarial_candidates_in_one_stripe():
+    # the best values all sit in the columns of one thread's stripe
+    for NT, K in [(128, 1024), (256, 4096), (512, 12287)]:
+        plane = torch.randn((2, 4, K))
+        cols = torch.arange(0, K, NT)
+        plane[:, :, cols] = 100.0 + torch.arange(cols.numel()).float()
+        plane[1, :, cols] = 100.0                    # tied as well
+        nvp = torch.tensor([K, K], dtype=torch.int32)
+        _check(plane, nvp, 2, 3, what=f"stripe NT={NT}")
+
+
+def test_index_scale_and_offset():
+    plane, _ = W.make_select_plane(T=6, K=2000, seed=9)
+    nvp = torch.tensor([1, 10, 33, 500, 4000, 4001], dtype=torch.int32)
+    for scale, offset in [(2, 0), (2, 1), (3, 2)]:
+        _check(plane, nvp, 2, 4, scale=scale, offset=offset, what=f"scale {scale} off {offset}")
+
+
+def test_signed_zero_and_duplicates():
+    plane = torch.zeros((2, 4, 600))
+    plane[0, :, :300] = -0.0
+    plane[1] = torch.randn(4, 600)
+    plane[1, :, 300:] = plane[1, :, :300]
+    nvp = torch.tensor([600, 600], dtype=torch.int32)
+    _check(plane, nvp, 3, 3, what="zeros")
+
+
+def test_select_on_gpu_plane_of_batched_workload():
+    from gpu_util import gpu_score, to_dev
+    inp = W.make_decode_inputs(W.BATCHED, seed=1, batch=16)
+    q, k, bt, sl, nvp = to_dev(inp)
+    cols = W.columns_for(W.BATCHED, int(inp.seq_lens.max()))
+    plane = gpu_score(q, k, bt, sl, cols=cols, rank=0, world_size=1, page_size=128, dql=1)
+    gs, gi = gpu_select(plane, nvp, init=1, local=4)
+    torch.cuda.synchronize()
+    os_, oi = oracle.select(plane.cpu().numpy(), inp.num_valid_pages.numpy(), init_blocks=1,
+                            local_blocks=4)
+    assert_select_equal(gs, gi, os_, oi, "batched plane")
