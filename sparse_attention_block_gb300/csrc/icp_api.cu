@@ -107,7 +107,8 @@ icp::ScoreGeom make_geom(int ps, int ws, int dql) {
   g.split = (ps == 256 && ws == 1) ? 1 : 0;
   g.R = g.split ? 128 : g.rows_per_page;
   g.cpt = 128 / g.R;
-  g.nq = (4 * dql <= 16) ? 16 : 32;
+  g.nq = 32;  // query rows staged per request (4 * dql <= 32), one TMA box
+  (void)dql;
   return g;
 }
 

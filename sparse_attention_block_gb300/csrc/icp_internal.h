@@ -14,7 +14,7 @@ struct ScoreGeom {
   int R;              // K rows feeding one plane column (32, 64 or 128)
   int cpt;            // plane columns per 128-row MMA tile: 128 / R
   int split;          // 1 when a column is one half of a 256-row page (P256, world_size 1)
-  int nq;             // MMA N: query rows of a request (4 * dql) rounded up to 16 or 32
+  int nq;             // query rows staged per request: 32 (4 * dql of them are used)
 };
 
 struct ScoreArgs {

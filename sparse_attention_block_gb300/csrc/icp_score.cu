@@ -10,14 +10,19 @@
 // How (one persistent CTA per SM, 192 threads, warp-specialised):
 //   warp 0     TMA producer: streams the 128-row K tiles of the CTA's share of
 //              all requests' pages (each page read once per call) into an
-//              8-stage shared-memory ring, and each request's queries once.
-//   warp 1     MMA issuer: per tile, 4 x tcgen05.mma kind::f8f6f4 (M=128 keys,
-//              N = 16 or 32 query rows, K = 32) into an fp32 TMEM accumulator.
+//              8-stage shared-memory ring, and each request's 32 query rows
+//              (4 * dql used) once, stored four times so that every TMEM lane
+//              quarter receives all of them.
+//   warp 1     MMA issuer: per tile, 4 x tcgen05.mma kind::f8f6f4 with
+//              A = the replicated queries (M = 128), B = the 128 keys of the
+//              tile (N = 128), K = 32, into one of 4 fp32 TMEM accumulators.
 //              All 4 heads and all dql tokens share one K tile.
-//   warps 2-5  epilogue: tcgen05.ld of the accumulator (thread = key, registers
-//              = query rows), causal mask, max over the column's keys by a
-//              transposed warp butterfly (plus shared memory across warps when a
-//              column spans several warps), and the plane store.
+//   warps 2-5  epilogue: tile i belongs to epilogue warp i % 4, which reads
+//              its lane quarter of the accumulator (thread = query row,
+//              registers = the tile's 128 key scores), applies the causal
+//              mask, folds each column's keys with a register max tree and
+//              stores one plane value per (query row, column).  No shuffles
+//              and no cross-warp synchronisation are needed.
 // The tiles of all requests form one list that is cut into gridDim.x equal
 // contiguous ranges, so every CTA streams the same number of K bytes.
 // Products of two e4m3 values are exact in fp32; the MMA sums 128 of them in
@@ -30,11 +35,13 @@ namespace icp {
 namespace {
 
 constexpr int kStages = 8;
-constexpr int kAcc = 8;
+constexpr int kAcc = 4;                // one accumulator per epilogue warp
 constexpr int kTileBytes = 128 * 128;  // 128 K rows x 128 fp8
-constexpr int kQBytes = 32 * 128;      // up to 32 query rows x 128 fp8
+constexpr int kQRows = 32;             // query rows staged per request (4 * dql <= 32)
+constexpr int kQBytes = 4 * kQRows * 128;  // four copies -> the 128-row A operand
 constexpr int kThreads = 192;
-constexpr uint32_t kTmemCols = 256;    // kAcc accumulators of up to 32 columns
+constexpr uint32_t kAccCols = 128;     // N = 128 keys per accumulator
+constexpr uint32_t kTmemCols = kAcc * kAccCols;
 constexpr int kNumBars = 2 * kStages + 2 * kAcc + 4 + 1;
 
 // Shared-memory carve-up (offsets from a 1024-byte aligned base).
@@ -42,8 +49,7 @@ constexpr uint32_t kOffStages = 0;
 constexpr uint32_t kOffQ = kOffStages + kStages * kTileBytes;
 constexpr uint32_t kOffBars = kOffQ + 2 * kQBytes;
 constexpr uint32_t kOffMisc = kOffBars + ((kNumBars * 8 + 127) / 128) * 128;
-constexpr uint32_t kOffRed = kOffMisc + 128;
-constexpr uint32_t kOffPrefix = kOffRed + 2 * 4 * 32 * 4;
+constexpr uint32_t kOffPrefix = kOffMisc + 128;
 
 __device__ __forceinline__ int units_of(int seq_len, int page_size, int split) {
   const int u = split ? 128 : page_size;
@@ -82,86 +88,50 @@ struct SegmentWalker {
 __device__ __forceinline__ int page_slot_of(int c, int split) { return split ? (c >> 1) : c; }
 __device__ __forceinline__ int row_off_of(int c, int split) { return split ? (c & 1) * 128 : 0; }
 
-// Max over the 32 lanes of the warp for each of N values, done as a
-// transposed butterfly: each exchange halves the values a lane keeps, so the
-// whole reduction costs about N shuffles per lane.  On return v[0] of lane l
-// holds the maximum for value index l (N = 32) or l >> 1 (N = 16).
-template <int N>
-__device__ __forceinline__ void warp_transpose_max(float (&v)[N], int lane) {
-  static_assert(N == 16 || N == 32, "N");
+// Epilogue of one tile for the warp that owns it.  taddr addresses the
+// warp's lane quarter of the tile's accumulator: lane l holds query row l
+// (row = token j * 4 + head), columns 0..127 hold the tile's keys in order.
+// R keys feed one plane column, so the tile covers 128 / R columns.
+template <int R>
+__device__ __forceinline__ void epilogue_tile(const ScoreArgs &a, uint32_t taddr, int lane, int b,
+                                              int tl, int nunits, int seq_len, uint32_t tempty,
+                                              volatile int *abort_flag) {
+  constexpr int CPT = 128 / R;
+  float v[128];
 #pragma unroll
-  for (int o = 16, n = N; o >= 1; o >>= 1) {
-    if (n > 1) {
-      const bool upper = (lane & o) != 0;
-      const int h = n >> 1;
-#pragma unroll
-      for (int i = 0; i < h; ++i) {
-        const float send = upper ? v[i] : v[i + h];
-        const float keep = upper ? v[i + h] : v[i];
-        const float got = __shfl_xor_sync(0xFFFFFFFFu, send, o);
-        v[i] = fmaxf(keep, got);
-      }
-      n = h;
-    } else {
-      v[0] = fmaxf(v[0], __shfl_xor_sync(0xFFFFFFFFu, v[0], o));
-    }
-  }
-}
-
-__device__ __forceinline__ void named_bar_sync(int id, int nthreads) {
-  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
-}
-
-template <int NQ>
-__device__ __forceinline__ void epilogue_tile(const ScoreArgs &a, uint32_t taddr, int q, int lane,
-                                              int b, int tl, int nunits, int seq_len,
-                                              float *red_buf, int par) {
-  float v[NQ];
-  {
-    float lo[16];
-    tmem_ld16(taddr, lo);
-#pragma unroll
-    for (int i = 0; i < 16; ++i) v[i] = lo[i];
-    if constexpr (NQ == 32) {
-      float hi[16];
-      tmem_ld16(taddr + 16, hi);
-#pragma unroll
-      for (int i = 0; i < 16; ++i) v[16 + i] = hi[i];
-    }
-  }
+  for (int k = 0; k < 4; ++k) tmem_ld32(taddr + 32u * k, v + 32 * k);
   tmem_wait_ld();
-  (void)b;
+  // the accumulator is in registers: hand it back to the MMA warp
+  tc_fence_before();
+  __syncwarp();
+  if (lane == 0) mbar_arrive(tempty);
+  (void)abort_flag;
+
   const ScoreGeom &g = a.g;
-  const int cc = (q * 32) / g.R;
-  const int c = tl * g.cpt + cc;
-  const int i = (q * 32) % g.R + lane;
-  const long long pos0 = g.split ? (long long)c * 128
-                                 : (long long)c * a.page_size + (long long)a.rank * g.rows_per_page;
-  const long long pos = pos0 + i;
   const long long pfirst = (long long)seq_len - a.dql;  // position of token 0
-  if (pos > pfirst) {
+  const long long p_lane = pfirst + (lane >> 2);        // position of this row's token
+  const bool row_ok = lane < 4 * a.dql;
 #pragma unroll
-    for (int r = 0; r < NQ; ++r)
-      if (pos > pfirst + (r >> 2)) v[r] = -INFINITY;
-  }
-  warp_transpose_max<NQ>(v, lane);
-  float m = v[0];
-  const int wpc = g.R >> 5;  // warps per column
-  bool writer = true;
-  if (wpc > 1) {
-    red_buf[(par * 4 + q) * 32 + lane] = m;
-    named_bar_sync(1, 128);
-    writer = (q % wpc) == 0;
-    if (writer) {
-      for (int w = 1; w < wpc; ++w) m = fmaxf(m, red_buf[(par * 4 + q + w) * 32 + lane]);
+  for (int cc = 0; cc < CPT; ++cc) {
+    const int c = tl * CPT + cc;
+    if (c >= nunits) break;
+    float *vc = v + cc * R;
+    const long long pos0 = g.split ? (long long)c * 128
+                                   : (long long)c * a.page_size +
+                                         (long long)a.rank * g.rows_per_page;
+    if (pos0 + R - 1 > pfirst) {
+#pragma unroll
+      for (int i = 0; i < R; ++i)
+        if (pos0 + i > p_lane) vc[i] = -INFINITY;
     }
-  }
-  if (writer && c < nunits && c < a.cols) {
-    const int row = (NQ == 32) ? lane : (lane >> 1);
-    const bool holder = (NQ == 32) || ((lane & 1) == 0);
-    if (holder && row < 4 * a.dql) {
-      const long long prow = (long long)b * a.dql * 4 + row;
-      a.score_out[prow * a.cols + c] = m + 0.0f;  // + 0 folds -0 onto +0
+#pragma unroll
+    for (int st = R / 2; st >= 1; st >>= 1) {
+#pragma unroll
+      for (int i = 0; i < st; ++i) vc[i] = fmaxf(vc[i], vc[i + st]);
+    }
+    if (row_ok && c < a.cols) {
+      const long long prow = (long long)b * a.dql * 4 + lane;
+      a.score_out[prow * a.cols + c] = vc[0] + 0.0f;  // + 0 folds -0 onto +0
     }
   }
 }
@@ -187,7 +157,6 @@ score_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CU
   const uint32_t bar_done = sb + kOffBars + 8u * (2 * kStages + 2 * kAcc + 4);
 
   volatile int *misc = reinterpret_cast<volatile int *>(gb + kOffMisc);  // [0] tmem, [1] abort
-  float *red_buf = reinterpret_cast<float *>(gb + kOffRed);
   int *prefix = reinterpret_cast<int *>(gb + kOffPrefix);
   int *partial = prefix + a.batch + 1;  // kThreads scratch ints
 
@@ -198,7 +167,7 @@ score_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CU
     }
     for (int i = 0; i < kAcc; ++i) {
       mbar_init(bar_tfull(i), 1);
-      mbar_init(bar_tempty(i), 4);
+      mbar_init(bar_tempty(i), 1);
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(bar_qfull(i), 1);
@@ -270,8 +239,10 @@ score_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CU
       ok = __shfl_sync(0xFFFFFFFFu, ok, 0) != 0;
       if (!ok) break;
       if (lane == 0) {
-        mbar_arrive_expect_tx(bar_qfull(qslot), (uint32_t)(g.nq * 128));
-        tma_load_2d(sb + kOffQ + qslot * kQBytes, &tmq, 0, b * a.dql * 4, bar_qfull(qslot));
+        mbar_arrive_expect_tx(bar_qfull(qslot), (uint32_t)kQBytes);
+        for (int r = 0; r < 4; ++r)
+          tma_load_2d(sb + kOffQ + qslot * kQBytes + r * kQRows * 128, &tmq, 0, b * a.dql * 4,
+                      bar_qfull(qslot));
       }
       last_qslot = qslot;
       qph[qslot] ^= 1u;
@@ -323,7 +294,7 @@ score_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CU
     }
   } else if (warp == 1) {
     // ---------------------------------------------------------- MMA issuer
-    const uint32_t idesc = idesc_f8_f32(128, g.nq);
+    const uint32_t idesc = idesc_f8_f32(128, (int)kAccCols);
     int stage = 0, acc = 0;
     uint32_t sphase = 0, aphase = 0;
     uint32_t qph[2] = {0u, 0u};
@@ -343,10 +314,10 @@ score_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CU
           if (ok) {
             tc_fence_after();
             const uint32_t kaddr = sb + kOffStages + stage * kTileBytes;
-            const uint32_t d = tmem_base + (uint32_t)(acc * g.nq);
+            const uint32_t d = tmem_base + (uint32_t)acc * kAccCols;
 #pragma unroll
             for (int k = 0; k < 4; ++k)
-              mma_f8(d, smem_desc_sw128(kaddr + 32 * k), smem_desc_sw128(qaddr + 32 * k), idesc,
+              mma_f8(d, smem_desc_sw128(qaddr + 32 * k), smem_desc_sw128(kaddr + 32 * k), idesc,
                      k > 0 ? 1u : 0u);
             mma_commit(bar_empty(stage));
             mma_commit(bar_tfull(acc));
@@ -376,7 +347,8 @@ score_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CU
     }
   } else {
     // ------------------------------------------------------------ epilogue
-    const int q = warp & 3;  // TMEM lane quarter this warp may access
+    const int q = warp & 3;      // TMEM lane quarter this warp may access
+    const int e = warp - 2;      // owns tiles i with i % 4 == e, accumulator e
     const int et = threadIdx.x - 64;
     // padding columns [units, round_up(units, 4)) of the requests this CTA owns
     for (int b = blockIdx.x; b < a.batch; b += gridDim.x) {
@@ -390,36 +362,32 @@ score_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CU
         a.score_out[((long long)b * a.dql * 4 + r) * a.cols + c] = -INFINITY;
       }
     }
-    int acc = 0, par = 0;
     uint32_t aphase = 0;
+    int idx = 0;
+    const uint32_t taddr = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)e * kAccCols;
     SegmentWalker walk(prefix, a.batch, g0, g1);
     int b, t0, t1;
     bool ok = true;
     while (ok && walk.next(b, t0, t1)) {
       const int seq_len = a.seq_lens[b];
       const int nunits = units_of(seq_len, a.page_size, g.split);
-      for (int tl = t0; tl < t1; ++tl) {
-        if (lane == 0) ok = mbar_wait(bar_tfull(acc), aphase, abort_flag);
+      // first tile of this segment that belongs to this warp
+      int tl = t0 + ((e - idx) % 4 + 4) % 4;
+      idx += t1 - t0;
+      for (; tl < t1; tl += 4) {
+        if (lane == 0) ok = mbar_wait(bar_tfull(e), aphase, abort_flag);
         ok = __shfl_sync(0xFFFFFFFFu, ok, 0) != 0;
         if (!ok) break;
         tc_fence_after();
-        const uint32_t taddr = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * g.nq);
-        if (g.nq == 32)
-          epilogue_tile<32>(a, taddr, q, lane, b, tl, nunits, seq_len, red_buf, par);
+        if (g.R == 128)
+          epilogue_tile<128>(a, taddr, lane, b, tl, nunits, seq_len, bar_tempty(e), abort_flag);
+        else if (g.R == 64)
+          epilogue_tile<64>(a, taddr, lane, b, tl, nunits, seq_len, bar_tempty(e), abort_flag);
         else
-          epilogue_tile<16>(a, taddr, q, lane, b, tl, nunits, seq_len, red_buf, par);
-        // epilogue_tile has read the accumulator (tcgen05.wait::ld inside)
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(bar_tempty(acc));
-        par ^= 1;
-        if (++acc == kAcc) {
-          acc = 0;
-          aphase ^= 1u;
-        }
+          epilogue_tile<32>(a, taddr, lane, b, tl, nunits, seq_len, bar_tempty(e), abort_flag);
+        aphase ^= 1u;
       }
     }
-    (void)et;
   }
 
   __syncthreads();
