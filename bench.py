@@ -44,7 +44,12 @@ FALLBACK_HBM_GBS = 6800.0
 # ncu DRAM counters of icp_score per unit of work (bytes per index-K byte
 # streamed), measured for the kernel source with this digest.  When the
 # kernel changes the digest no longer matches and `traffic` is reported null.
-NCU_TRAFFIC = {}
+NCU_TRAFFIC = {
+    # dram__bytes_read.sum + dram__bytes_write.sum = 282.52 MB for 278.33 MB of
+    # index-K (first 32 requests of the multitoken workload), see
+    # profiles/icp_score_multitoken.md
+    ("multitoken", "6bd521b5662f04b5"): 282.524928 / 278.330624,
+}
 
 
 # ---------------------------------------------------------------- utilities
