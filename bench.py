@@ -237,10 +237,25 @@ class DecodeBench:
         self.out_i = [torch.empty((self.T, self.hpr, 16), dtype=torch.int32, device=device)
                       for _ in range(ws)]
         self.slot = 0
+        wsz = icp.icp_score_select_workspace_bytes(len(inp.seq_lens), spec.decode_query_len)
+        self.work = torch.empty((wsz,), dtype=torch.uint8, device=device)
+        self.f_s = [torch.empty((self.T, 4, 16), dtype=torch.float32, device=device)
+                    for _ in range(ws)]
+        self.f_i = [torch.empty((self.T, 4, 16), dtype=torch.int32, device=device)
+                    for _ in range(ws)]
         self.seq_list = inp.seq_lens.cpu().tolist()
         self.score_bytes, self.select_bytes, self.merge_bytes, self.kbytes = \
             algorithmic_bytes(spec, self.seq_list, self.cols)
         self.launches_per_step = 3 * ws
+
+    @property
+    def fused_bytes(self):
+        """icp_score_select per step: index-K rows needed + queries + block table +
+        num_valid_pages + the Top16 output, per shard; no plane."""
+        spec, ws = self.spec, self.ws
+        bt = ws * sum(4 * ((int(L) + spec.page_size - 1) // spec.page_size)
+                      for L in self.seq_list)
+        return self.kbytes + ws * (self.T * 512 + self.T * 4 + self.T * 4 * 16 * 8) + bt
 
     @property
     def step_bytes(self):
@@ -276,6 +291,18 @@ class DecodeBench:
                           init_blocks=spec.init_blocks, local_blocks=spec.local_blocks,
                           spin_limit=1 << 22)
         self.slot = (slot + 1) % 3
+
+    def fused_step(self):
+        """The fused scorer + Top16 select (no score plane), one launch per shard."""
+        icp, spec, ws = self.icp, self.spec, self.ws
+        for rank in range(ws):
+            icp.icp_score_select(self.q, self.shards[rank], self.bt, self.sl, self.nvp,
+                                 self.f_s[rank], self.f_i[rank], self.work, cols=self.cols,
+                                 rank=rank, world_size=ws, page_size=spec.page_size,
+                                 decode_query_len=spec.decode_query_len,
+                                 max_decode_query_len=spec.max_decode_query_len,
+                                 init_blocks=spec.init_blocks, local_blocks=spec.local_blocks,
+                                 errors=self.errors)
 
     def e2e(self, steps, warmup):
         """Same chain with per-step inputs copied from pinned host memory and
@@ -537,6 +564,25 @@ def run_ours(args, spec_name):
         "gpu_launches": bench.launches_per_step * args.steps,
     }
     if spec_name != "select":
+        for _ in range(max(args.warmup, 3)):
+            bench.fused_step()
+        torch.cuda.synchronize()
+        fa, fb = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        fa.record(stream)
+        for _ in range(args.steps):
+            bench.fused_step()
+        fb.record(stream)
+        torch.cuda.synchronize()
+        f_ms = fa.elapsed_time(fb) / args.steps
+        f_bytes = bench.fused_bytes
+        line["fused_score_select"] = {
+            "ms_per_step": round(f_ms, 5),
+            "GB/s": round(f_bytes / (f_ms / 1e3) / 1e9, 1),
+            "frac_of_peak": round(f_bytes / (f_ms / 1e3) / 1e9 / peak, 4),
+            "rows_per_s": round(bench.rows / (f_ms / 1e3), 1),
+            "launches_per_step": bench.ws,
+            "note": "icp_score_select: scorer bytes without the plane write, plus Top16 "
+                    "output; no score plane"}
         e2e_s, bi, bo = bench.e2e(args.steps, max(args.warmup, 3))
         e2e_s = max_over_ranks(dist, e2e_s, device)
         line["e2e"] = {"value": round(n * bench.step_bytes / e2e_s / 1e9, 2), "unit": UNIT,

@@ -157,6 +157,39 @@ int icp_merge(int32_t *recv, const int32_t *num_valid_pages, int T, int slot, in
               int64_t spin_limit, int32_t *errors, float *out_scores, int32_t *out_ids,
               void *stream);
 
+/*
+ * Workspace bytes icp_score_select needs for `batch` requests of
+ * decode_query_len tokens (per-request partial Top16 lists and counters).
+ * Returns 0 for invalid arguments.  Host only.
+ */
+size_t icp_score_select_workspace_bytes(int batch, int decode_query_len);
+
+/*
+ * Fused scorer + Top16 select (the fused decode chain of
+ * prepare_msa_icp_indexer, decode(pool=...), whose scorer feeds the select
+ * directly and leaves no score plane).  Arguments as icp_score plus
+ * num_valid_pages / init_blocks / local_blocks as icp_top16_select (global
+ * id of column c = c * index_scale + index_offset, with index_scale 2 and
+ * index_offset rank * 2 / world_size for page_size 256 with world_size 2 or 4,
+ * else 1 and 0).  The output equals icp_score followed by icp_top16_select
+ * on a plane of width cols, bit for bit, whenever num_valid_pages[t] does not
+ * exceed the number of B128 blocks of the token's request (as in decode,
+ * where it counts the blocks holding visible keys); ids beyond the request's
+ * columns are treated as absent.
+ *   workspace  device buffer of icp_score_select_workspace_bytes(batch, dql)
+ *              bytes, 256-byte aligned; its contents need no initialisation
+ *              and are scratch between calls.  Calls that share a workspace
+ *              must not overlap on the GPU.
+ *   out_scores float32 [batch * dql, 4, 16], out_ids int32 [batch * dql, 4, 16].
+ */
+int icp_score_select(const uint8_t *index_q, const uint8_t *index_k, int64_t num_pages,
+                     const int32_t *block_table, int64_t block_table_stride,
+                     const int32_t *seq_lens, int batch, int cols, int rank, int world_size,
+                     int page_size, int decode_query_len, int max_decode_query_len,
+                     const int32_t *num_valid_pages, int init_blocks, int local_blocks,
+                     void *workspace, size_t workspace_bytes, float *out_scores,
+                     int32_t *out_ids, int32_t *errors, void *stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -161,6 +161,7 @@ int icp_score(const uint8_t *index_q, const uint8_t *index_k, int64_t num_pages,
   if (st != ICP_OK) return st;
 
   icp::ScoreArgs a;
+  memset(&a, 0, sizeof(a));
   a.block_table = block_table;
   a.bt_stride = block_table_stride;
   a.seq_lens = seq_lens;
@@ -274,6 +275,71 @@ int icp_merge(int32_t *recv, const int32_t *num_valid_pages, int T, int slot, in
   a.out_scores = out_scores;
   a.out_ids = out_ids;
   return to_status(icp::launch_merge(a, static_cast<cudaStream_t>(stream)));
+}
+
+size_t icp_score_select_workspace_bytes(int batch, int decode_query_len) {
+  if (batch < 0 || batch > ICP_MAX_BATCH || decode_query_len < 1 || decode_query_len > 8)
+    return 0;
+  return icp::fused_workspace_bytes(batch, decode_query_len);
+}
+
+int icp_score_select(const uint8_t *index_q, const uint8_t *index_k, int64_t num_pages,
+                     const int32_t *block_table, int64_t block_table_stride,
+                     const int32_t *seq_lens, int batch, int cols, int rank, int world_size,
+                     int page_size, int decode_query_len, int max_decode_query_len,
+                     const int32_t *num_valid_pages, int init_blocks, int local_blocks,
+                     void *workspace, size_t workspace_bytes, float *out_scores,
+                     int32_t *out_ids, int32_t *errors, void *stream) {
+  int st = check_score_args(index_q, index_k, num_pages, block_table, block_table_stride,
+                            seq_lens, batch, cols, rank, world_size, page_size, decode_query_len,
+                            max_decode_query_len);
+  if (st != ICP_OK) return st;
+  if (init_blocks < 0 || local_blocks < 0 || init_blocks + local_blocks > ICP_TOPK)
+    return ICP_ERR_INVALID_ARG;
+  if (batch == 0) return ICP_OK;
+  if (!num_valid_pages || !out_scores || !out_ids || !workspace) return ICP_ERR_INVALID_ARG;
+  if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return ICP_ERR_INVALID_ARG;
+  if (workspace_bytes < icp::fused_workspace_bytes(batch, decode_query_len))
+    return ICP_ERR_INVALID_ARG;
+  int dev = 0, sms = 0;
+  st = current_device(&dev, &sms);
+  if (st != ICP_OK) return st;
+
+  icp::ScoreArgs a;
+  memset(&a, 0, sizeof(a));
+  a.block_table = block_table;
+  a.bt_stride = block_table_stride;
+  a.seq_lens = seq_lens;
+  a.errors = errors;
+  a.batch = batch;
+  a.cols = cols;
+  a.rank = rank;
+  a.world_size = world_size;
+  a.page_size = page_size;
+  a.dql = decode_query_len;
+  a.g = make_geom(page_size, world_size, decode_query_len);
+  a.nvp = num_valid_pages;
+  a.init_blocks = init_blocks;
+  a.local_blocks = local_blocks;
+  // global id of column c (msa_icp_decode_index_score_sharded: P256 sharded
+  // columns are local pages of global block 2 c + rank * 2 // world_size)
+  const bool local_pages = page_size == 256 && world_size > 1;
+  a.index_scale = local_pages ? 2 : 1;
+  a.index_offset = local_pages ? rank * 2 / world_size : 0;
+  a.out_scores = out_scores;
+  a.out_ids = out_ids;
+  const size_t counters = ((size_t)batch * 16 + 255) / 256 * 256;  // per-request info
+  a.ws_counters = static_cast<int32_t *>(workspace);
+  a.ws_records = static_cast<uint8_t *>(workspace) + counters;
+
+  CUtensorMap tmk, tmq;
+  st = encode_rows(&tmk, index_k, (uint64_t)num_pages * a.g.rows_per_page, (uint32_t)a.g.R);
+  if (st != ICP_OK) return st;
+  st = encode_rows(&tmq, index_q, (uint64_t)batch * decode_query_len * ICP_HEADS,
+                   (uint32_t)a.g.nq);
+  if (st != ICP_OK) return st;
+  return to_status(
+      icp::launch_score_select(tmk, tmq, a, sms, static_cast<cudaStream_t>(stream)));
 }
 
 }  // extern "C"

@@ -262,4 +262,38 @@ __device__ __forceinline__ uint64_t warp_max_key(uint64_t k) {
   return ((uint64_t)mhi << 32) | mlo;
 }
 
+// ------------------------------------------------------------- Top16 rule
+constexpr int kTopK = 16;
+
+// Forced ids of a row: every valid id when num_valid_pages <= 16, else the
+// first init and the last local blocks below num_valid_pages.
+__device__ __forceinline__ bool forced_id(int id, int nvp, int init, int local) {
+  return nvp <= kTopK || id < init || id >= nvp - local;
+}
+
+// Sorts the n <= 16 entries held by lanes 0..n-1 by id and writes the 16
+// output slots: lane r < 16 ends up owning slot r.
+__device__ __forceinline__ void sort_by_id_16(int lane, int n, int my_id, float my_sc, int &out_id,
+                                              float &out_sc) {
+  int rank = 0;
+#pragma unroll
+  for (int j = 0; j < kTopK; ++j) {
+    const int oid = __shfl_sync(0xFFFFFFFFu, my_id, j);
+    if (j < n && lane < n && oid < my_id) ++rank;
+  }
+  // scatter through shuffles: slot r takes the entry of rank r
+  out_id = -1;
+  out_sc = -INFINITY;
+#pragma unroll
+  for (int j = 0; j < kTopK; ++j) {
+    const int r = __shfl_sync(0xFFFFFFFFu, rank, j);
+    const int id = __shfl_sync(0xFFFFFFFFu, my_id, j);
+    const float sc = __shfl_sync(0xFFFFFFFFu, my_sc, j);
+    if (j < n && r == lane) {
+      out_id = id;
+      out_sc = sc;
+    }
+  }
+}
+
 }  // namespace icp

@@ -17,14 +17,26 @@ struct ScoreGeom {
   int nq;             // query rows staged per request: 32 (4 * dql of them are used)
 };
 
+// The fused scorer + select covers at most this many CTAs (workspace sizing).
+constexpr int kFusedMaxGrid = 160;
+// Largest batch a scoring launch accepts (shared-memory sizing).
+constexpr int kMaxBatchDevice = 4096;
+
 struct ScoreArgs {
   const int32_t *block_table;
   int64_t bt_stride;
   const int32_t *seq_lens;
-  float *score_out;
+  float *score_out;  // plane (icp_score only)
   int32_t *errors;
   int batch, cols, rank, world_size, page_size, dql;
   ScoreGeom g;
+  // fused scorer + select only
+  const int32_t *nvp;
+  int init_blocks, local_blocks, index_scale, index_offset;
+  float *out_scores;
+  int32_t *out_ids;
+  int32_t *ws_counters;  // [batch] 16-byte records: where each request's lists are
+  void *ws_records;      // partial Top16 lists
 };
 
 struct SelectArgs {
@@ -57,6 +69,10 @@ cudaError_t launch_score(const CUtensorMap &tmk, const CUtensorMap &tmq, const S
                          int grid, cudaStream_t stream);
 size_t score_smem_bytes(int batch);
 cudaError_t score_prepare(int device);  // one-time per-device kernel attributes
+
+size_t fused_workspace_bytes(int batch, int dql);
+cudaError_t launch_score_select(const CUtensorMap &tmk, const CUtensorMap &tmq, ScoreArgs a,
+                                int grid, cudaStream_t stream);
 
 cudaError_t launch_select(const SelectArgs &a, bool publish, cudaStream_t stream);
 cudaError_t launch_merge(const MergeArgs &a, cudaStream_t stream);

@@ -1,11 +1,15 @@
-// icp_score.cu - decode index scorer (msa_icp_decode_index_score_sharded).
+// icp_score.cu - decode index scorer (msa_icp_decode_index_score_sharded) and
+// the fused scorer + Top16 select (prepare_msa_icp_indexer, decode(pool=...),
+// whose fused scorer leaves no score plane).
 //
-// What it computes: for every request b, token j (position
+// What the scorer computes: for every request b, token j (position
 // seq_len_b - dql + j), head h and plane column c of the request,
 //   score_out[t][h][c] = max over the column's keys at positions <= the
 //                        token's position of dot(deq(q[t,h,:]), deq(k[key,:]))
 // (-inf when no key is visible), for c < round_up(columns, 4); the other
-// columns are not written.
+// columns are not written.  The fused variant computes the same column
+// values and applies the Top16 rule of msa_icp_topk_select_publish to them
+// directly.
 //
 // How (one persistent CTA per SM, 192 threads, warp-specialised):
 //   warp 0     TMA producer: streams the 128-row K tiles of the CTA's share of
@@ -20,9 +24,12 @@
 //   warps 2-5  epilogue: tile i belongs to epilogue warp i % 4, which reads
 //              its lane quarter of the accumulator (thread = query row,
 //              registers = the tile's 128 key scores), applies the causal
-//              mask, folds each column's keys with a register max tree and
-//              stores one plane value per (query row, column).  No shuffles
-//              and no cross-warp synchronisation are needed.
+//              mask and folds each column's keys with a register max tree.
+//              Scorer: one plane store per (query row, column).
+//              Fused: the column value goes into the row's running Top16
+//              (forced ids kept aside); at the end of each request segment
+//              every epilogue warp writes its lists to the workspace, and the
+//              last CTA to finish a request merges all lists of that request.
 // The tiles of all requests form one list that is cut into gridDim.x equal
 // contiguous ranges, so every CTA streams the same number of K bytes.
 // Products of two e4m3 values are exact in fp32; the MMA sums 128 of them in
@@ -49,7 +56,16 @@ constexpr uint32_t kOffStages = 0;
 constexpr uint32_t kOffQ = kOffStages + kStages * kTileBytes;
 constexpr uint32_t kOffBars = kOffQ + 2 * kQBytes;
 constexpr uint32_t kOffMisc = kOffBars + ((kNumBars * 8 + 127) / 128) * 128;
-constexpr uint32_t kOffPrefix = kOffMisc + 128;
+constexpr uint32_t kOffLists = kOffMisc + 128;  // fused only
+// fused epilogue: per warp 16 list keys x 32 lanes (u64) + 16 forced (id, score) x 32 lanes
+constexpr uint32_t kWarpListBytes = 16 * 32 * 8 + 16 * 32 * 8;
+constexpr uint32_t kListBytes = 4 * kWarpListBytes;   // 32 KB
+constexpr uint32_t kFusedExtra = kListBytes;
+
+template <bool FUSED>
+struct PrefixOffset {
+  static constexpr uint32_t value = FUSED ? kOffLists + kFusedExtra : kOffLists;
+};
 
 __device__ __forceinline__ int units_of(int seq_len, int page_size, int split) {
   const int u = split ? 128 : page_size;
@@ -63,8 +79,7 @@ struct SegmentWalker {
   int g, g1, b;
   __device__ SegmentWalker(const int *p, int nb, int g0_, int g1_)
       : prefix(p), batch(nb), g(g0_), g1(g1_), b(0) {
-    // largest b with prefix[b] <= g0
-    int lo = 0, hi = nb;  // invariant: prefix[lo] <= g0
+    int lo = 0, hi = nb;  // largest lo with prefix[lo] <= g0
     while (lo < hi) {
       const int mid = (lo + hi + 1) >> 1;
       if (prefix[mid] <= g) lo = mid; else hi = mid - 1;
@@ -88,14 +103,65 @@ struct SegmentWalker {
 __device__ __forceinline__ int page_slot_of(int c, int split) { return split ? (c >> 1) : c; }
 __device__ __forceinline__ int row_off_of(int c, int split) { return split ? (c & 1) * 128 : 0; }
 
+// ------------------------------------------------------------ fused state
+// Workspace record of one (partial list, query row), 288 bytes:
+//   u64 keys[16]   best non-forced entries seen (unsorted, 0 = empty)
+//   u64 max        largest of keys (0 = none)
+//   i32 fcount     forced entries that follow
+//   i32 fid[16], f32 fsc[16]
+struct alignas(16) PartialRec {
+  unsigned long long keys[16];
+  unsigned long long max;
+  int fcount;
+  int pad_;
+  int fid[16];
+  float fsc[16];
+  int pad2_[4];
+};
+static_assert(sizeof(PartialRec) == 288, "record layout");
+
+// Per-lane running Top16 of one query row over the columns a warp has seen.
+struct LaneTop {
+  int cnt;                 // list entries used (<= 16)
+  unsigned long long kmin; // smallest listed key once the list is full
+  int fcnt;                // forced entries kept
+  int nvp;                 // the row's num_valid_pages
+};
+
+__device__ __forceinline__ void lane_insert(LaneTop &s, unsigned long long *lk, int lane,
+                                            unsigned long long key) {
+  if (s.cnt < kTopK) {
+    lk[s.cnt * 32 + lane] = key;
+    if (++s.cnt == kTopK) {
+      unsigned long long mn = lk[lane];
+      for (int j = 1; j < kTopK; ++j) mn = min(mn, lk[j * 32 + lane]);
+      s.kmin = mn;
+    }
+  } else if (key > s.kmin) {
+    unsigned long long mn = ~0ull;
+    bool replaced = false;
+    for (int j = 0; j < kTopK; ++j) {
+      unsigned long long x = lk[j * 32 + lane];
+      if (!replaced && x == s.kmin) {
+        lk[j * 32 + lane] = key;
+        x = key;
+        replaced = true;
+      }
+      mn = min(mn, x);
+    }
+    s.kmin = mn;
+  }
+}
+
 // Epilogue of one tile for the warp that owns it.  taddr addresses the
 // warp's lane quarter of the tile's accumulator: lane l holds query row l
 // (row = token j * 4 + head), columns 0..127 hold the tile's keys in order.
 // R keys feed one plane column, so the tile covers 128 / R columns.
-template <int R>
+template <int R, bool FUSED>
 __device__ __forceinline__ void epilogue_tile(const ScoreArgs &a, uint32_t taddr, int lane, int b,
                                               int tl, int nunits, int seq_len, uint32_t tempty,
-                                              volatile int *abort_flag) {
+                                              LaneTop &lt, unsigned long long *lk, int *lfid,
+                                              float *lfsc) {
   constexpr int CPT = 128 / R;
   float v[128];
 #pragma unroll
@@ -105,7 +171,6 @@ __device__ __forceinline__ void epilogue_tile(const ScoreArgs &a, uint32_t taddr
   tc_fence_before();
   __syncwarp();
   if (lane == 0) mbar_arrive(tempty);
-  (void)abort_flag;
 
   const ScoreGeom &g = a.g;
   const long long pfirst = (long long)seq_len - a.dql;  // position of token 0
@@ -129,13 +194,217 @@ __device__ __forceinline__ void epilogue_tile(const ScoreArgs &a, uint32_t taddr
 #pragma unroll
       for (int i = 0; i < st; ++i) vc[i] = fmaxf(vc[i], vc[i + st]);
     }
+    const float val = vc[0] + 0.0f;  // + 0 folds -0 onto +0
     if (row_ok && c < a.cols) {
-      const long long prow = (long long)b * a.dql * 4 + lane;
-      a.score_out[prow * a.cols + c] = vc[0] + 0.0f;  // + 0 folds -0 onto +0
+      if constexpr (!FUSED) {
+        const long long prow = (long long)b * a.dql * 4 + lane;
+        a.score_out[prow * a.cols + c] = val;
+      } else {
+        const int id = c * a.index_scale + a.index_offset;
+        if (id < lt.nvp) {
+          if (forced_id(id, lt.nvp, a.init_blocks, a.local_blocks)) {
+            if (lt.fcnt < kTopK) {
+              lfid[lt.fcnt * 32 + lane] = id;
+              lfsc[lt.fcnt * 32 + lane] = val;
+              ++lt.fcnt;
+            }
+          } else {
+            lane_insert(lt, lk, lane, make_key(val, id));
+          }
+        }
+      }
     }
   }
 }
 
+__device__ __forceinline__ PartialRec *partial_rec(const ScoreArgs &a, int pidx, int row) {
+  return reinterpret_cast<PartialRec *>(a.ws_records) + (size_t)pidx * (4 * a.dql) + row;
+}
+
+// Index of the CTA whose tile range contains tile x.
+__device__ __forceinline__ int cta_of(long long total, int grid, long long x) {
+  int lo = 0, hi = grid - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (total * mid / grid <= x) lo = mid; else hi = mid - 1;
+  }
+  return lo;
+}
+
+// Per-request facts the fused scorer leaves for the merge kernel.
+struct alignas(16) ReqInfo {
+  int i0, i1;   // first and last CTA whose tile range covers the request (i1 < i0: none)
+  int total;    // tiles of the whole launch
+  int nunits;   // plane columns of the request
+};
+
+// Final Top16 of one (token, head) row from the partial lists that the
+// epilogue warps of every CTA covering the token's request wrote, plus the
+// request's padding columns [units, round_up(units, 4)), which hold -inf.
+// One warp per row; the lists holding the m largest entries are found from
+// the lists' maxima (tau = the m-th largest maximum), so at most m * 16
+// candidates are read.
+__global__ void __launch_bounds__(128)
+fused_merge_kernel(const ScoreArgs a, const ReqInfo *info, int grid_a) {
+  __shared__ unsigned long long s_mx[4][4 * kFusedMaxGrid];
+  __shared__ unsigned long long s_cand[4][kTopK * 16 + 8];
+  __shared__ int s_fid[4][kTopK];
+  __shared__ float s_fsc[4][kTopK];
+  // wait for the fused scorer (programmatic dependent launch)
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int row = blockIdx.x * 4 + warp;   // t * 4 + h
+  const int T = a.batch * a.dql;
+  if (row >= T * 4) return;
+  const int t = row >> 2, h = row & 3;
+  const int b = t / a.dql;
+  const int r = (t - b * a.dql) * 4 + h;   // query row inside the request
+  unsigned long long *mx = s_mx[warp];
+  unsigned long long *cand = s_cand[warp];
+  int *fbuf_id = s_fid[warp];
+  float *fbuf_sc = s_fsc[warp];
+
+  const ReqInfo in = info[b];
+  const long long total = in.total;
+  const int G = grid_a;
+  const int i0 = in.i0;
+  const int P = in.i1 >= in.i0 ? (in.i1 - in.i0 + 1) * 4 : 0;
+  const int nunits = in.nunits;
+  const int wcols = min((nunits + 3) & ~3, a.cols);
+  const int nvp = a.nvp[t];
+  auto pidx_of = [&](int k) { return (i0 + (k >> 2) + b) * 4 + (k & 3); };
+  // a CTA in [i0, i1] with an empty tile range never wrote lists for b
+  auto part_valid = [&](int k) {
+    const int i = i0 + (k >> 2);
+    return total * i / G < total * (i + 1) / G;
+  };
+
+  // forced entries: each forced id was seen by exactly one partial list
+  int nf = 0;
+  for (int k0 = 0; k0 < P; k0 += 32) {
+    const int k = k0 + lane;
+    int fc = 0;
+    if (k < P && part_valid(k)) fc = __ldcg(&partial_rec(a, pidx_of(k), r)->fcount);
+    unsigned msk = __ballot_sync(0xFFFFFFFFu, fc > 0);
+    while (msk) {
+      const int src = __ffs(msk) - 1;
+      msk &= msk - 1;
+      const int cnt = __shfl_sync(0xFFFFFFFFu, fc, src);
+      const PartialRec *pr = partial_rec(a, pidx_of(k0 + src), r);
+      if (lane < cnt && nf + lane < kTopK) {
+        fbuf_id[nf + lane] = __ldcg(&pr->fid[lane]);
+        fbuf_sc[nf + lane] = __ldcg(&pr->fsc[lane]);
+      }
+      nf = min(nf + cnt, kTopK);
+    }
+  }
+  for (int c = nunits; c < wcols; ++c) {
+    const int id = c * a.index_scale + a.index_offset;
+    if (id < nvp && forced_id(id, nvp, a.init_blocks, a.local_blocks) && nf < kTopK) {
+      if (lane == 0) {
+        fbuf_id[nf] = id;
+        fbuf_sc[nf] = -INFINITY;
+      }
+      ++nf;
+    }
+  }
+  const int m = kTopK - nf;
+  // tau = m-th largest list maximum; the lists holding keys >= tau are
+  // exactly the round winners
+  for (int k = lane; k < P; k += 32)
+    mx[k] = part_valid(k) ? __ldcg(&partial_rec(a, pidx_of(k), r)->max) : 0ull;
+  __syncwarp();
+  unsigned long long prev = ~0ull, tau = 0;
+  int found = 0, my_winner = -1;
+  for (int rd = 0; rd < m; ++rd) {
+    unsigned long long local = 0;
+    int lidx = -1;
+    for (int k = lane; k < P; k += 32) {
+      const unsigned long long x = mx[k];
+      if (x < prev && x > local) {
+        local = x;
+        lidx = k;
+      }
+    }
+    const unsigned long long w = warp_max_key(local);
+    if (w == 0) break;
+    const int src = __ffs(__ballot_sync(0xFFFFFFFFu, local == w)) - 1;
+    const int widx = __shfl_sync(0xFFFFFFFFu, lidx, src);
+    if (lane == rd) my_winner = widx;
+    prev = w;
+    tau = w;
+    ++found;
+  }
+  if (found < m) tau = 1;  // fewer than m lists hold entries: take all of them
+  int nc = 0;
+  for (int w0 = 0; w0 < found; w0 += 2) {
+    const int wi = w0 + (lane >> 4);
+    const int k = __shfl_sync(0xFFFFFFFFu, my_winner, wi & 31);
+    unsigned long long key = 0;
+    if (wi < found) key = __ldcg(&partial_rec(a, pidx_of(k), r)->keys[lane & 15]);
+    const bool keep = key != 0 && key >= tau;
+    const unsigned bal = __ballot_sync(0xFFFFFFFFu, keep);
+    if (keep) cand[nc + __popc(bal & ((1u << lane) - 1u))] = key;
+    nc += __popc(bal);
+  }
+  for (int c = nunits; c < wcols; ++c) {
+    const int id = c * a.index_scale + a.index_offset;
+    if (id < nvp && !forced_id(id, nvp, a.init_blocks, a.local_blocks)) {
+      const unsigned long long key = make_key(-INFINITY, id);
+      if (key >= tau) {
+        if (lane == 0) cand[nc] = key;
+        ++nc;
+      }
+    }
+  }
+  __syncwarp();
+  // the m largest candidates; lane nf + rd receives the rd-th
+  unsigned long long cl[9];
+  unsigned long long lmax = 0;
+#pragma unroll
+  for (int j = 0; j < 9; ++j) {
+    const int k = lane + 32 * j;
+    cl[j] = (k < nc) ? cand[k] : 0ull;
+    lmax = cl[j] > lmax ? cl[j] : lmax;
+  }
+  unsigned long long mine = 0;
+  int nch = 0;
+  for (int rd = 0; rd < m; ++rd) {
+    const unsigned long long w = warp_max_key(lmax);
+    if (w == 0) break;
+    if (lane == nf + rd) mine = w;
+    ++nch;
+    if (lmax == w) {
+      lmax = 0;
+#pragma unroll
+      for (int j = 0; j < 9; ++j) {
+        if (cl[j] == w) cl[j] = 0;
+        lmax = cl[j] > lmax ? cl[j] : lmax;
+      }
+    }
+  }
+  const int n = nf + nch;
+  int my_id = 0x7FFFFFFF;
+  float my_sc = -INFINITY;
+  if (lane < nf) {
+    my_id = fbuf_id[lane];
+    my_sc = fbuf_sc[lane];
+  } else if (lane < n) {
+    my_id = key_id(mine);
+    my_sc = unord_float((uint32_t)(mine >> 32));
+  }
+  int out_id;
+  float out_sc;
+  sort_by_id_16(lane, n, my_id, my_sc, out_id, out_sc);
+  if (lane < kTopK) {
+    const long long o = (long long)row * kTopK + lane;
+    a.out_scores[o] = out_sc;
+    a.out_ids[o] = out_id;
+  }
+}
+
+template <bool FUSED>
 __global__ void __launch_bounds__(kThreads, 1)
 score_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmq,
              const ScoreArgs a) {
@@ -156,8 +425,9 @@ score_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CU
   auto bar_qempty = [&](int i) { return sb + kOffBars + 8u * (2 * kStages + 2 * kAcc + 2 + i); };
   const uint32_t bar_done = sb + kOffBars + 8u * (2 * kStages + 2 * kAcc + 4);
 
-  volatile int *misc = reinterpret_cast<volatile int *>(gb + kOffMisc);  // [0] tmem, [1] abort
-  int *prefix = reinterpret_cast<int *>(gb + kOffPrefix);
+  // [0] TMEM base, [1] abort flag
+  volatile int *misc = reinterpret_cast<volatile int *>(gb + kOffMisc);
+  int *prefix = reinterpret_cast<int *>(gb + PrefixOffset<FUSED>::value);
   int *partial = prefix + a.batch + 1;  // kThreads scratch ints
 
   if (threadIdx.x == 0) {
@@ -226,7 +496,7 @@ score_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CU
     const uint64_t pol = policy_evict_first();
     int stage = 0;
     uint32_t sphase = 0;
-    uint32_t qph[2] = {0u, 0u};
+    uint32_t qph0 = 0, qph1 = 0;
     int qslot = 0;
     long long issued = 0;
     int last_qslot = -1;
@@ -235,7 +505,8 @@ score_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CU
     bool ok = true;
     while (ok && walk.next(b, t0, t1)) {
       const int nunits = units_of(a.seq_lens[b], a.page_size, g.split);
-      if (lane == 0) ok = mbar_wait(bar_qempty(qslot), qph[qslot] ^ 1u, abort_flag);
+      const uint32_t qph = qslot ? qph1 : qph0;
+      if (lane == 0) ok = mbar_wait(bar_qempty(qslot), qph ^ 1u, abort_flag);
       ok = __shfl_sync(0xFFFFFFFFu, ok, 0) != 0;
       if (!ok) break;
       if (lane == 0) {
@@ -245,7 +516,7 @@ score_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CU
                       bar_qfull(qslot));
       }
       last_qslot = qslot;
-      qph[qslot] ^= 1u;
+      if (qslot) qph1 ^= 1u; else qph0 ^= 1u;
       qslot ^= 1;
       const int cbeg = t0 * g.cpt;
       const int cend = min(t1 * g.cpt, nunits);
@@ -264,16 +535,18 @@ score_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CU
         if (lane == 0) ok = mbar_wait(bar_empty(stage), sphase ^ 1u, abort_flag);
         ok = __shfl_sync(0xFFFFFFFFu, ok, 0) != 0;
         if (!ok) break;
-        int pages[4];
-#pragma unroll
-        for (int k = 0; k < 4; ++k) pages[k] = __shfl_sync(0xFFFFFFFFu, pg_cur, (c0 - grp + k) & 31);
+        const int p0 = __shfl_sync(0xFFFFFFFFu, pg_cur, (c0 - grp) & 31);
+        const int p1 = __shfl_sync(0xFFFFFFFFu, pg_cur, (c0 - grp + 1) & 31);
+        const int p2 = __shfl_sync(0xFFFFFFFFu, pg_cur, (c0 - grp + 2) & 31);
+        const int p3 = __shfl_sync(0xFFFFFFFFu, pg_cur, (c0 - grp + 3) & 31);
         if (lane == 0) {
           const uint32_t bar = bar_full(stage);
           mbar_arrive_expect_tx(bar, (uint32_t)(ncol * g.R * 128));
           const uint32_t dst = sb + kOffStages + stage * kTileBytes;
           for (int k = 0; k < ncol; ++k) {
             const int c = c0 + k;
-            const int y = pages[k] * g.rows_per_page + row_off_of(c, g.split);
+            const int pg = k == 0 ? p0 : (k == 1 ? p1 : (k == 2 ? p2 : p3));
+            const int y = pg * g.rows_per_page + row_off_of(c, g.split);
             tma_load_2d_hint(dst + k * g.R * 128, &tmk, 0, y, bar, pol);
           }
         }
@@ -290,20 +563,21 @@ score_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CU
       const long long first = issued > kStages ? issued - kStages : 0;
       for (long long n = first; n < issued; ++n)
         mbar_wait_drain(bar_full((int)(n % kStages)), (uint32_t)((n / kStages) & 1));
-      if (last_qslot >= 0) mbar_wait_drain(bar_qfull(last_qslot), qph[last_qslot] ^ 1u);
+      if (last_qslot >= 0)
+        mbar_wait_drain(bar_qfull(last_qslot), (last_qslot ? qph1 : qph0) ^ 1u);
     }
   } else if (warp == 1) {
     // ---------------------------------------------------------- MMA issuer
     const uint32_t idesc = idesc_f8_f32(128, (int)kAccCols);
     int stage = 0, acc = 0;
     uint32_t sphase = 0, aphase = 0;
-    uint32_t qph[2] = {0u, 0u};
+    uint32_t qph0 = 0, qph1 = 0;
     int qslot = 0;
     SegmentWalker walk(prefix, a.batch, g0, g1);
     int b, t0, t1;
     bool ok = true;
     while (ok && walk.next(b, t0, t1)) {
-      if (lane == 0) ok = mbar_wait(bar_qfull(qslot), qph[qslot], abort_flag);
+      if (lane == 0) ok = mbar_wait(bar_qfull(qslot), qslot ? qph1 : qph0, abort_flag);
       ok = __shfl_sync(0xFFFFFFFFu, ok, 0) != 0;
       if (!ok) break;
       const uint32_t qaddr = sb + kOffQ + qslot * kQBytes;
@@ -337,7 +611,7 @@ score_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CU
       if (!ok) break;
       if (lane == 0) mma_commit(bar_qempty(qslot));
       __syncwarp();
-      qph[qslot] ^= 1u;
+      if (qslot) qph1 ^= 1u; else qph0 ^= 1u;
       qslot ^= 1;
     }
     if (*abort_flag && lane == 0) {
@@ -350,42 +624,103 @@ score_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CU
     const int q = warp & 3;      // TMEM lane quarter this warp may access
     const int e = warp - 2;      // owns tiles i with i % 4 == e, accumulator e
     const int et = threadIdx.x - 64;
-    // padding columns [units, round_up(units, 4)) of the requests this CTA owns
     for (int b = blockIdx.x; b < a.batch; b += gridDim.x) {
       const int u = units_of(a.seq_lens[b], a.page_size, g.split);
       const int wcols = (u + 3) & ~3;
       if (wcols > a.cols && et == 0 && a.errors) atomicAdd(a.errors, 1);  // plane too narrow
-      const int npad = min(wcols, a.cols) - min(u, a.cols);
       const int rows = 4 * a.dql;
-      for (int k = et; k < npad * rows; k += 128) {
-        const int r = k / npad, c = u + k % npad;
-        a.score_out[((long long)b * a.dql * 4 + r) * a.cols + c] = -INFINITY;
+      if constexpr (!FUSED) {
+        // padding columns [units, round_up(units, 4)) of the requests this CTA owns
+        const int npad = min(wcols, a.cols) - min(u, a.cols);
+        for (int k = et; k < npad * rows; k += 128) {
+          const int r = k / npad, c = u + k % npad;
+          a.score_out[((long long)b * a.dql * 4 + r) * a.cols + c] = -INFINITY;
+        }
+      } else if (et == 0) {
+        // where the merge kernel finds this request's partial lists
+        ReqInfo in;
+        in.total = (int)total;
+        in.nunits = u;
+        if (prefix[b + 1] > prefix[b]) {
+          in.i0 = cta_of(total, gridDim.x, prefix[b]);
+          in.i1 = cta_of(total, gridDim.x, prefix[b + 1] - 1);
+        } else {
+          in.i0 = 0;
+          in.i1 = -1;
+        }
+        reinterpret_cast<ReqInfo *>(a.ws_counters)[b] = in;
+        (void)rows;
       }
     }
     uint32_t aphase = 0;
     int idx = 0;
     const uint32_t taddr = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)e * kAccCols;
+    unsigned long long *lk = nullptr;
+    int *lfid = nullptr;
+    float *lfsc = nullptr;
+    if constexpr (FUSED) {
+      uint8_t *wl = gb + kOffLists + e * kWarpListBytes;
+      lk = reinterpret_cast<unsigned long long *>(wl);
+      lfid = reinterpret_cast<int *>(wl + 16 * 32 * 8);
+      lfsc = reinterpret_cast<float *>(wl + 16 * 32 * 8 + 16 * 32 * 4);
+    }
     SegmentWalker walk(prefix, a.batch, g0, g1);
     int b, t0, t1;
     bool ok = true;
-    while (ok && walk.next(b, t0, t1)) {
+    while (walk.next(b, t0, t1)) {
+      if (!FUSED && !ok) break;
       const int seq_len = a.seq_lens[b];
       const int nunits = units_of(seq_len, a.page_size, g.split);
+      LaneTop lt;
+      lt.cnt = 0;
+      lt.kmin = 0;
+      lt.fcnt = 0;
+      lt.nvp = 0;
+      if constexpr (FUSED) {
+        if (lane < 4 * a.dql) lt.nvp = a.nvp[b * a.dql + (lane >> 2)];
+#pragma unroll
+        for (int j = 0; j < kTopK; ++j) lk[j * 32 + lane] = 0ull;
+      }
       // first tile of this segment that belongs to this warp
       int tl = t0 + ((e - idx) % 4 + 4) % 4;
-      idx += t1 - t0;
-      for (; tl < t1; tl += 4) {
+      const int seg_tiles = t1 - t0;
+      idx += seg_tiles;
+      for (; ok && tl < t1; tl += 4) {
         if (lane == 0) ok = mbar_wait(bar_tfull(e), aphase, abort_flag);
         ok = __shfl_sync(0xFFFFFFFFu, ok, 0) != 0;
         if (!ok) break;
         tc_fence_after();
         if (g.R == 128)
-          epilogue_tile<128>(a, taddr, lane, b, tl, nunits, seq_len, bar_tempty(e), abort_flag);
+          epilogue_tile<128, FUSED>(a, taddr, lane, b, tl, nunits, seq_len, bar_tempty(e), lt,
+                                    lk, lfid, lfsc);
         else if (g.R == 64)
-          epilogue_tile<64>(a, taddr, lane, b, tl, nunits, seq_len, bar_tempty(e), abort_flag);
+          epilogue_tile<64, FUSED>(a, taddr, lane, b, tl, nunits, seq_len, bar_tempty(e), lt,
+                                   lk, lfid, lfsc);
         else
-          epilogue_tile<32>(a, taddr, lane, b, tl, nunits, seq_len, bar_tempty(e), abort_flag);
+          epilogue_tile<32, FUSED>(a, taddr, lane, b, tl, nunits, seq_len, bar_tempty(e), lt,
+                                   lk, lfid, lfsc);
         aphase ^= 1u;
+      }
+      if constexpr (FUSED) {
+        // publish this warp's lists of the segment, then count the segment's
+        // tiles; the CTA that completes the request merges it
+        const int pidx = (blockIdx.x + b) * 4 + e;
+        if (lane < 4 * a.dql) {
+          PartialRec *pr = partial_rec(a, pidx, lane);
+          unsigned long long mxk = 0;
+#pragma unroll
+          for (int j = 0; j < kTopK; ++j) {
+            const unsigned long long x = lk[j * 32 + lane];
+            pr->keys[j] = x;
+            mxk = x > mxk ? x : mxk;
+          }
+          pr->max = mxk;
+          pr->fcount = lt.fcnt;
+          for (int j = 0; j < lt.fcnt; ++j) {
+            pr->fid[j] = lfid[j * 32 + lane];
+            pr->fsc[j] = lfsc[j * 32 + lane];
+          }
+        }
       }
     }
   }
@@ -398,23 +733,59 @@ score_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CU
   if (threadIdx.x == 0 && *abort_flag && a.errors) atomicAdd(a.errors, 1);
 }
 
+template <bool FUSED>
+size_t smem_bytes_for(int batch) {
+  return 1024 + PrefixOffset<FUSED>::value + sizeof(int) * (size_t)(batch + 1 + kThreads);
+}
+
 }  // namespace
 
-size_t score_smem_bytes(int batch) {
-  return 1024 + kOffPrefix + sizeof(int) * (size_t)(batch + 1 + kThreads);
-}
+
+size_t score_smem_bytes(int batch) { return smem_bytes_for<false>(batch); }
 
 cudaError_t score_prepare(int device) {
   (void)device;
-  return cudaFuncSetAttribute(score_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                              (int)score_smem_bytes(4096));
+  cudaError_t e = cudaFuncSetAttribute(score_kernel<false>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       (int)smem_bytes_for<false>(kMaxBatchDevice));
+  if (e != cudaSuccess) return e;
+  return cudaFuncSetAttribute(score_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              (int)smem_bytes_for<true>(kMaxBatchDevice));
 }
 
 cudaError_t launch_score(const CUtensorMap &tmk, const CUtensorMap &tmq, const ScoreArgs &a,
                          int grid, cudaStream_t stream) {
-  const size_t smem = score_smem_bytes(a.batch);
-  score_kernel<<<grid, kThreads, smem, stream>>>(tmk, tmq, a);
+  score_kernel<false><<<grid, kThreads, smem_bytes_for<false>(a.batch), stream>>>(tmk, tmq, a);
   return cudaGetLastError();
+}
+
+size_t fused_workspace_bytes(int batch, int dql) {
+  const size_t counters = ((size_t)batch * sizeof(ReqInfo) + 255) / 256 * 256;
+  const size_t records =
+      (size_t)(kFusedMaxGrid + batch) * 4 * (size_t)(4 * dql) * sizeof(PartialRec);
+  return counters + records;
+}
+
+cudaError_t launch_score_select(const CUtensorMap &tmk, const CUtensorMap &tmq, ScoreArgs a,
+                                int grid, cudaStream_t stream) {
+  grid = grid > kFusedMaxGrid ? kFusedMaxGrid : grid;
+  score_kernel<true><<<grid, kThreads, smem_bytes_for<true>(a.batch), stream>>>(tmk, tmq, a);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  // the merge kernel starts early and waits on griddepcontrol for the scorer
+  const int rows = a.batch * a.dql * 4;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)((rows + 3) / 4));
+  cfg.blockDim = dim3(128);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  const ReqInfo *info = reinterpret_cast<const ReqInfo *>(a.ws_counters);
+  return cudaLaunchKernelEx(&cfg, fused_merge_kernel, a, info, grid);
 }
 
 }  // namespace icp

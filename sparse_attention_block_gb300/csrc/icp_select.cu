@@ -19,12 +19,7 @@
 namespace icp {
 namespace {
 
-constexpr int kTopK = 16;
 constexpr int kRowWords = 33;
-
-__device__ __forceinline__ bool forced_id(int id, int nvp, int init, int local) {
-  return nvp <= kTopK || id < init || id >= nvp - local;
-}
 
 // Bounded poll of a ready flag until it equals `want`.  Returns false after
 // spin_limit polls or kWaitTimeoutNs, whichever comes first.
@@ -35,31 +30,6 @@ __device__ __forceinline__ bool poll_flag(const int *flag, int want, long long s
     if ((it & 255) == 255 && globaltimer_ns() - t0 > kWaitTimeoutNs) return false;
   }
   return false;
-}
-
-// Sorts the n <= 16 entries held by lanes 0..n-1 by id and writes the 16
-// output slots: lane r < 16 ends up owning slot r.
-__device__ __forceinline__ void sort_by_id_16(int lane, int n, int my_id, float my_sc, int &out_id,
-                                              float &out_sc) {
-  int rank = 0;
-#pragma unroll
-  for (int j = 0; j < kTopK; ++j) {
-    const int oid = __shfl_sync(0xFFFFFFFFu, my_id, j);
-    if (j < n && lane < n && oid < my_id) ++rank;
-  }
-  // scatter through shuffles: slot r takes the entry of rank r
-  out_id = -1;
-  out_sc = -INFINITY;
-#pragma unroll
-  for (int j = 0; j < kTopK; ++j) {
-    const int r = __shfl_sync(0xFFFFFFFFu, rank, j);
-    const int id = __shfl_sync(0xFFFFFFFFu, my_id, j);
-    const float sc = __shfl_sync(0xFFFFFFFFu, my_sc, j);
-    if (j < n && r == lane) {
-      out_id = id;
-      out_sc = sc;
-    }
-  }
 }
 
 template <int NT, int EPT, bool PUBLISH>
@@ -273,7 +243,7 @@ __global__ void __launch_bounds__(128) merge_kernel(const MergeArgs a) {
     for (int s = 0; s < ws; ++s)
       if (read_mask & (1u << s)) {
         const long long r = (((long long)a.slot * ws + s) * hpr + hl) * a.capacity + t;
-        st_relaxed_gpu(a.recv + r * kRowWords + 32, 0);
+        st_release_gpu(a.recv + r * kRowWords + 32, 0);
       }
   }
 

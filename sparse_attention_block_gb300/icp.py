@@ -43,6 +43,11 @@ lib.icp_top16_select.argtypes = [_P, _I32, _I32, _P, _I32, _I32, _I32, _I32, _P,
 lib.icp_publish_rows.restype = _I32
 lib.icp_publish_rows.argtypes = [_P, _I32, _I32, _P, _P, _P, _I32, _I32, _I32, _I32, _I32, _I32,
                                  _I32, _I64, _I32, _I32, _P]
+lib.icp_score_select_workspace_bytes.restype = _SZ
+lib.icp_score_select_workspace_bytes.argtypes = [_I32, _I32]
+lib.icp_score_select.restype = _I32
+lib.icp_score_select.argtypes = [_P, _P, _I64, _P, _I64, _P, _I32, _I32, _I32, _I32, _I32, _I32,
+                                 _I32, _P, _I32, _I32, _P, _SZ, _P, _P, _P, _P]
 lib.icp_merge.restype = _I32
 lib.icp_merge.argtypes = [_P, _P, _I32, _I32, _I32, _I32, _I32, _I32, _I32, _I64, _P, _P, _P, _P]
 
@@ -175,3 +180,45 @@ def icp_merge(recv, num_valid_pages, out_scores, out_ids, errors, *, T: int, slo
     ep = _dev(errors, "errors", (torch.int32,), 1)
     _check(lib.icp_merge(rp, np_, T, slot, world_size, heads_per_rank, capacity, init_blocks,
                          local_blocks, spin_limit, ep, osp, oip, _stream(stream)), "icp_merge")
+
+
+def icp_score_select_workspace_bytes(batch: int, decode_query_len: int) -> int:
+    n = lib.icp_score_select_workspace_bytes(int(batch), int(decode_query_len))
+    if n == 0 and batch > 0:
+        raise ValueError("invalid arguments for icp_score_select_workspace_bytes")
+    return n
+
+
+def icp_score_select(index_q, index_k, block_table, seq_lens, num_valid_pages, out_scores,
+                     out_ids, workspace, *, cols: int, rank: int, world_size: int,
+                     page_size: int, decode_query_len: int, max_decode_query_len: int,
+                     init_blocks: int, local_blocks: int, errors=None, stream=None):
+    """Fused scorer + Top16 select (no score plane) into out_* [T, 4, 16].
+
+    ``workspace`` is a uint8 device tensor of at least
+    icp_score_select_workspace_bytes(batch, decode_query_len) bytes (256-byte aligned).
+    """
+    B = seq_lens.shape[0]
+    T = B * decode_query_len
+    qp = _dev(index_q, "index_q", _FP8, 3)
+    kp = _dev(index_k, "index_k", _FP8, 3)
+    if tuple(index_q.shape) != (T, HEADS, DIM):
+        raise ValueError(f"index_q must be [{T}, 4, 128], got {tuple(index_q.shape)}")
+    if tuple(index_k.shape[1:]) != (page_size // world_size, DIM):
+        raise ValueError(f"index_k must be [pages, {page_size // world_size}, 128]")
+    if block_table.dim() != 2 or block_table.stride(1) != 1:
+        raise ValueError("block_table must be 2-D with unit last stride")
+    btp = _dev(block_table, "block_table", (torch.int32,), 2, contiguous=False)
+    slp = _dev(seq_lens, "seq_lens", (torch.int32,), 1)
+    np_ = _dev(num_valid_pages, "num_valid_pages", (torch.int32,), 1)
+    osp = _dev(out_scores, "out_scores", (torch.float32,), 3)
+    oip = _dev(out_ids, "out_ids", (torch.int32,), 3)
+    if tuple(out_scores.shape) != (T, HEADS, TOPK) or tuple(out_ids.shape) != (T, HEADS, TOPK):
+        raise ValueError("out_scores / out_ids must be [T, 4, 16]")
+    wp = _dev(workspace, "workspace", (torch.uint8,), 1)
+    ep = 0 if errors is None else _dev(errors, "errors", (torch.int32,), 1)
+    _check(lib.icp_score_select(qp, kp, index_k.shape[0], btp, block_table.stride(0), slp, B,
+                                cols, rank, world_size, page_size, decode_query_len,
+                                max_decode_query_len, np_, init_blocks, local_blocks, wp,
+                                workspace.numel(), osp, oip, ep, _stream(stream)),
+           "icp_score_select")

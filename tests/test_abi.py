@@ -26,6 +26,7 @@ def declared_functions():
 def test_header_declares_the_entry_points():
     names = declared_functions()
     for n in ["icp_score", "icp_top16_select", "icp_publish_rows", "icp_merge",
+              "icp_score_select", "icp_score_select_workspace_bytes",
               "icp_score_columns", "icp_status_string"]:
         assert n in names
 
@@ -91,3 +92,25 @@ def test_invalid_arguments_are_rejected_before_any_launch(lib):
     assert lib.icp_publish_rows(a, 4, 10, a, a, a, 0, 0, 2, 1, 4, 1, 2, 100, 1, 0, None) == INVALID
     lib.icp_status_string.restype = ctypes.c_char_p
     assert lib.icp_status_string(1) == b"invalid argument"
+
+
+def test_fused_workspace_size_and_checks(lib):
+    lib.icp_score_select_workspace_bytes.restype = ctypes.c_size_t
+    n = lib.icp_score_select_workspace_bytes(128, 4)
+    assert n >= (160 + 128) * 4 * 16 * 288
+    assert lib.icp_score_select_workspace_bytes(-1, 4) == 0
+    assert lib.icp_score_select_workspace_bytes(4, 9) == 0
+    P = ctypes.c_void_p
+    buf = ctypes.create_string_buffer(1 << 16)
+    a = ctypes.cast(ctypes.addressof(buf) + (-ctypes.addressof(buf) % 256), P)
+    lib.icp_score_select.argtypes = [P, P, ctypes.c_int64, P, ctypes.c_int64, P] + \
+        [ctypes.c_int] * 7 + [P, ctypes.c_int, ctypes.c_int, P, ctypes.c_size_t, P, P, P, P]
+    ok = lib.icp_score_select_workspace_bytes(1, 1)
+    # workspace too small / init + local > 16 / misaligned workspace
+    assert lib.icp_score_select(a, a, 4, a, 4, a, 1, 8, 0, 1, 128, 1, 1, a, 1, 2, a, ok - 1,
+                                a, a, None, None) == 1
+    assert lib.icp_score_select(a, a, 4, a, 4, a, 1, 8, 0, 1, 128, 1, 1, a, 9, 8, a, ok,
+                                a, a, None, None) == 1
+    bad = ctypes.c_void_p(a.value + 16)
+    assert lib.icp_score_select(a, a, 4, a, 4, a, 1, 8, 0, 1, 128, 1, 1, a, 1, 2, bad, ok,
+                                a, a, None, None) == 1
