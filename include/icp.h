@@ -190,6 +190,37 @@ int icp_score_select(const uint8_t *index_q, const uint8_t *index_k, int64_t num
                      void *workspace, size_t workspace_bytes, float *out_scores,
                      int32_t *out_ids, int32_t *errors, void *stream);
 
+/*
+ * icp_score_select for callers that cannot allocate device memory when they
+ * call: a serving engine that splits the GPU into fixed pools at start-up and
+ * allows no later allocation, a decode step being recorded into a CUDA graph,
+ * or a latency-critical path that cannot pay for cudaMalloc's implicit
+ * synchronisation.  The pages document no counterpart of this entry point.
+ *
+ * Arguments, output and behaviour are those of icp_score_select without the
+ * workspace: the scratch is a fixed array of ICP_NOALLOC_SCRATCH_BYTES held
+ * by every GPU that loads this library until the process exits.  Nothing is
+ * allocated or freed by the call.
+ *   - Limit: accepted when icp_score_select_workspace_bytes(batch,
+ *     decode_query_len) <= ICP_NOALLOC_SCRATCH_BYTES (for example up to 128
+ *     requests of 4 tokens, or 8 requests of 8 tokens); a larger batch returns
+ *     ICP_ERR_INVALID_ARG and launches nothing.
+ *   - The first call on each device looks up the array's device address
+ *     (cudaGetSymbolAddress, with that device current); make that first call
+ *     before any stream capture begins.
+ *   - All calls on a device share the array and it keeps what the last call
+ *     left; no part of it needs clearing, but calls that overlap on the GPU
+ *     race on it, so the caller must not run two at once.
+ */
+#define ICP_NOALLOC_SCRATCH_BYTES (8u * 1024u * 1024u)
+int icp_score_select_noalloc(const uint8_t *index_q, const uint8_t *index_k, int64_t num_pages,
+                             const int32_t *block_table, int64_t block_table_stride,
+                             const int32_t *seq_lens, int batch, int cols, int rank,
+                             int world_size, int page_size, int decode_query_len,
+                             int max_decode_query_len, const int32_t *num_valid_pages,
+                             int init_blocks, int local_blocks, float *out_scores,
+                             int32_t *out_ids, int32_t *errors, void *stream);
+
 #ifdef __cplusplus
 }
 #endif

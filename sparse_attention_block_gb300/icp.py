@@ -48,6 +48,9 @@ lib.icp_score_select_workspace_bytes.argtypes = [_I32, _I32]
 lib.icp_score_select.restype = _I32
 lib.icp_score_select.argtypes = [_P, _P, _I64, _P, _I64, _P, _I32, _I32, _I32, _I32, _I32, _I32,
                                  _I32, _P, _I32, _I32, _P, _SZ, _P, _P, _P, _P]
+lib.icp_score_select_noalloc.restype = _I32
+lib.icp_score_select_noalloc.argtypes = [_P, _P, _I64, _P, _I64, _P, _I32, _I32, _I32, _I32,
+                                         _I32, _I32, _I32, _P, _I32, _I32, _P, _P, _P, _P]
 lib.icp_merge.restype = _I32
 lib.icp_merge.argtypes = [_P, _P, _I32, _I32, _I32, _I32, _I32, _I32, _I32, _I64, _P, _P, _P, _P]
 
@@ -222,3 +225,39 @@ def icp_score_select(index_q, index_k, block_table, seq_lens, num_valid_pages, o
                                 max_decode_query_len, np_, init_blocks, local_blocks, wp,
                                 workspace.numel(), osp, oip, ep, _stream(stream)),
            "icp_score_select")
+
+
+NOALLOC_SCRATCH_BYTES = 8 * 1024 * 1024
+
+
+def icp_score_select_noalloc(index_q, index_k, block_table, seq_lens, num_valid_pages,
+                             out_scores, out_ids, *, cols: int, rank: int, world_size: int,
+                             page_size: int, decode_query_len: int, max_decode_query_len: int,
+                             init_blocks: int, local_blocks: int, errors=None, stream=None):
+    """icp_score_select with the library's fixed scratch array instead of a
+    workspace, for callers that cannot allocate device memory at call time.
+    Raises IcpError (invalid argument) when the batch needs more scratch than
+    NOALLOC_SCRATCH_BYTES."""
+    B = seq_lens.shape[0]
+    T = B * decode_query_len
+    qp = _dev(index_q, "index_q", _FP8, 3)
+    kp = _dev(index_k, "index_k", _FP8, 3)
+    if tuple(index_q.shape) != (T, HEADS, DIM):
+        raise ValueError(f"index_q must be [{T}, 4, 128], got {tuple(index_q.shape)}")
+    if tuple(index_k.shape[1:]) != (page_size // world_size, DIM):
+        raise ValueError(f"index_k must be [pages, {page_size // world_size}, 128]")
+    if block_table.dim() != 2 or block_table.stride(1) != 1:
+        raise ValueError("block_table must be 2-D with unit last stride")
+    btp = _dev(block_table, "block_table", (torch.int32,), 2, contiguous=False)
+    slp = _dev(seq_lens, "seq_lens", (torch.int32,), 1)
+    np_ = _dev(num_valid_pages, "num_valid_pages", (torch.int32,), 1)
+    osp = _dev(out_scores, "out_scores", (torch.float32,), 3)
+    oip = _dev(out_ids, "out_ids", (torch.int32,), 3)
+    if tuple(out_scores.shape) != (T, HEADS, TOPK) or tuple(out_ids.shape) != (T, HEADS, TOPK):
+        raise ValueError("out_scores / out_ids must be [T, 4, 16]")
+    ep = 0 if errors is None else _dev(errors, "errors", (torch.int32,), 1)
+    _check(lib.icp_score_select_noalloc(qp, kp, index_k.shape[0], btp, block_table.stride(0),
+                                        slp, B, cols, rank, world_size, page_size,
+                                        decode_query_len, max_decode_query_len, np_,
+                                        init_blocks, local_blocks, osp, oip, ep,
+                                        _stream(stream)), "icp_score_select_noalloc")
