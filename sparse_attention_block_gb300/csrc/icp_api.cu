@@ -40,7 +40,7 @@ int current_device(int *dev_out, int *sm_count) {
       return ICP_ERR_CUDA;
     if (major != 10 || minor != 3) {
       d.status = ICP_ERR_UNSUPPORTED;
-    } else if (icp::score_prepare(dev) != cudaSuccess) {
+    } else if (icp::score_prepare(dev) != cudaSuccess || icp::select_prepare() != cudaSuccess) {
       d.status = ICP_ERR_CUDA;
     } else {
       d.status = ICP_OK;
@@ -206,7 +206,7 @@ int icp_top16_select(const float *scores, int T, int K, const int32_t *num_valid
   a.index_offset = index_offset;
   a.out_scores = out_scores;
   a.out_ids = out_ids;
-  return to_status(icp::launch_select(a, false, static_cast<cudaStream_t>(stream)));
+  return to_status(icp::launch_select(a, false, sms, static_cast<cudaStream_t>(stream)));
 }
 
 int icp_publish_rows(const float *scores, int T, int K, const int32_t *num_valid_pages,
@@ -243,7 +243,7 @@ int icp_publish_rows(const float *scores, int T, int K, const int32_t *num_valid
   a.heads_per_rank = heads_per_rank;
   a.capacity = capacity;
   a.spin_limit = spin_limit;
-  return to_status(icp::launch_select(a, true, static_cast<cudaStream_t>(stream)));
+  return to_status(icp::launch_select(a, true, sms, static_cast<cudaStream_t>(stream)));
 }
 
 int icp_merge(int32_t *recv, const int32_t *num_valid_pages, int T, int slot, int world_size,

@@ -74,7 +74,8 @@ size_t fused_workspace_bytes(int batch, int dql);
 cudaError_t launch_score_select(const CUtensorMap &tmk, const CUtensorMap &tmq, ScoreArgs a,
                                 int grid, cudaStream_t stream);
 
-cudaError_t launch_select(const SelectArgs &a, bool publish, cudaStream_t stream);
+cudaError_t select_prepare();  // one-time per-device kernel attributes
+cudaError_t launch_select(const SelectArgs &a, bool publish, int sm_count, cudaStream_t stream);
 cudaError_t launch_merge(const MergeArgs &a, cudaStream_t stream);
 
 }  // namespace icp

@@ -7,12 +7,13 @@
 // slots go to the best remaining ids by (score descending, id ascending).
 // Output: ids ascending with their raw scores, then (-1, -inf) padding.
 //
-// Select: one CTA per (token, head) row, the row held in registers.  Every
-// non-forced valid score becomes a unique 64-bit key (score order, then
-// lower id).  With m free slots, tau = the m-th largest per-thread maximum
-// is a lower bound of the m-th largest key, and only the m threads whose
-// maximum reaches tau can hold keys >= tau, so at most m * EPT candidates
-// survive; one warp then picks the m largest candidates exactly.
+// Select: one CTA per (token, head) row, the row staged in shared memory.
+// Every non-forced valid score becomes a unique 64-bit key (score order,
+// then lower id).  With m free slots, tau = the m-th largest per-thread
+// maximum is a lower bound of the m-th largest key, and only the m threads
+// whose maximum reaches tau can hold keys >= tau, so at most m * EPT
+// candidates survive (EPT = row entries per thread); the m largest of them
+// are then found exactly, by rank when there are few.
 #include "icp_device.cuh"
 #include "icp_internal.h"
 
@@ -32,178 +33,273 @@ __device__ __forceinline__ bool poll_flag(const int *flag, int want, long long s
   return false;
 }
 
-template <int NT, int EPT, bool PUBLISH>
+// Persistent select: each CTA takes rows blockIdx.x, blockIdx.x + gridDim.x,
+// ... and stages them in shared memory with bulk async copies into two
+// buffers, so the next row streams in while the current one is processed.
+// MAXK bounds the row length of the variant.
+template <int NT, int MAXK, bool PUBLISH>
 __global__ void __launch_bounds__(NT) select_kernel(const SelectArgs a) {
   constexpr int NW = NT / 32;
-  constexpr int LPT = NT / 32;            // thread maxima per lane in warp 0
-  constexpr int CAP = kTopK * EPT;        // candidate bound
-  constexpr int CPL = (CAP + 31) / 32;    // candidates per lane in warp 0
-  static_assert(NW >= 1, "NT");
+  constexpr int EPT = ((MAXK + 4 * NT - 1) / (4 * NT)) * 4;  // row entries per thread
+  constexpr int CAP = kTopK * EPT;           // candidate bound (see the file comment)
+  constexpr int WL = (NW * kTopK + 31) / 32; // per-warp maxima per lane in warp 0
+  constexpr int BUF = ((MAXK + 3) / 4) * 4;  // floats per row buffer
 
-  __shared__ int s_nf, s_nc;
+  extern __shared__ __align__(16) unsigned char dyn_smem[];
+  float *bufs = reinterpret_cast<float *>(dyn_smem);  // [2][BUF] (bulk) or [1][BUF]
+  __shared__ __align__(8) unsigned long long s_bar[2];
+  __shared__ int s_nc, s_nf, s_abort;
   __shared__ int s_fid[kTopK];
   __shared__ float s_fsc[kTopK];
-  __shared__ unsigned long long s_tm[NT];
-  __shared__ unsigned long long s_cand[CAP];
+  __shared__ unsigned long long s_wtop[NW][kTopK];
   __shared__ unsigned long long s_tau;
+  __shared__ unsigned long long s_cand[CAP];
+  __shared__ unsigned long long s_sel[kTopK];
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int row = blockIdx.x;
-  const int t = row >> 2;
-  const int h = row & 3;
-  const float *src = a.scores + (long long)row * a.K;
-  const int nvp = a.nvp[t];
+  const int K = a.K;
+  const int rows = a.T * 4;
+  const int scale = a.index_scale, off = a.index_offset;
+  const bool bulk = (K % 4 == 0) && ((reinterpret_cast<uintptr_t>(a.scores) & 15u) == 0);
+  const uint32_t bytes = (uint32_t)K * 4u;
 
   if (tid == 0) {
-    s_nf = 0;
-    s_nc = 0;
+    s_abort = 0;
+    if (bulk) {
+      mbar_init(smem_u32(&s_bar[0]), 1);
+      mbar_init(smem_u32(&s_bar[1]), 1);
+      fence_mbarrier_init();
+    }
   }
   __syncthreads();
+  if (bulk && tid == 0 && (int)blockIdx.x < rows) {
+    mbar_arrive_expect_tx(smem_u32(&s_bar[0]), bytes);
+    bulk_load(smem_u32(bufs), a.scores + (long long)blockIdx.x * K, bytes, smem_u32(&s_bar[0]));
+  }
 
-  unsigned long long key[EPT];
-  unsigned long long tm = 0;
+  int it = 0;
+  int nvp_next = (int)blockIdx.x < rows ? __ldg(a.nvp + (blockIdx.x >> 2)) : 0;
+  for (int row = blockIdx.x; row < rows; row += gridDim.x, ++it) {
+    const int cur = bulk ? (it & 1) : 0;
+    float *rowv = bufs + cur * BUF;
+    const int nvp = nvp_next;  // loaded one row ahead, off the critical path
+    if (row + (int)gridDim.x < rows) nvp_next = __ldg(a.nvp + ((row + gridDim.x) >> 2));
+    if (bulk) {
+      const int next = row + gridDim.x;
+      if (tid == 0 && next < rows) {
+        const int nb = cur ^ 1;  // freed by the previous iteration's last barrier
+        mbar_arrive_expect_tx(smem_u32(&s_bar[nb]), bytes);
+        bulk_load(smem_u32(bufs + nb * BUF), a.scores + (long long)next * K, bytes,
+                  smem_u32(&s_bar[nb]));
+      }
+      if (!mbar_wait(smem_u32(&s_bar[cur]), (uint32_t)((it >> 1) & 1), &s_abort)) {
+        // a copy did not land in time: report and stop (no trap)
+        if (tid == 0 && a.errors) atomicAdd(a.errors, 1);
+        return;
+      }
+    } else {
+      const float *src = a.scores + (long long)row * K;
+      for (int c = tid; c < K; c += NT) rowv[c] = src[c];
+    }
+    if (tid == 0) s_nc = 0;
+    const int t = row >> 2;
+    const int h = row & 3;
+
+    // forced ids, in increasing order: every valid id when nvp <= 16, else
+    // [0, init) then [nvp - local, nvp); each exists when it maps to a column
+    if (warp == 0) {
+      const bool all = nvp <= kTopK;
+      const int nforced = all ? max(nvp, 0) : a.init_blocks + a.local_blocks;
+      int id = -1;
+      bool ok = false;
+      if (lane < nforced && lane < kTopK) {
+        id = all ? lane
+                 : (lane < a.init_blocks ? lane : nvp - a.local_blocks + (lane - a.init_blocks));
+        const int d = id - off;
+        ok = id >= 0 && id < nvp && d >= 0 && d % scale == 0 && d / scale < K;
+      }
+      const unsigned bal = __ballot_sync(0xFFFFFFFFu, ok);
+      if (ok) s_fid[__popc(bal & ((1u << lane) - 1u))] = id;
+      if (lane == 0) s_nf = __popc(bal);
+    }
+    __syncthreads();  // the row buffer and the forced ids are ready
+    const int nf = s_nf;
+    const int m = kTopK - nf;
+    if (tid < nf) s_fsc[tid] = rowv[(s_fid[tid] - off) / scale];
+
+    // free columns: ids in [init, nvp - local) when nvp > 16, else none
+    int c_lo = 0, c_hi = 0;
+    if (nvp > kTopK) {
+      const int id_lo = a.init_blocks, id_hi = nvp - a.local_blocks;   // [id_lo, id_hi)
+      c_lo = id_lo - off <= 0 ? 0 : (id_lo - off + scale - 1) / scale;
+      c_hi = id_hi - off <= 0 ? 0 : (id_hi - off + scale - 1) / scale;
+      c_hi = min(c_hi, K);
+      c_lo = min(c_lo, c_hi);
+    }
+    // phase 1: per-thread best free entry (score, then lower column)
+    float best = 0.0f;
+    int bc = -1;
+    {
+      const float4 *r4 = reinterpret_cast<const float4 *>(rowv);
+      const int f_lo = c_lo >> 2, f_hi = (c_hi + 3) >> 2;
+      for (int f = f_lo + tid; f < f_hi; f += NT) {
+        const float4 x = r4[f];
+        const float vv[4] = {x.x, x.y, x.z, x.w};
 #pragma unroll
-  for (int i = 0; i < EPT; ++i) {
-    const int c = tid + i * NT;
-    key[i] = 0;
-    if (c < a.K) {
-      const float v = src[c];
-      const int id = c * a.index_scale + a.index_offset;
-      if (id < nvp) {
-        if (forced_id(id, nvp, a.init_blocks, a.local_blocks)) {
-          const int slot = atomicAdd(&s_nf, 1);
-          if (slot < kTopK) {
-            s_fid[slot] = id;
-            s_fsc[slot] = v;
+        for (int k = 0; k < 4; ++k) {
+          const int c = 4 * f + k;
+          if ((unsigned)(c - c_lo) < (unsigned)(c_hi - c_lo) && (bc < 0 || vv[k] > best)) {
+            best = vv[k];
+            bc = c;
           }
+        }
+      }
+    }
+    const unsigned long long tm = bc < 0 ? 0ull : make_key(best, bc * scale + off);
+
+    // tau = m-th largest thread maximum, in two levels: each warp's top m of
+    // its lanes' maxima, then the top m of those lists (1 = fewer than m exist)
+    {
+      unsigned long long my = tm;
+      for (int r = 0; r < m; ++r) {
+        const unsigned long long w = warp_max_key(my);
+        if (lane == 0) s_wtop[warp][r] = w;
+        if (w != 0 && my == w) my = 0;
+      }
+    }
+    __syncthreads();
+    if (warp == 0) {
+      unsigned long long loc[WL];
+      unsigned long long lmax = 0;
+#pragma unroll
+      for (int j = 0; j < WL; ++j) {
+        const int k = lane + 32 * j;
+        const int w = k / kTopK, r = k % kTopK;
+        loc[j] = (w < NW && r < m) ? s_wtop[w][r] : 0ull;
+        lmax = loc[j] > lmax ? loc[j] : lmax;
+      }
+      unsigned long long tau = 0;
+      int found = 0;
+      for (int r = 0; r < m; ++r) {
+        const unsigned long long w = warp_max_key(lmax);
+        if (w == 0) break;
+        tau = w;
+        ++found;
+        if (lmax == w) {
+          lmax = 0;
+#pragma unroll
+          for (int j = 0; j < WL; ++j) {
+            if (loc[j] == w) loc[j] = 0;
+            lmax = loc[j] > lmax ? loc[j] : lmax;
+          }
+        }
+      }
+      if (lane == 0) s_tau = (found < m) ? 1ull : tau;
+    }
+    __syncthreads();
+
+    // candidates: keys >= tau (only the m threads whose maximum reached tau hold any)
+    if (m > 0 && tm != 0 && tm >= s_tau) {
+      const unsigned long long tau = s_tau;
+      const float4 *r4 = reinterpret_cast<const float4 *>(rowv);
+      const int f_lo = c_lo >> 2, f_hi = (c_hi + 3) >> 2;
+      for (int f = f_lo + tid; f < f_hi; f += NT) {
+        const float4 x = r4[f];
+        const float vv[4] = {x.x, x.y, x.z, x.w};
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          const int c = 4 * f + k;
+          if ((unsigned)(c - c_lo) >= (unsigned)(c_hi - c_lo)) continue;
+          const unsigned long long key = make_key(vv[k], c * scale + off);
+          if (key >= tau) {
+            const int slot = atomicAdd(&s_nc, 1);
+            if (slot < CAP) s_cand[slot] = key;
+          }
+        }
+      }
+    }
+    __syncthreads();
+    const int nc = min(s_nc, CAP);
+    const int nch = min(nc, m);
+
+    // the m largest candidates: by rank when few, else by rounds in warp 0
+    if (nc <= m) {
+      if (tid < nc) s_sel[tid] = s_cand[tid];
+    } else if (nc <= NT) {
+      if (tid < nc) {
+        const unsigned long long my = s_cand[tid];
+        int rank = 0;
+        for (int j = 0; j < nc; ++j) rank += (s_cand[j] > my) ? 1 : 0;
+        if (rank < m) s_sel[rank] = my;
+      }
+    } else if (warp == 0) {
+      unsigned long long prev = ~0ull;
+      for (int r = 0; r < m; ++r) {
+        unsigned long long local = 0;
+        for (int j = lane; j < nc; j += 32) {
+          const unsigned long long x = s_cand[j];
+          if (x < prev && x > local) local = x;
+        }
+        const unsigned long long w = warp_max_key(local);
+        if (lane == 0) s_sel[r] = w;
+        prev = w;
+      }
+    }
+    __syncthreads();
+
+    if (warp == 0) {
+      const int n = nf + nch;
+      int my_id = 0x7FFFFFFF;
+      float my_sc = -INFINITY;
+      if (lane < nf) {
+        my_id = s_fid[lane];
+        my_sc = s_fsc[lane];
+      } else if (lane < n) {
+        my_id = key_id(s_sel[lane - nf]);
+        my_sc = rowv[(my_id - off) / scale];  // raw score bits
+      }
+      int out_id;
+      float out_sc;
+      sort_by_id_16(lane, n, my_id, my_sc, out_id, out_sc);
+
+      if constexpr (!PUBLISH) {
+        if (lane < kTopK) {
+          a.out_scores[(long long)row * kTopK + lane] = out_sc;
+          a.out_ids[(long long)row * kTopK + lane] = out_id;
+        }
+      } else {
+        const int hpr = a.heads_per_rank;
+        int *base = reinterpret_cast<int *>(a.recv_bases[h / hpr]);
+        const long long r =
+            (((long long)a.slot * a.world_size + a.rank) * hpr + h % hpr) * a.capacity + t;
+        int *dst = base + r * kRowWords;
+        int ok = 0;
+        if (lane == 0) ok = poll_flag(dst + 32, 0, a.spin_limit) ? 1 : 0;
+        ok = __shfl_sync(0xFFFFFFFFu, ok, 0);
+        if (!ok) {
+          if (lane == 0) atomicAdd(a.errors, 1);
         } else {
-          key[i] = make_key(v, id);
+          if (lane < kTopK) {
+            dst[lane] = __float_as_int(out_sc);
+            dst[kTopK + lane] = out_id;
+          }
+          __threadfence();
+          __syncwarp();
+          if (lane == 0) st_release_gpu(dst + 32, 1);
         }
       }
     }
-    tm = key[i] > tm ? key[i] : tm;
-  }
-  s_tm[tid] = tm;
-  __syncthreads();
-  const int nf = min(s_nf, kTopK);
-  const int m = kTopK - nf;
-
-  // tau = m-th largest thread maximum (1 = "take every key" when fewer than
-  // m threads hold one)
-  if (warp == 0) {
-    unsigned long long loc[LPT];
-    unsigned long long lmax = 0;
-#pragma unroll
-    for (int j = 0; j < LPT; ++j) {
-      loc[j] = s_tm[lane + 32 * j];
-      lmax = loc[j] > lmax ? loc[j] : lmax;
-    }
-    unsigned long long tau = 0;
-    int found = 0;
-    for (int r = 0; r < m; ++r) {
-      const unsigned long long w = warp_max_key(lmax);
-      if (w == 0) break;
-      tau = w;
-      ++found;
-      if (lmax == w) {
-        lmax = 0;
-#pragma unroll
-        for (int j = 0; j < LPT; ++j) {
-          if (loc[j] == w) loc[j] = 0;
-          lmax = loc[j] > lmax ? loc[j] : lmax;
-        }
-      }
-    }
-    if (lane == 0) s_tau = (found < m) ? 1ull : tau;
-  }
-  __syncthreads();
-  if (m > 0) {
-    const unsigned long long tau = s_tau;
-#pragma unroll
-    for (int i = 0; i < EPT; ++i) {
-      if (key[i] != 0 && key[i] >= tau) {
-        const int slot = atomicAdd(&s_nc, 1);
-        if (slot < CAP) s_cand[slot] = key[i];
-      }
-    }
-  }
-  __syncthreads();
-
-  if (warp != 0) return;
-  const int nc = min(s_nc, CAP);
-  // pick the m largest candidates; lane nf + r receives the r-th
-  unsigned long long cl[CPL];
-  unsigned long long lmax = 0;
-#pragma unroll
-  for (int j = 0; j < CPL; ++j) {
-    const int k = lane + 32 * j;
-    cl[j] = (k < nc) ? s_cand[k] : 0ull;
-    lmax = cl[j] > lmax ? cl[j] : lmax;
-  }
-  unsigned long long mine = 0;
-  int nch = 0;
-  for (int r = 0; r < m; ++r) {
-    const unsigned long long w = warp_max_key(lmax);
-    if (w == 0) break;
-    if (lane == nf + r) mine = w;
-    ++nch;
-    if (lmax == w) {
-      lmax = 0;
-#pragma unroll
-      for (int j = 0; j < CPL; ++j) {
-        if (cl[j] == w) cl[j] = 0;
-        lmax = cl[j] > lmax ? cl[j] : lmax;
-      }
-    }
-  }
-  const int n = nf + nch;
-  int my_id = 0x7FFFFFFF;
-  float my_sc = -INFINITY;
-  if (lane < nf) {
-    my_id = s_fid[lane];
-    my_sc = s_fsc[lane];
-  } else if (lane < n) {
-    my_id = key_id(mine);
-    my_sc = src[(my_id - a.index_offset) / a.index_scale];  // raw score bits
-  }
-  int out_id;
-  float out_sc;
-  sort_by_id_16(lane, n, my_id, my_sc, out_id, out_sc);
-
-  if constexpr (!PUBLISH) {
-    if (lane < kTopK) {
-      a.out_scores[(long long)row * kTopK + lane] = out_sc;
-      a.out_ids[(long long)row * kTopK + lane] = out_id;
-    }
-  } else {
-    const int hpr = a.heads_per_rank;
-    int *base = reinterpret_cast<int *>(a.recv_bases[h / hpr]);
-    const long long r =
-        (((long long)a.slot * a.world_size + a.rank) * hpr + h % hpr) * a.capacity + t;
-    int *dst = base + r * kRowWords;
-    int ok = 0;
-    if (lane == 0) ok = poll_flag(dst + 32, 0, a.spin_limit) ? 1 : 0;
-    ok = __shfl_sync(0xFFFFFFFFu, ok, 0);
-    if (!ok) {
-      if (lane == 0) atomicAdd(a.errors, 1);
-      return;
-    }
-    if (lane < kTopK) {
-      dst[lane] = __float_as_int(out_sc);
-      dst[kTopK + lane] = out_id;
-    }
-    __threadfence();
-    __syncwarp();
-    if (lane == 0) st_release_gpu(dst + 32, 1);
+    __syncthreads();  // this row's buffer and scratch may be reused
   }
 }
 
-// One warp per (token, owned head).
+// One warp per (token, owned head).  Lane i < 16 holds entry i of every
+// source row (at most 4 sources), so the union, the per-id maximum and the
+// ranking are done with shuffles; the result is compacted through shared
+// memory and ordered by id.
 __global__ void __launch_bounds__(128) merge_kernel(const MergeArgs a) {
-  __shared__ int s_id[4][64];
-  __shared__ float s_sc[4][64];
-  __shared__ unsigned long long s_key[4][64];
-  __shared__ int s_sel[4][64];
+  __shared__ int s_id[4][kTopK];
+  __shared__ float s_sc[4][kTopK];
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int item = blockIdx.x * 4 + warp;
@@ -213,13 +309,13 @@ __global__ void __launch_bounds__(128) merge_kernel(const MergeArgs a) {
   const int nvp = a.nvp[t];
   const int ws = a.world_size;
 
+  int ids[4];
+  float scs[4];
   unsigned read_mask = 0;
+#pragma unroll
   for (int s = 0; s < 4; ++s) {
-    const int e = s * 16 + (lane & 15);
-    if (lane < 16) {
-      s_id[warp][e] = -1;
-      s_sc[warp][e] = -INFINITY;
-    }
+    ids[s] = -1;
+    scs[s] = -INFINITY;
     if (s >= ws) continue;
     const long long r = (((long long)a.slot * ws + s) * hpr + hl) * a.capacity + t;
     int *row = a.recv + r * kRowWords;
@@ -231,10 +327,10 @@ __global__ void __launch_bounds__(128) merge_kernel(const MergeArgs a) {
       continue;
     }
     read_mask |= 1u << s;
-    if (lane < 16) {
+    if (lane < kTopK) {
       (void)ld_acquire_gpu(row + 32);  // order this lane's reads after the flag
-      s_sc[warp][e] = __int_as_float(row[lane]);
-      s_id[warp][e] = row[16 + lane];
+      scs[s] = __int_as_float(row[lane]);
+      ids[s] = row[kTopK + lane];
     }
   }
   __syncwarp();
@@ -247,59 +343,82 @@ __global__ void __launch_bounds__(128) merge_kernel(const MergeArgs a) {
       }
   }
 
-  // union with the maximum score per id (first source wins a tie)
-  int nforced = 0;
+  // keep an entry unless another source holds the same id with a higher
+  // score (an exact tie goes to the lower source)
+  bool keep[4];
 #pragma unroll
-  for (int k = 0; k < 2; ++k) {
-    const int e = lane + 32 * k;
-    const int id = s_id[warp][e];
-    const float sc = s_sc[warp][e];
-    bool keep = (id >= 0) && (id < nvp);
-    if (keep) {
-      for (int e2 = 0; e2 < 64; ++e2) {
-        if (e2 == e || s_id[warp][e2] != id) continue;
-        const float s2 = s_sc[warp][e2];
-        if (s2 > sc || (s2 == sc && e2 < e)) {
-          keep = false;
-          break;
+  for (int s = 0; s < 4; ++s) keep[s] = lane < kTopK && ids[s] >= 0 && ids[s] < nvp;
+  if (ws > 1) {
+#pragma unroll
+    for (int s2 = 0; s2 < 4; ++s2) {
+      if (s2 >= ws) break;
+      for (int j = 0; j < kTopK; ++j) {
+        const int id2 = __shfl_sync(0xFFFFFFFFu, ids[s2], j);
+        const float sc2 = __shfl_sync(0xFFFFFFFFu, scs[s2], j);
+#pragma unroll
+        for (int s = 0; s < 4; ++s) {
+          if (s == s2 || !keep[s] || ids[s] != id2) continue;
+          if (sc2 > scs[s] || (sc2 == scs[s] && s2 < s)) keep[s] = false;
         }
       }
     }
-    const bool f = keep && forced_id(id, nvp, a.init_blocks, a.local_blocks);
-    s_key[warp][e] = (keep && !f) ? make_key(sc, id) : 0ull;
-    s_sel[warp][e] = f ? 1 : 0;
-    nforced += f ? 1 : 0;
   }
-  nforced = __reduce_add_sync(0xFFFFFFFFu, nforced);
-  __syncwarp();
-  const int m = kTopK - min(nforced, kTopK);
-  // keep the m best free entries: rank = number of larger keys
+  int total = 0, nforced = 0;
+  bool forced[4];
 #pragma unroll
-  for (int k = 0; k < 2; ++k) {
-    const int e = lane + 32 * k;
-    const unsigned long long my = s_key[warp][e];
-    if (my != 0) {
-      int rank = 0;
-      for (int e2 = 0; e2 < 64; ++e2) rank += (s_key[warp][e2] > my) ? 1 : 0;
-      if (rank < m) s_sel[warp][e] = 1;
-    }
+  for (int s = 0; s < 4; ++s) {
+    forced[s] = keep[s] && forced_id(ids[s], nvp, a.init_blocks, a.local_blocks);
+    total += __popc(__ballot_sync(0xFFFFFFFFu, keep[s]));
+    nforced += __popc(__ballot_sync(0xFFFFFFFFu, forced[s]));
   }
-  __syncwarp();
-  // compact the selected entries into lanes and order them by id
-  int nsel = 0, my_id = 0x7FFFFFFF;
-  float my_sc = -INFINITY;
-  for (int e = 0; e < 64; ++e) {
-    if (s_sel[warp][e]) {
-      if (nsel == lane) {
-        my_id = s_id[warp][e];
-        my_sc = s_sc[warp][e];
+  bool sel[4];
+  if (total <= kTopK) {
+#pragma unroll
+    for (int s = 0; s < 4; ++s) sel[s] = keep[s];
+  } else {
+    // m best free entries by (score desc, id asc)
+    const int m = kTopK - min(nforced, kTopK);
+    unsigned long long key[4];
+#pragma unroll
+    for (int s = 0; s < 4; ++s) key[s] = (keep[s] && !forced[s]) ? make_key(scs[s], ids[s]) : 0ull;
+    int rank[4] = {0, 0, 0, 0};
+#pragma unroll
+    for (int s2 = 0; s2 < 4; ++s2) {
+      if (s2 >= ws) break;
+      for (int j = 0; j < kTopK; ++j) {
+        const unsigned long long k2 = __shfl_sync(0xFFFFFFFFu, key[s2], j);
+#pragma unroll
+        for (int s = 0; s < 4; ++s) rank[s] += (k2 > key[s]) ? 1 : 0;
       }
-      ++nsel;
     }
+#pragma unroll
+    for (int s = 0; s < 4; ++s) sel[s] = forced[s] || (key[s] != 0 && rank[s] < m);
+  }
+  // compact the selected entries (at most 16) and order them by id
+  int n = 0;
+#pragma unroll
+  for (int s = 0; s < 4; ++s) {
+    const unsigned bal = __ballot_sync(0xFFFFFFFFu, sel[s]);
+    if (sel[s]) {
+      const int pos = n + __popc(bal & ((1u << lane) - 1u));
+      if (pos < kTopK) {
+        s_id[warp][pos] = ids[s];
+        s_sc[warp][pos] = scs[s];
+      }
+    }
+    n += __popc(bal);
+  }
+  n = min(n, kTopK);
+  __syncwarp();
+  int my_id = 0x7FFFFFFF;
+  float my_sc = -INFINITY;
+  if (lane < n) {
+    my_id = s_id[warp][lane];
+    my_sc = s_sc[warp][lane];
   }
   int out_id;
   float out_sc;
-  sort_by_id_16(lane, min(nsel, kTopK), my_id, my_sc, out_id, out_sc);
+  sort_by_id_16(lane, n, my_id, my_sc, out_id, out_sc);
   if (lane < kTopK) {
     const long long o = ((long long)t * hpr + hl) * kTopK + lane;
     a.out_scores[o] = out_sc;
@@ -309,18 +428,33 @@ __global__ void __launch_bounds__(128) merge_kernel(const MergeArgs a) {
 
 }  // namespace
 
-cudaError_t launch_select(const SelectArgs &a, bool publish, cudaStream_t stream) {
+constexpr int kSmallK = 1024;
+constexpr int kLargeK = 12288;
+
+cudaError_t select_prepare() {
+  const int big = 2 * kLargeK * 4;
+  cudaError_t e;
+  e = cudaFuncSetAttribute(select_kernel<256, kLargeK, false>,
+                           cudaFuncAttributeMaxDynamicSharedMemorySize, big);
+  if (e != cudaSuccess) return e;
+  return cudaFuncSetAttribute(select_kernel<256, kLargeK, true>,
+                              cudaFuncAttributeMaxDynamicSharedMemorySize, big);
+}
+
+cudaError_t launch_select(const SelectArgs &a, bool publish, int sm_count, cudaStream_t stream) {
   const int rows = a.T * 4;
   if (rows == 0) return cudaSuccess;
-  if (a.K <= 1024) {
-    if (publish) select_kernel<128, 8, true><<<rows, 128, 0, stream>>>(a);
-    else select_kernel<128, 8, false><<<rows, 128, 0, stream>>>(a);
-  } else if (a.K <= 4096) {
-    if (publish) select_kernel<256, 16, true><<<rows, 256, 0, stream>>>(a);
-    else select_kernel<256, 16, false><<<rows, 256, 0, stream>>>(a);
+  // two row buffers; rows start 16-byte aligned when K % 4 == 0
+  if (a.K <= kSmallK) {
+    const size_t smem = 2 * (size_t)((kSmallK + 3) / 4 * 4) * 4;
+    const int grid = rows < 8 * sm_count ? rows : 8 * sm_count;
+    if (publish) select_kernel<128, kSmallK, true><<<grid, 128, smem, stream>>>(a);
+    else select_kernel<128, kSmallK, false><<<grid, 128, smem, stream>>>(a);
   } else {
-    if (publish) select_kernel<512, 24, true><<<rows, 512, 0, stream>>>(a);
-    else select_kernel<512, 24, false><<<rows, 512, 0, stream>>>(a);
+    const size_t smem = 2 * (size_t)((kLargeK + 3) / 4 * 4) * 4;
+    const int grid = rows < 2 * sm_count ? rows : 2 * sm_count;
+    if (publish) select_kernel<256, kLargeK, true><<<grid, 256, smem, stream>>>(a);
+    else select_kernel<256, kLargeK, false><<<grid, 256, smem, stream>>>(a);
   }
   return cudaGetLastError();
 }
