@@ -7,13 +7,13 @@
 // slots go to the best remaining ids by (score descending, id ascending).
 // Output: ids ascending with their raw scores, then (-1, -inf) padding.
 //
-// Select: one CTA per (token, head) row, the row staged in shared memory.
-// Every non-forced valid score becomes a unique 64-bit key (score order,
-// then lower id).  With m free slots, tau = the m-th largest per-thread
-// maximum is a lower bound of the m-th largest key, and only the m threads
-// whose maximum reaches tau can hold keys >= tau, so at most m * EPT
-// candidates survive (EPT = row entries per thread); the m largest of them
-// are then found exactly, by rank when there are few.
+// Select: one warp per row for rows up to 2048 columns, a CTA per row
+// (persistent, double-buffered in shared memory) for longer rows.  Every
+// non-forced valid score
+// becomes a unique 64-bit key (score order, then lower id).  With m free
+// slots, tau = the m-th largest per-thread best is a lower bound of the m-th
+// largest key, and only the m threads whose best reaches tau can hold keys
+// >= tau; those are collected and the m largest picked exactly.
 #include "icp_device.cuh"
 #include "icp_internal.h"
 
@@ -33,12 +33,12 @@ __device__ __forceinline__ bool poll_flag(const int *flag, int want, long long s
   return false;
 }
 
-// Persistent select: each CTA takes rows blockIdx.x, blockIdx.x + gridDim.x,
+// Persistent block select (long rows): each CTA takes rows blockIdx.x, blockIdx.x + gridDim.x,
 // ... and stages them in shared memory with bulk async copies into two
 // buffers, so the next row streams in while the current one is processed.
 // MAXK bounds the row length of the variant.
 template <int NT, int MAXK, bool PUBLISH>
-__global__ void __launch_bounds__(NT) select_kernel(const SelectArgs a) {
+__global__ void __launch_bounds__(NT) select_block_kernel(const SelectArgs a) {
   constexpr int NW = NT / 32;
   constexpr int EPT = ((MAXK + 4 * NT - 1) / (4 * NT)) * 4;  // row entries per thread
   constexpr int CAP = kTopK * EPT;           // candidate bound (see the file comment)
@@ -116,7 +116,8 @@ __global__ void __launch_bounds__(NT) select_kernel(const SelectArgs a) {
         id = all ? lane
                  : (lane < a.init_blocks ? lane : nvp - a.local_blocks + (lane - a.init_blocks));
         const int d = id - off;
-        ok = id >= 0 && id < nvp && d >= 0 && d % scale == 0 && d / scale < K;
+        ok = id >= 0 && id < nvp && d >= 0 &&
+             (scale == 1 ? d < K : (d % scale == 0 && d / scale < K));
       }
       const unsigned bal = __ballot_sync(0xFFFFFFFFu, ok);
       if (ok) s_fid[__popc(bal & ((1u << lane) - 1u))] = id;
@@ -125,7 +126,10 @@ __global__ void __launch_bounds__(NT) select_kernel(const SelectArgs a) {
     __syncthreads();  // the row buffer and the forced ids are ready
     const int nf = s_nf;
     const int m = kTopK - nf;
-    if (tid < nf) s_fsc[tid] = rowv[(s_fid[tid] - off) / scale];
+    if (tid < nf) {
+      const int d = s_fid[tid] - off;
+      s_fsc[tid] = rowv[scale == 1 ? d : d / scale];
+    }
 
     // free columns: ids in [init, nvp - local) when nvp > 16, else none
     int c_lo = 0, c_hi = 0;
@@ -201,6 +205,8 @@ __global__ void __launch_bounds__(NT) select_kernel(const SelectArgs a) {
     // candidates: keys >= tau (only the m threads whose maximum reached tau hold any)
     if (m > 0 && tm != 0 && tm >= s_tau) {
       const unsigned long long tau = s_tau;
+      // keys >= tau have scores >= tau's score (tau = 1 has none: -inf)
+      const float ts = (tau >> 32) == 0 ? -INFINITY : unord_float((uint32_t)(tau >> 32));
       const float4 *r4 = reinterpret_cast<const float4 *>(rowv);
       const int f_lo = c_lo >> 2, f_hi = (c_hi + 3) >> 2;
       for (int f = f_lo + tid; f < f_hi; f += NT) {
@@ -209,7 +215,7 @@ __global__ void __launch_bounds__(NT) select_kernel(const SelectArgs a) {
 #pragma unroll
         for (int k = 0; k < 4; ++k) {
           const int c = 4 * f + k;
-          if ((unsigned)(c - c_lo) >= (unsigned)(c_hi - c_lo)) continue;
+          if (!(vv[k] >= ts) || (unsigned)(c - c_lo) >= (unsigned)(c_hi - c_lo)) continue;
           const unsigned long long key = make_key(vv[k], c * scale + off);
           if (key >= tau) {
             const int slot = atomicAdd(&s_nc, 1);
@@ -256,7 +262,8 @@ __global__ void __launch_bounds__(NT) select_kernel(const SelectArgs a) {
         my_sc = s_fsc[lane];
       } else if (lane < n) {
         my_id = key_id(s_sel[lane - nf]);
-        my_sc = rowv[(my_id - off) / scale];  // raw score bits
+        const int d = my_id - off;
+        my_sc = rowv[scale == 1 ? d : d / scale];  // raw score bits
       }
       int out_id;
       float out_sc;
@@ -290,6 +297,272 @@ __global__ void __launch_bounds__(NT) select_kernel(const SelectArgs a) {
       }
     }
     __syncthreads();  // this row's buffer and scratch may be reused
+  }
+}
+
+// Warp-per-row select: each warp owns whole rows (row = global warp index,
+// then + total warps), so no CTA barrier sits between the phases and every
+// row of a launch can be in flight at once.
+//   1. forced ids (at most 16, read directly) go to lanes 0..nf-1;
+//   2. every lane scans its strided float4s of the free column range and
+//      keeps its best entry (score, then lower column);
+//   3. tau = m-th largest lane best (m = 16 - nf, rounds of a warp max);
+//      only the <= m lanes whose best reaches tau hold keys >= tau, and they
+//      rescan their share into a per-warp candidate buffer (a float compare
+//      against tau's score filters first);
+//   4. the m largest candidates (rounds of a warp max), forced + chosen
+//      ordered by id, written or published.
+// If a row has more candidates than the buffer holds (only possible with
+// very many equal scores), the warp picks the m largest directly from the
+// row by rounds instead.  Rows are read with float4 loads when K % 4 == 0 and
+// the plane is 16-byte aligned, else with scalar loads.
+constexpr int kSelWarps = 4;    // warps (rows in flight) per CTA
+constexpr int kCandCap = 256;   // candidates per warp
+constexpr int kChunk = 8;       // float4 loads in flight per lane
+
+// Best (score, then lower column) over columns [c_lo, c_hi) owned by this
+// lane, and keys >= tau collected into cand[] when collect is set.
+template <bool VEC>
+__device__ __forceinline__ void scan_row(const float *src, int c_lo, int c_hi, int lane,
+                                         float &best, int &bc) {
+  if constexpr (VEC) {
+    const float4 *r4 = reinterpret_cast<const float4 *>(src);
+    const int f_lo = c_lo >> 2, f_hi = (c_hi + 3) >> 2;
+    for (int f0 = f_lo + lane; f0 < f_hi; f0 += 32 * kChunk) {
+      float4 x[kChunk];
+#pragma unroll
+      for (int u = 0; u < kChunk; ++u) {
+        const int f = f0 + 32 * u;
+        x[u] = f < f_hi ? __ldg(r4 + f) : make_float4(0.f, 0.f, 0.f, 0.f);
+      }
+#pragma unroll
+      for (int u = 0; u < kChunk; ++u) {
+        const int f = f0 + 32 * u;
+        const float vv[4] = {x[u].x, x[u].y, x[u].z, x[u].w};
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          const int c = 4 * f + k;
+          if ((unsigned)(c - c_lo) < (unsigned)(c_hi - c_lo) && (bc < 0 || vv[k] > best)) {
+            best = vv[k];
+            bc = c;
+          }
+        }
+      }
+    }
+  } else {
+    for (int c = c_lo + lane; c < c_hi; c += 32) {
+      const float v = __ldg(src + c);
+      if (bc < 0 || v > best) {
+        best = v;
+        bc = c;
+      }
+    }
+  }
+}
+
+// Appends this lane's keys >= tau among columns [c_lo, c_hi) to cand.
+template <bool VEC>
+__device__ __forceinline__ void collect_row(const float *src, int c_lo, int c_hi, int lane,
+                                            int scale, int off, unsigned long long tau,
+                                            unsigned long long *cand, int *ncand) {
+  const float ts = (tau >> 32) == 0 ? -INFINITY : unord_float((uint32_t)(tau >> 32));
+  auto offer = [&](float v, int c) {
+    if (!(v >= ts)) return;
+    const unsigned long long key = make_key(v, c * scale + off);
+    if (key >= tau) {
+      const int slot = atomicAdd(ncand, 1);
+      if (slot < kCandCap) cand[slot] = key;
+    }
+  };
+  if constexpr (VEC) {
+    const float4 *r4 = reinterpret_cast<const float4 *>(src);
+    const int f_lo = c_lo >> 2, f_hi = (c_hi + 3) >> 2;
+    for (int f = f_lo + lane; f < f_hi; f += 32) {
+      const float4 x = __ldg(r4 + f);
+      const float vv[4] = {x.x, x.y, x.z, x.w};
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        const int c = 4 * f + k;
+        if ((unsigned)(c - c_lo) < (unsigned)(c_hi - c_lo)) offer(vv[k], c);
+      }
+    }
+  } else {
+    for (int c = c_lo + lane; c < c_hi; c += 32) offer(__ldg(src + c), c);
+  }
+}
+
+// The m largest keys < prev among this lane's free columns, by rounds (the
+// exact path for rows whose candidates overflow the buffer).
+template <bool VEC>
+__device__ void rounds_from_row(const float *src, int c_lo, int c_hi, int lane, int scale,
+                                int off, int m, unsigned long long *sel) {
+  unsigned long long prev = ~0ull;
+  for (int r = 0; r < m; ++r) {
+    unsigned long long local = 0;
+    for (int c = c_lo + lane; c < c_hi; c += 32) {
+      const unsigned long long key = make_key(__ldg(src + c), c * scale + off);
+      if (key < prev && key > local) local = key;
+    }
+    const unsigned long long w = warp_max_key(local);
+    if (lane == 0) sel[r] = w;
+    prev = w;
+    if (w == 0) break;
+  }
+  (void)VEC;
+}
+
+template <bool PUBLISH, bool VEC>
+__global__ void __launch_bounds__(32 * kSelWarps, 8) select_warp_kernel(const SelectArgs a) {
+  __shared__ unsigned long long s_cand[kSelWarps][kCandCap];
+  __shared__ unsigned long long s_sel[kSelWarps][kTopK];
+  __shared__ int s_nc[kSelWarps];
+
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int K = a.K;
+  const int rows = a.T * 4;
+  const int scale = a.index_scale, off = a.index_offset;
+  unsigned long long *cand = s_cand[warp];
+  unsigned long long *sel = s_sel[warp];
+
+  for (int row = blockIdx.x * kSelWarps + warp; row < rows; row += gridDim.x * kSelWarps) {
+    const int t = row >> 2, h = row & 3;
+    const int nvp = __ldg(a.nvp + t);
+    const float *src = a.scores + (long long)row * K;
+
+    // forced ids in increasing order: every valid id when nvp <= 16, else
+    // [0, init) then [nvp - local, nvp); lane f < nf holds the f-th
+    int fid = 0x7FFFFFFF;
+    float fsc = -INFINITY;
+    int nf;
+    {
+      const bool all = nvp <= kTopK;
+      const int nforced = all ? max(nvp, 0) : a.init_blocks + a.local_blocks;
+      int id = -1, col = 0;
+      bool ok = false;
+      if (lane < nforced && lane < kTopK) {
+        id = all ? lane
+                 : (lane < a.init_blocks ? lane : nvp - a.local_blocks + (lane - a.init_blocks));
+        const int d = id - off;
+        if (scale == 1) {
+          col = d;
+          ok = id >= 0 && id < nvp && d >= 0 && d < K;
+        } else {
+          col = d / scale;
+          ok = id >= 0 && id < nvp && d >= 0 && d % scale == 0 && col < K;
+        }
+      }
+      const float v = ok ? __ldg(src + col) : 0.0f;
+      const unsigned bal = __ballot_sync(0xFFFFFFFFu, ok);
+      nf = __popc(bal);
+      // move entry of lane L (pos p) to lane p
+      const int pos = __popc(bal & ((1u << lane) - 1u));
+      for (int p = 0; p < nf; ++p) {
+        const int srcl = __fns(bal, 0, p + 1);
+        const int i2 = __shfl_sync(0xFFFFFFFFu, id, srcl);
+        const float v2 = __shfl_sync(0xFFFFFFFFu, v, srcl);
+        if (lane == p) {
+          fid = i2;
+          fsc = v2;
+        }
+      }
+      (void)pos;
+    }
+    const int m = kTopK - nf;
+
+    // free columns: ids in [init, nvp - local) when nvp > 16, else none
+    int c_lo = 0, c_hi = 0;
+    if (nvp > kTopK) {
+      const int id_lo = a.init_blocks, id_hi = nvp - a.local_blocks;
+      c_lo = id_lo - off <= 0 ? 0 : (id_lo - off + scale - 1) / scale;
+      c_hi = id_hi - off <= 0 ? 0 : (id_hi - off + scale - 1) / scale;
+      c_hi = min(c_hi, K);
+      c_lo = min(c_lo, c_hi);
+    }
+    float best = 0.0f;
+    int bc = -1;
+    scan_row<VEC>(src, c_lo, c_hi, lane, best, bc);
+    const unsigned long long tm = bc < 0 ? 0ull : make_key(best, bc * scale + off);
+
+    // tau = m-th largest lane best (1 = fewer than m lanes hold an entry)
+    unsigned long long tau = 0;
+    {
+      unsigned long long my = tm;
+      int found = 0;
+      for (int r = 0; r < m; ++r) {
+        const unsigned long long w = warp_max_key(my);
+        if (w == 0) break;
+        tau = w;
+        ++found;
+        if (my == w) my = 0;
+      }
+      if (found < m) tau = 1;
+    }
+    if (lane == 0) s_nc[warp] = 0;
+    __syncwarp();
+    if (m > 0 && tm != 0 && tm >= tau)
+      collect_row<VEC>(src, c_lo, c_hi, lane, scale, off, tau, cand, &s_nc[warp]);
+    __syncwarp();
+    const int nc = s_nc[warp];
+    int nch = 0;
+    if (m > 0) {
+      if (nc > kCandCap) {
+        rounds_from_row<VEC>(src, c_lo, c_hi, lane, scale, off, m, sel);
+        nch = 0;
+        __syncwarp();
+        for (int r = 0; r < m; ++r) nch += sel[r] != 0 ? 1 : 0;
+      } else if (nc <= m) {
+        for (int j = lane; j < nc; j += 32) sel[j] = cand[j];
+        nch = nc;
+      } else {
+        // rank each candidate among the others (nc <= 256: 8 per lane)
+        for (int j = lane; j < nc; j += 32) {
+          const unsigned long long my = cand[j];
+          int rank = 0;
+          for (int i = 0; i < nc; ++i) rank += (cand[i] > my) ? 1 : 0;
+          if (rank < m) sel[rank] = my;
+        }
+        nch = m;
+      }
+    }
+    __syncwarp();
+    const int n = nf + nch;
+    int my_id = fid;
+    float my_sc = fsc;
+    if (lane >= nf && lane < n) {
+      my_id = key_id(sel[lane - nf]);
+      const int d = my_id - off;
+      my_sc = __ldg(src + (scale == 1 ? d : d / scale));  // raw score bits
+    }
+    int out_id;
+    float out_sc;
+    sort_by_id_16(lane, n, my_id, my_sc, out_id, out_sc);
+    if constexpr (!PUBLISH) {
+      if (lane < kTopK) {
+        a.out_scores[(long long)row * kTopK + lane] = out_sc;
+        a.out_ids[(long long)row * kTopK + lane] = out_id;
+      }
+    } else {
+      const int hpr = a.heads_per_rank;
+      int *base = reinterpret_cast<int *>(a.recv_bases[h / hpr]);
+      const long long r =
+          (((long long)a.slot * a.world_size + a.rank) * hpr + h % hpr) * a.capacity + t;
+      int *dst = base + r * kRowWords;
+      int ok = 0;
+      if (lane == 0) ok = poll_flag(dst + 32, 0, a.spin_limit) ? 1 : 0;
+      ok = __shfl_sync(0xFFFFFFFFu, ok, 0);
+      if (!ok) {
+        if (lane == 0) atomicAdd(a.errors, 1);
+      } else {
+        if (lane < kTopK) {
+          dst[lane] = __float_as_int(out_sc);
+          dst[kTopK + lane] = out_id;
+        }
+        __threadfence();
+        __syncwarp();
+        if (lane == 0) st_release_gpu(dst + 32, 1);
+      }
+    }
+    __syncwarp();
   }
 }
 
@@ -428,33 +701,39 @@ __global__ void __launch_bounds__(128) merge_kernel(const MergeArgs a) {
 
 }  // namespace
 
-constexpr int kSmallK = 1024;
+constexpr int kWarpRowMaxK = 2048;  // rows up to this long: one warp per row
 constexpr int kLargeK = 12288;
 
 cudaError_t select_prepare() {
   const int big = 2 * kLargeK * 4;
-  cudaError_t e;
-  e = cudaFuncSetAttribute(select_kernel<256, kLargeK, false>,
-                           cudaFuncAttributeMaxDynamicSharedMemorySize, big);
+  cudaError_t e = cudaFuncSetAttribute(select_block_kernel<256, kLargeK, false>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, big);
   if (e != cudaSuccess) return e;
-  return cudaFuncSetAttribute(select_kernel<256, kLargeK, true>,
+  return cudaFuncSetAttribute(select_block_kernel<256, kLargeK, true>,
                               cudaFuncAttributeMaxDynamicSharedMemorySize, big);
 }
 
 cudaError_t launch_select(const SelectArgs &a, bool publish, int sm_count, cudaStream_t stream) {
   const int rows = a.T * 4;
   if (rows == 0) return cudaSuccess;
-  // two row buffers; rows start 16-byte aligned when K % 4 == 0
-  if (a.K <= kSmallK) {
-    const size_t smem = 2 * (size_t)((kSmallK + 3) / 4 * 4) * 4;
-    const int grid = rows < 8 * sm_count ? rows : 8 * sm_count;
-    if (publish) select_kernel<128, kSmallK, true><<<grid, 128, smem, stream>>>(a);
-    else select_kernel<128, kSmallK, false><<<grid, 128, smem, stream>>>(a);
-  } else {
-    const size_t smem = 2 * (size_t)((kLargeK + 3) / 4 * 4) * 4;
+  if (a.K > kWarpRowMaxK) {
+    // long rows: two CTAs per SM, each double-buffering rows in shared memory
+    const size_t smem = 2 * (size_t)kLargeK * 4;
     const int grid = rows < 2 * sm_count ? rows : 2 * sm_count;
-    if (publish) select_kernel<256, kLargeK, true><<<grid, 256, smem, stream>>>(a);
-    else select_kernel<256, kLargeK, false><<<grid, 256, smem, stream>>>(a);
+    if (publish) select_block_kernel<256, kLargeK, true><<<grid, 256, smem, stream>>>(a);
+    else select_block_kernel<256, kLargeK, false><<<grid, 256, smem, stream>>>(a);
+    return cudaGetLastError();
+  }
+  // short rows: one warp per row; float4 loads when every row is 16-byte aligned
+  const bool vec = (a.K % 4 == 0) && ((reinterpret_cast<uintptr_t>(a.scores) & 15u) == 0);
+  const int grid = (rows + kSelWarps - 1) / kSelWarps;
+  const int threads = 32 * kSelWarps;
+  if (publish) {
+    if (vec) select_warp_kernel<true, true><<<grid, threads, 0, stream>>>(a);
+    else select_warp_kernel<true, false><<<grid, threads, 0, stream>>>(a);
+  } else {
+    if (vec) select_warp_kernel<false, true><<<grid, threads, 0, stream>>>(a);
+    else select_warp_kernel<false, false><<<grid, threads, 0, stream>>>(a);
   }
   return cudaGetLastError();
 }

@@ -83,3 +83,32 @@ def test_select_on_gpu_plane_of_batched_workload():
     os_, oi = oracle.select(plane.cpu().numpy(), inp.num_valid_pages.numpy(), init_blocks=1,
                             local_blocks=4)
     assert_select_equal(gs, gi, os_, oi, "batched plane")
+
+
+def test_candidate_overflow_takes_the_exact_fallback():
+    # Rows up to 2048 columns are read by one warp with float4 loads, lane l
+    # owning columns 4 * (l + 32 j) .. + 3.  Making every column of lanes
+    # 0..15 larger than the rest leaves about 16 * 64 keys above the
+    # threshold, more than the per-warp candidate buffer, which exercises the
+    # exact fallback selection.
+    K = 2048
+    plane = torch.randn((3, 4, K))
+    lanes = torch.arange(16)
+    cols = (4 * (lanes[:, None, None] + 32 * torch.arange(K // 128)[None, :, None])
+            + torch.arange(4)[None, None, :]).reshape(-1)
+    plane[:, :, cols] = 100.0 + torch.rand(cols.numel())
+    plane[1, :, cols] = 100.0                       # and all tied
+    nvp = torch.tensor([K, K, K // 2], dtype=torch.int32)
+    for init, local in [(0, 0), (2, 3)]:
+        _check(plane, nvp, init, local, what=f"overflow init={init} local={local}")
+
+
+def test_long_rows_with_concentrated_maxima():
+    # the same concentration on rows long enough for the block-per-row kernel
+    K = 12284
+    plane = torch.randn((3, 4, K))
+    cols = torch.arange(0, K, 256)
+    plane[:, :, cols] = 100.0 + torch.rand(cols.numel())
+    plane[1, :, cols] = 100.0
+    nvp = torch.tensor([K, K, K // 3], dtype=torch.int32)
+    _check(plane, nvp, 2, 3, what="long rows")
