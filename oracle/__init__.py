@@ -63,6 +63,9 @@ def _load():
     lib.icp_orc_recv_row.argtypes = [i32, i32, i32, i32, i32, i32, i32]
     lib.icp_orc_publish.argtypes = [P, i32, i32, P, P, i32, i32, i32, i32, i32, i32, i32, i32, i32]
     lib.icp_orc_merge.argtypes = [P, P, i32, i32, i32, i32, i32, i32, i32, i32, P, P]
+    lib.icp_orc_publish_tagged.argtypes = [P, i32, i32, P, P, P, i32, i32, i32, i32, i32, i32, i32,
+                                           i32, i32]
+    lib.icp_orc_merge_tagged.argtypes = [P, P, P, i32, i32, i32, i32, i32, i32, i32, P, P]
     _lib = lib
     return lib
 
@@ -188,6 +191,43 @@ def merge(recv, num_valid_pages, *, T, slot, owner, world_size, heads_per_rank, 
                            capacity, init_blocks, local_blocks, _ptr(out_s), _ptr(out_i))
     if rc < 0:
         raise ValueError("icp_orc_merge failed")
+    return out_s, out_i, rc
+
+
+def publish_tagged(scores, num_valid_pages, recv, generations, *, slot, rank, world_size,
+                   heads_per_rank, capacity, force_begin_blocks, force_end_blocks,
+                   index_scale=1, index_offset=0):
+    """Tagged publish into ``recv`` (ws int64 arrays [rows, 32]); advances
+    ``generations`` (int32 [3, ws*hpr, capacity])."""
+    lib = _load()
+    sc = _c(scores, np.float32)
+    nvp = _c(num_valid_pages, np.int32)
+    T, H, K = sc.shape
+    for r in recv:
+        assert r.dtype == np.int64 and r.flags.c_contiguous
+    assert generations.dtype == np.int32 and generations.flags.c_contiguous
+    arr = (ctypes.c_void_p * world_size)(*[r.ctypes.data for r in recv])
+    rc = lib.icp_orc_publish_tagged(_ptr(sc), T, K, _ptr(nvp), arr, _ptr(generations), slot, rank,
+                                    world_size, heads_per_rank, capacity, force_begin_blocks,
+                                    force_end_blocks, index_scale, index_offset)
+    if rc < 0:
+        raise ValueError("icp_orc_publish_tagged failed")
+
+
+def merge_tagged(recv, expected, num_valid_pages, *, T, slot, world_size, heads_per_rank,
+                 capacity, init_blocks, local_blocks):
+    """Owner merge of tagged rows -> (scores, ids, #sources that had not arrived)."""
+    lib = _load()
+    assert recv.dtype == np.int64 and recv.flags.c_contiguous
+    assert expected.dtype == np.int32 and expected.flags.c_contiguous
+    nvp = _c(num_valid_pages, np.int32)
+    out_s = np.empty((T, heads_per_rank, TOPK), np.float32)
+    out_i = np.empty((T, heads_per_rank, TOPK), np.int32)
+    rc = lib.icp_orc_merge_tagged(_ptr(recv), _ptr(expected), _ptr(nvp), T, slot, world_size,
+                                  heads_per_rank, capacity, init_blocks, local_blocks,
+                                  _ptr(out_s), _ptr(out_i))
+    if rc < 0:
+        raise ValueError("icp_orc_merge_tagged failed")
     return out_s, out_i, rc
 
 

@@ -508,3 +508,123 @@ int icp_orc_merge(int32_t *recv, const int32_t *num_valid_pages, int T, int slot
         }
     return missing;
 }
+
+/* ------------------------------------------------------------------------ */
+/* Tagged receive rows [SELECT description, parameter generations]          */
+/* ------------------------------------------------------------------------ */
+/*
+ * A tagged row is 32 int64 words, word i = (generation << 32) | payload_i,
+ * payload 0..15 the fp32 bits of the scores and 16..31 the ids (the legacy
+ * row without its ready flag).  Readings where the pages are silent:
+ *   - the publisher keeps counters generations[slot][h][t] (int32
+ *     [3, ws*hpr, capacity], zeroed once) and publishes row (t, h) with
+ *     generation = counter + 1, storing the new value back;
+ *   - the owner keeps expected counters expected[slot][src][hl][t] (int32
+ *     [3, ws, hpr, capacity], zeroed once); a merge of slot `slot` takes a
+ *     source row as arrived when all 32 words carry expected + 1, and the
+ *     counter advances on every merge, arrived or not;
+ *   - nothing waits for a free row: the pages require at least two sparse
+ *     layers between uses of a slot set instead.
+ */
+int icp_orc_publish_tagged(const float *scores, int T, int K, const int32_t *num_valid_pages,
+                           int64_t *const *recv, int32_t *generations, int slot, int rank,
+                           int world_size, int heads_per_rank, int capacity,
+                           int force_begin_blocks, int force_end_blocks, int index_scale,
+                           int index_offset)
+{
+    int heads = world_size * heads_per_rank;
+    float *sc = NULL;
+    int32_t *id = NULL;
+    if (T > capacity || slot < 0 || slot > 2 || rank < 0 || rank >= world_size)
+        return -1;
+    sc = (float *)malloc(sizeof(float) * (size_t)T * heads * ORC_TOPK);
+    id = (int32_t *)malloc(sizeof(int32_t) * (size_t)T * heads * ORC_TOPK);
+    if (!sc || !id) {
+        free(sc);
+        free(id);
+        return -1;
+    }
+    if (icp_orc_select(scores, T, heads, K, num_valid_pages, force_begin_blocks,
+                       force_end_blocks, index_scale, index_offset, sc, id) != 0) {
+        free(sc);
+        free(id);
+        return -1;
+    }
+    for (int t = 0; t < T; ++t)
+        for (int h = 0; h < heads; ++h) {
+            int32_t *gen = generations + ((int64_t)slot * heads + h) * capacity + t;
+            uint32_t g = (uint32_t)(*gen) + 1u;
+            int64_t *row = recv[h / heads_per_rank] +
+                           icp_orc_recv_row(slot, rank, world_size, heads_per_rank, h,
+                                            capacity, t) *
+                               32;
+            for (int i = 0; i < 32; ++i) {
+                uint32_t payload;
+                if (i < ORC_TOPK)
+                    memcpy(&payload, &sc[((int64_t)t * heads + h) * ORC_TOPK + i], 4);
+                else
+                    payload = (uint32_t)id[((int64_t)t * heads + h) * ORC_TOPK + i - ORC_TOPK];
+                row[i] = (int64_t)(((uint64_t)g << 32) | payload);
+            }
+            *gen = (int32_t)g;
+        }
+    free(sc);
+    free(id);
+    return 0;
+}
+
+int icp_orc_merge_tagged(const int64_t *recv, int32_t *expected, const int32_t *num_valid_pages,
+                         int T, int slot, int world_size, int heads_per_rank, int capacity,
+                         int init_blocks, int local_blocks, float *out_scores, int32_t *out_ids)
+{
+    int missing = 0;
+    int32_t ids[4 * ORC_TOPK];
+    float sc[4 * ORC_TOPK];
+    if (world_size < 1 || world_size > 4 || T > capacity || slot < 0 || slot > 2)
+        return -1;
+    for (int t = 0; t < T; ++t)
+        for (int hl = 0; hl < heads_per_rank; ++hl) {
+            int n = 0;
+            int64_t o = ((int64_t)t * heads_per_rank + hl) * ORC_TOPK;
+            for (int s = 0; s < world_size; ++s) {
+                int32_t *e = expected +
+                             (((int64_t)slot * world_size + s) * heads_per_rank + hl) * capacity + t;
+                uint32_t want = (uint32_t)(*e) + 1u;
+                const int64_t *row = recv + icp_orc_recv_row(slot, s, world_size, heads_per_rank,
+                                                             hl, capacity, t) *
+                                                32;
+                int arrived = 1;
+                *e = (int32_t)want;
+                for (int i = 0; i < 32; ++i)
+                    if ((uint32_t)((uint64_t)row[i] >> 32) != want)
+                        arrived = 0;
+                if (!arrived) {
+                    missing++;
+                    continue;
+                }
+                for (int i = 0; i < ORC_TOPK; ++i) {
+                    float v;
+                    uint32_t pb = (uint32_t)((uint64_t)row[i] & 0xFFFFFFFFu);
+                    int32_t d = (int32_t)(uint32_t)((uint64_t)row[ORC_TOPK + i] & 0xFFFFFFFFu);
+                    int found = -1;
+                    memcpy(&v, &pb, 4);
+                    if (d == -1)
+                        continue;
+                    for (int q = 0; q < n; ++q)
+                        if (ids[q] == d)
+                            found = q;
+                    if (found < 0) {
+                        ids[n] = d;
+                        sc[n] = v;
+                        n++;
+                    } else if (v > sc[found]) {
+                        sc[found] = v;
+                    }
+                }
+            }
+            if (icp_orc_select_pairs(n, ids, sc, num_valid_pages[t], init_blocks, local_blocks,
+                                     out_scores + o, out_ids + o) < 0)
+                return -1;
+        }
+    return missing;
+}
