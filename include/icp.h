@@ -158,6 +158,47 @@ int icp_merge(int32_t *recv, const int32_t *num_valid_pages, int T, int slot, in
               void *stream);
 
 /*
+ * Tagged publish (msa_icp_topk_select_publish with `generations`: tagged
+ * mode).  The same Top16 select as icp_publish_rows; row (t, h) goes to owner
+ * h / heads_per_rank at the same row index, as 32 int64 words
+ * (generation << 32) | word, word 0-15 the fp32 bits of the scores and
+ * 16-31 the ascending ids.
+ *   recv_bases   int64 [world_size] DEVICE array of device addresses of each
+ *                owner's tagged storage, int64 [3][world_size][hpr][capacity][32],
+ *                8-byte aligned.
+ *   generations  int32 [3, world_size * heads_per_rank, capacity] DEVICE
+ *                publish counters of this rank, zeroed once by the caller and
+ *                never between steps: row (t, h) of slot s is published with
+ *                generation generations[s][h][t] + 1, which is stored back.
+ *   Nothing waits for a free row: as the page states, tagged mode needs at
+ *   least two sparse layers between uses of one slot set.  Every row t < T,
+ *   padding rows included, is written on every call.  Limits as
+ *   icp_publish_rows (no spin_limit, no errors).
+ */
+int icp_publish_rows_tagged(const float *scores, int T, int K, const int32_t *num_valid_pages,
+                            const int64_t *recv_bases, int32_t *generations, int slot, int rank,
+                            int world_size, int heads_per_rank, int capacity,
+                            int force_begin_blocks, int force_end_blocks, int index_scale,
+                            int index_offset, void *stream);
+
+/*
+ * Owner merge of tagged rows (this library's reading; the counters of the
+ * receiving side are described on a page the documentation does not carry).
+ *   recv      this owner's tagged storage, int64 [3][world_size][hpr][capacity][32].
+ *   expected  int32 [3][world_size][hpr][capacity] DEVICE counters of this owner,
+ *             zeroed once.  A merge of slot s takes the source row of rank r
+ *             as arrived when all 32 words carry generation expected + 1; the
+ *             counter advances on every merge.  Each wait is bounded by
+ *             spin_limit polls and about two seconds; a source that has not
+ *             arrived is left out and adds 1 to errors[0].
+ *   Output and rule as icp_merge.  Rows are not modified (no flags to free).
+ */
+int icp_merge_tagged(const int64_t *recv, int32_t *expected, const int32_t *num_valid_pages,
+                     int T, int slot, int world_size, int heads_per_rank, int capacity,
+                     int init_blocks, int local_blocks, int64_t spin_limit, int32_t *errors,
+                     float *out_scores, int32_t *out_ids, void *stream);
+
+/*
  * Workspace bytes icp_score_select needs for `batch` requests of
  * decode_query_len tokens (per-request partial Top16 lists and counters).
  * Returns 0 for invalid arguments.  Host only.

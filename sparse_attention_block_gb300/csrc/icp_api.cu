@@ -206,7 +206,7 @@ int icp_top16_select(const float *scores, int T, int K, const int32_t *num_valid
   a.index_offset = index_offset;
   a.out_scores = out_scores;
   a.out_ids = out_ids;
-  return to_status(icp::launch_select(a, false, sms, static_cast<cudaStream_t>(stream)));
+  return to_status(icp::launch_select(a, 0, sms, static_cast<cudaStream_t>(stream)));
 }
 
 int icp_publish_rows(const float *scores, int T, int K, const int32_t *num_valid_pages,
@@ -243,7 +243,7 @@ int icp_publish_rows(const float *scores, int T, int K, const int32_t *num_valid
   a.heads_per_rank = heads_per_rank;
   a.capacity = capacity;
   a.spin_limit = spin_limit;
-  return to_status(icp::launch_select(a, true, sms, static_cast<cudaStream_t>(stream)));
+  return to_status(icp::launch_select(a, 1, sms, static_cast<cudaStream_t>(stream)));
 }
 
 int icp_merge(int32_t *recv, const int32_t *num_valid_pages, int T, int slot, int world_size,
@@ -261,6 +261,7 @@ int icp_merge(int32_t *recv, const int32_t *num_valid_pages, int T, int slot, in
   int st = current_device(&dev, &sms);
   if (st != ICP_OK) return st;
   icp::MergeArgs a;
+  memset(&a, 0, sizeof(a));
   a.recv = recv;
   a.nvp = num_valid_pages;
   a.T = T;
@@ -274,7 +275,78 @@ int icp_merge(int32_t *recv, const int32_t *num_valid_pages, int T, int slot, in
   a.errors = errors;
   a.out_scores = out_scores;
   a.out_ids = out_ids;
-  return to_status(icp::launch_merge(a, static_cast<cudaStream_t>(stream)));
+  return to_status(icp::launch_merge(a, false, static_cast<cudaStream_t>(stream)));
+}
+
+int icp_publish_rows_tagged(const float *scores, int T, int K, const int32_t *num_valid_pages,
+                            const int64_t *recv_bases, int32_t *generations, int slot, int rank,
+                            int world_size, int heads_per_rank, int capacity,
+                            int force_begin_blocks, int force_end_blocks, int index_scale,
+                            int index_offset, void *stream) {
+  if (!valid_select_common(T, K, force_begin_blocks, force_end_blocks, index_scale,
+                           index_offset))
+    return ICP_ERR_INVALID_ARG;
+  if (world_size != 1 && world_size != 2 && world_size != 4) return ICP_ERR_INVALID_ARG;
+  if (heads_per_rank * world_size != ICP_HEADS) return ICP_ERR_INVALID_ARG;
+  if (rank < 0 || rank >= world_size || slot < 0 || slot > 2) return ICP_ERR_INVALID_ARG;
+  if (T < 1 || T > capacity) return ICP_ERR_INVALID_ARG;
+  if (!scores || !num_valid_pages || !recv_bases || !generations) return ICP_ERR_INVALID_ARG;
+  int dev = 0, sms = 0;
+  int st = current_device(&dev, &sms);
+  if (st != ICP_OK) return st;
+  icp::SelectArgs a;
+  memset(&a, 0, sizeof(a));
+  a.scores = scores;
+  a.T = T;
+  a.K = K;
+  a.nvp = num_valid_pages;
+  a.init_blocks = force_begin_blocks;
+  a.local_blocks = force_end_blocks;
+  a.index_scale = index_scale;
+  a.index_offset = index_offset;
+  a.recv_bases = recv_bases;
+  a.generations = generations;
+  a.slot = slot;
+  a.rank = rank;
+  a.world_size = world_size;
+  a.heads_per_rank = heads_per_rank;
+  a.capacity = capacity;
+  return to_status(icp::launch_select(a, 2, sms, static_cast<cudaStream_t>(stream)));
+}
+
+int icp_merge_tagged(const int64_t *recv, int32_t *expected, const int32_t *num_valid_pages,
+                     int T, int slot, int world_size, int heads_per_rank, int capacity,
+                     int init_blocks, int local_blocks, int64_t spin_limit, int32_t *errors,
+                     float *out_scores, int32_t *out_ids, void *stream) {
+  if (world_size != 1 && world_size != 2 && world_size != 4) return ICP_ERR_INVALID_ARG;
+  if (heads_per_rank * world_size != ICP_HEADS) return ICP_ERR_INVALID_ARG;
+  if (slot < 0 || slot > 2 || T < 1 || T > capacity || spin_limit < 1)
+    return ICP_ERR_INVALID_ARG;
+  if (init_blocks < 0 || local_blocks < 0 || init_blocks + local_blocks > ICP_TOPK)
+    return ICP_ERR_INVALID_ARG;
+  if (!recv || !expected || !num_valid_pages || !errors || !out_scores || !out_ids)
+    return ICP_ERR_INVALID_ARG;
+  if ((reinterpret_cast<uintptr_t>(recv) & 7u) != 0) return ICP_ERR_INVALID_ARG;
+  int dev = 0, sms = 0;
+  int st = current_device(&dev, &sms);
+  if (st != ICP_OK) return st;
+  icp::MergeArgs a;
+  memset(&a, 0, sizeof(a));
+  a.recv64 = reinterpret_cast<const unsigned long long *>(recv);
+  a.expected = expected;
+  a.nvp = num_valid_pages;
+  a.T = T;
+  a.slot = slot;
+  a.world_size = world_size;
+  a.heads_per_rank = heads_per_rank;
+  a.capacity = capacity;
+  a.init_blocks = init_blocks;
+  a.local_blocks = local_blocks;
+  a.spin_limit = spin_limit;
+  a.errors = errors;
+  a.out_scores = out_scores;
+  a.out_ids = out_ids;
+  return to_status(icp::launch_merge(a, true, static_cast<cudaStream_t>(stream)));
 }
 
 size_t icp_score_select_workspace_bytes(int batch, int decode_query_len) {

@@ -52,6 +52,7 @@ struct SelectArgs {
   int32_t *errors;
   int slot, rank, world_size, heads_per_rank, capacity;
   long long spin_limit;
+  int32_t *generations;  // tagged publish: [3][ws * hpr][capacity] counters
 };
 
 struct MergeArgs {
@@ -62,6 +63,8 @@ struct MergeArgs {
   int32_t *errors;
   float *out_scores;
   int32_t *out_ids;
+  const unsigned long long *recv64;  // tagged merge: this owner's tagged rows
+  int32_t *expected;                 // tagged merge: [3][ws][hpr][capacity] counters
 };
 
 // Launchers (return a cudaError_t from the launch).
@@ -75,7 +78,8 @@ cudaError_t launch_score_select(const CUtensorMap &tmk, const CUtensorMap &tmq, 
                                 int grid, cudaStream_t stream);
 
 cudaError_t select_prepare();  // one-time per-device kernel attributes
-cudaError_t launch_select(const SelectArgs &a, bool publish, int sm_count, cudaStream_t stream);
-cudaError_t launch_merge(const MergeArgs &a, cudaStream_t stream);
+// mode: 0 plain output, 1 legacy receive rows, 2 tagged receive rows
+cudaError_t launch_select(const SelectArgs &a, int mode, int sm_count, cudaStream_t stream);
+cudaError_t launch_merge(const MergeArgs &a, bool tagged, cudaStream_t stream);
 
 }  // namespace icp

@@ -37,7 +37,61 @@ __device__ __forceinline__ bool poll_flag(const int *flag, int want, long long s
 // ... and stages them in shared memory with bulk async copies into two
 // buffers, so the next row streams in while the current one is processed.
 // MAXK bounds the row length of the variant.
-template <int NT, int MAXK, bool PUBLISH>
+// Where a selected row goes: the plain output arrays, a legacy receive row
+// (bounded wait for a free row, 32 data words, release-stored ready flag) or
+// a tagged receive row (32 int64 words of generation << 32 | word, the
+// generation taken from the publisher's counter for (slot, head, token)).
+enum EmitMode { kEmitPlain = 0, kEmitLegacy = 1, kEmitTagged = 2 };
+
+template <int MODE>
+__device__ __forceinline__ void emit_row(const SelectArgs &a, int lane, int row, int t, int h,
+                                         int out_id, float out_sc) {
+  if constexpr (MODE == kEmitPlain) {
+    if (lane < kTopK) {
+      a.out_scores[(long long)row * kTopK + lane] = out_sc;
+      a.out_ids[(long long)row * kTopK + lane] = out_id;
+    }
+  } else {
+    const int hpr = a.heads_per_rank;
+    const long long r =
+        (((long long)a.slot * a.world_size + a.rank) * hpr + h % hpr) * a.capacity + t;
+    if constexpr (MODE == kEmitLegacy) {
+      int *dst = reinterpret_cast<int *>(a.recv_bases[h / hpr]) + r * kRowWords;
+      int ok = 0;
+      if (lane == 0) ok = poll_flag(dst + 32, 0, a.spin_limit) ? 1 : 0;
+      ok = __shfl_sync(0xFFFFFFFFu, ok, 0);
+      if (!ok) {
+        if (lane == 0) atomicAdd(a.errors, 1);
+      } else {
+        if (lane < kTopK) {
+          dst[lane] = __float_as_int(out_sc);
+          dst[kTopK + lane] = out_id;
+        }
+        __threadfence();
+        __syncwarp();
+        if (lane == 0) st_release_gpu(dst + 32, 1);
+      }
+    } else {
+      int *gen = a.generations +
+                 ((long long)a.slot * (a.world_size * hpr) + h) * a.capacity + t;
+      unsigned g = 0;
+      if (lane == 0) {
+        g = (unsigned)*gen + 1u;
+        *gen = (int)g;
+      }
+      g = __shfl_sync(0xFFFFFFFFu, g, 0);
+      const unsigned sb = __shfl_sync(0xFFFFFFFFu, __float_as_uint(out_sc), lane & 15);
+      const unsigned ib = __shfl_sync(0xFFFFFFFFu, (unsigned)out_id, lane & 15);
+      const unsigned long long word =
+          ((unsigned long long)g << 32) | (unsigned long long)(lane < kTopK ? sb : ib);
+      unsigned long long *dst =
+          reinterpret_cast<unsigned long long *>(a.recv_bases[h / hpr]) + r * 32;
+      st_relaxed_gpu_u64(dst + lane, word);
+    }
+  }
+}
+
+template <int NT, int MAXK, int MODE>
 __global__ void __launch_bounds__(NT) select_block_kernel(const SelectArgs a) {
   constexpr int NW = NT / 32;
   constexpr int EPT = ((MAXK + 4 * NT - 1) / (4 * NT)) * 4;  // row entries per thread
@@ -268,33 +322,7 @@ __global__ void __launch_bounds__(NT) select_block_kernel(const SelectArgs a) {
       int out_id;
       float out_sc;
       sort_by_id_16(lane, n, my_id, my_sc, out_id, out_sc);
-
-      if constexpr (!PUBLISH) {
-        if (lane < kTopK) {
-          a.out_scores[(long long)row * kTopK + lane] = out_sc;
-          a.out_ids[(long long)row * kTopK + lane] = out_id;
-        }
-      } else {
-        const int hpr = a.heads_per_rank;
-        int *base = reinterpret_cast<int *>(a.recv_bases[h / hpr]);
-        const long long r =
-            (((long long)a.slot * a.world_size + a.rank) * hpr + h % hpr) * a.capacity + t;
-        int *dst = base + r * kRowWords;
-        int ok = 0;
-        if (lane == 0) ok = poll_flag(dst + 32, 0, a.spin_limit) ? 1 : 0;
-        ok = __shfl_sync(0xFFFFFFFFu, ok, 0);
-        if (!ok) {
-          if (lane == 0) atomicAdd(a.errors, 1);
-        } else {
-          if (lane < kTopK) {
-            dst[lane] = __float_as_int(out_sc);
-            dst[kTopK + lane] = out_id;
-          }
-          __threadfence();
-          __syncwarp();
-          if (lane == 0) st_release_gpu(dst + 32, 1);
-        }
-      }
+      emit_row<MODE>(a, lane, row, t, h, out_id, out_sc);
     }
     __syncthreads();  // this row's buffer and scratch may be reused
   }
@@ -411,7 +439,7 @@ __device__ void rounds_from_row(const float *src, int c_lo, int c_hi, int lane, 
   (void)VEC;
 }
 
-template <bool PUBLISH, bool VEC>
+template <int MODE, bool VEC>
 __global__ void __launch_bounds__(32 * kSelWarps, 8) select_warp_kernel(const SelectArgs a) {
   __shared__ unsigned long long s_cand[kSelWarps][kCandCap];
   __shared__ unsigned long long s_sel[kSelWarps][kTopK];
@@ -536,86 +564,19 @@ __global__ void __launch_bounds__(32 * kSelWarps, 8) select_warp_kernel(const Se
     int out_id;
     float out_sc;
     sort_by_id_16(lane, n, my_id, my_sc, out_id, out_sc);
-    if constexpr (!PUBLISH) {
-      if (lane < kTopK) {
-        a.out_scores[(long long)row * kTopK + lane] = out_sc;
-        a.out_ids[(long long)row * kTopK + lane] = out_id;
-      }
-    } else {
-      const int hpr = a.heads_per_rank;
-      int *base = reinterpret_cast<int *>(a.recv_bases[h / hpr]);
-      const long long r =
-          (((long long)a.slot * a.world_size + a.rank) * hpr + h % hpr) * a.capacity + t;
-      int *dst = base + r * kRowWords;
-      int ok = 0;
-      if (lane == 0) ok = poll_flag(dst + 32, 0, a.spin_limit) ? 1 : 0;
-      ok = __shfl_sync(0xFFFFFFFFu, ok, 0);
-      if (!ok) {
-        if (lane == 0) atomicAdd(a.errors, 1);
-      } else {
-        if (lane < kTopK) {
-          dst[lane] = __float_as_int(out_sc);
-          dst[kTopK + lane] = out_id;
-        }
-        __threadfence();
-        __syncwarp();
-        if (lane == 0) st_release_gpu(dst + 32, 1);
-      }
-    }
+    emit_row<MODE>(a, lane, row, t, h, out_id, out_sc);
     __syncwarp();
   }
 }
 
-// One warp per (token, owned head).  Lane i < 16 holds entry i of every
-// source row (at most 4 sources), so the union, the per-id maximum and the
-// ranking are done with shuffles; the result is compacted through shared
-// memory and ordered by id.
-__global__ void __launch_bounds__(128) merge_kernel(const MergeArgs a) {
-  __shared__ int s_id[4][kTopK];
-  __shared__ float s_sc[4][kTopK];
-
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int item = blockIdx.x * 4 + warp;
+// Second half of a merge, once lane i < 16 holds entry i of every source in
+// ids[s] / scs[s] (id -1 = nothing): union with the maximum score per id,
+// the Top16 rule with num_valid_pages, and the output ordered by id.
+__device__ __forceinline__ void merge_finish(const MergeArgs &a, int lane, int t, int hl, int nvp,
+                                             const int (&ids)[4], const float (&scs)[4],
+                                             int *s_idw, float *s_scw) {
   const int hpr = a.heads_per_rank;
-  if (item >= a.T * hpr) return;
-  const int t = item / hpr, hl = item % hpr;
-  const int nvp = a.nvp[t];
   const int ws = a.world_size;
-
-  int ids[4];
-  float scs[4];
-  unsigned read_mask = 0;
-#pragma unroll
-  for (int s = 0; s < 4; ++s) {
-    ids[s] = -1;
-    scs[s] = -INFINITY;
-    if (s >= ws) continue;
-    const long long r = (((long long)a.slot * ws + s) * hpr + hl) * a.capacity + t;
-    int *row = a.recv + r * kRowWords;
-    int ok = 0;
-    if (lane == 0) ok = poll_flag(row + 32, 1, a.spin_limit) ? 1 : 0;
-    ok = __shfl_sync(0xFFFFFFFFu, ok, 0);
-    if (!ok) {
-      if (lane == 0) atomicAdd(a.errors, 1);
-      continue;
-    }
-    read_mask |= 1u << s;
-    if (lane < kTopK) {
-      (void)ld_acquire_gpu(row + 32);  // order this lane's reads after the flag
-      scs[s] = __int_as_float(row[lane]);
-      ids[s] = row[kTopK + lane];
-    }
-  }
-  __syncwarp();
-  // free the rows that were read
-  if (lane == 0) {
-    for (int s = 0; s < ws; ++s)
-      if (read_mask & (1u << s)) {
-        const long long r = (((long long)a.slot * ws + s) * hpr + hl) * a.capacity + t;
-        st_release_gpu(a.recv + r * kRowWords + 32, 0);
-      }
-  }
-
   // keep an entry unless another source holds the same id with a higher
   // score (an exact tie goes to the lower source)
   bool keep[4];
@@ -675,8 +636,8 @@ __global__ void __launch_bounds__(128) merge_kernel(const MergeArgs a) {
     if (sel[s]) {
       const int pos = n + __popc(bal & ((1u << lane) - 1u));
       if (pos < kTopK) {
-        s_id[warp][pos] = ids[s];
-        s_sc[warp][pos] = scs[s];
+        s_idw[pos] = ids[s];
+        s_scw[pos] = scs[s];
       }
     }
     n += __popc(bal);
@@ -686,8 +647,8 @@ __global__ void __launch_bounds__(128) merge_kernel(const MergeArgs a) {
   int my_id = 0x7FFFFFFF;
   float my_sc = -INFINITY;
   if (lane < n) {
-    my_id = s_id[warp][lane];
-    my_sc = s_sc[warp][lane];
+    my_id = s_idw[lane];
+    my_sc = s_scw[lane];
   }
   int out_id;
   float out_sc;
@@ -699,6 +660,115 @@ __global__ void __launch_bounds__(128) merge_kernel(const MergeArgs a) {
   }
 }
 
+// One warp per (token, owned head).  Lane i < 16 holds entry i of every
+// source row (at most 4 sources), so the union, the per-id maximum and the
+// ranking are done with shuffles; the result is compacted through shared
+// memory and ordered by id.
+__global__ void __launch_bounds__(128) merge_kernel(const MergeArgs a) {
+  __shared__ int s_id[4][kTopK];
+  __shared__ float s_sc[4][kTopK];
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int item = blockIdx.x * 4 + warp;
+  const int hpr = a.heads_per_rank;
+  if (item >= a.T * hpr) return;
+  const int t = item / hpr, hl = item % hpr;
+  const int nvp = a.nvp[t];
+  const int ws = a.world_size;
+
+  int ids[4];
+  float scs[4];
+  unsigned read_mask = 0;
+#pragma unroll
+  for (int s = 0; s < 4; ++s) {
+    ids[s] = -1;
+    scs[s] = -INFINITY;
+    if (s >= ws) continue;
+    const long long r = (((long long)a.slot * ws + s) * hpr + hl) * a.capacity + t;
+    int *row = a.recv + r * kRowWords;
+    int ok = 0;
+    if (lane == 0) ok = poll_flag(row + 32, 1, a.spin_limit) ? 1 : 0;
+    ok = __shfl_sync(0xFFFFFFFFu, ok, 0);
+    if (!ok) {
+      if (lane == 0) atomicAdd(a.errors, 1);
+      continue;
+    }
+    read_mask |= 1u << s;
+    if (lane < kTopK) {
+      (void)ld_acquire_gpu(row + 32);  // order this lane's reads after the flag
+      scs[s] = __int_as_float(row[lane]);
+      ids[s] = row[kTopK + lane];
+    }
+  }
+  __syncwarp();
+  // free the rows that were read
+  if (lane == 0) {
+    for (int s = 0; s < ws; ++s)
+      if (read_mask & (1u << s)) {
+        const long long r = (((long long)a.slot * ws + s) * hpr + hl) * a.capacity + t;
+        st_release_gpu(a.recv + r * kRowWords + 32, 0);
+      }
+  }
+
+  merge_finish(a, lane, t, hl, nvp, ids, scs, s_id[warp], s_sc[warp]);
+}
+
+// Owner merge of tagged rows: a source row has arrived when all 32 words
+// carry the owner's expected generation + 1 (the counter advances on every
+// merge).  Polls are bounded by spin_limit and the wait timeout.
+__global__ void __launch_bounds__(128) merge_tagged_kernel(const MergeArgs a) {
+  __shared__ int s_id[4][kTopK];
+  __shared__ float s_sc[4][kTopK];
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int item = blockIdx.x * 4 + warp;
+  const int hpr = a.heads_per_rank;
+  if (item >= a.T * hpr) return;
+  const int t = item / hpr, hl = item % hpr;
+  const int nvp = a.nvp[t];
+  const int ws = a.world_size;
+
+  int ids[4];
+  float scs[4];
+#pragma unroll
+  for (int s = 0; s < 4; ++s) {
+    ids[s] = -1;
+    scs[s] = -INFINITY;
+    if (s >= ws) continue;
+    const long long r = (((long long)a.slot * ws + s) * hpr + hl) * a.capacity + t;
+    int *e = a.expected + r;  // same [slot][src][hl][t] layout as the rows
+    unsigned want = 0;
+    if (lane == 0) {
+      want = (unsigned)*e + 1u;
+      *e = (int)want;
+    }
+    want = __shfl_sync(0xFFFFFFFFu, want, 0);
+    const unsigned long long *row = a.recv64 + r * 32;
+    const unsigned long long t0 = globaltimer_ns();
+    bool arrived = false;
+    unsigned long long w = 0;
+    for (long long it = 0; it < a.spin_limit; ++it) {
+      w = ld_relaxed_gpu_u64(row + lane);
+      if (__all_sync(0xFFFFFFFFu, (unsigned)(w >> 32) == want)) {
+        arrived = true;
+        break;
+      }
+      if ((it & 255) == 255 && globaltimer_ns() - t0 > kWaitTimeoutNs) break;
+    }
+    if (!arrived) {
+      if (lane == 0) atomicAdd(a.errors, 1);
+      continue;
+    }
+    const unsigned payload = (unsigned)w;
+    const unsigned idw = __shfl_sync(0xFFFFFFFFu, payload, (lane & 15) + kTopK);
+    if (lane < kTopK) {
+      scs[s] = __uint_as_float(payload);
+      ids[s] = (int)idw;
+    }
+  }
+  merge_finish(a, lane, t, hl, nvp, ids, scs, s_id[warp], s_sc[warp]);
+}
+
 }  // namespace
 
 constexpr int kWarpRowMaxK = 2048;  // rows up to this long: one warp per row
@@ -706,42 +776,53 @@ constexpr int kLargeK = 12288;
 
 cudaError_t select_prepare() {
   const int big = 2 * kLargeK * 4;
-  cudaError_t e = cudaFuncSetAttribute(select_block_kernel<256, kLargeK, false>,
+  cudaError_t e = cudaFuncSetAttribute(select_block_kernel<256, kLargeK, kEmitPlain>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, big);
   if (e != cudaSuccess) return e;
-  return cudaFuncSetAttribute(select_block_kernel<256, kLargeK, true>,
+  e = cudaFuncSetAttribute(select_block_kernel<256, kLargeK, kEmitLegacy>,
+                           cudaFuncAttributeMaxDynamicSharedMemorySize, big);
+  if (e != cudaSuccess) return e;
+  return cudaFuncSetAttribute(select_block_kernel<256, kLargeK, kEmitTagged>,
                               cudaFuncAttributeMaxDynamicSharedMemorySize, big);
 }
 
-cudaError_t launch_select(const SelectArgs &a, bool publish, int sm_count, cudaStream_t stream) {
+cudaError_t launch_select(const SelectArgs &a, int mode, int sm_count, cudaStream_t stream) {
   const int rows = a.T * 4;
   if (rows == 0) return cudaSuccess;
   if (a.K > kWarpRowMaxK) {
     // long rows: two CTAs per SM, each double-buffering rows in shared memory
     const size_t smem = 2 * (size_t)kLargeK * 4;
     const int grid = rows < 2 * sm_count ? rows : 2 * sm_count;
-    if (publish) select_block_kernel<256, kLargeK, true><<<grid, 256, smem, stream>>>(a);
-    else select_block_kernel<256, kLargeK, false><<<grid, 256, smem, stream>>>(a);
+    if (mode == kEmitLegacy)
+      select_block_kernel<256, kLargeK, kEmitLegacy><<<grid, 256, smem, stream>>>(a);
+    else if (mode == kEmitTagged)
+      select_block_kernel<256, kLargeK, kEmitTagged><<<grid, 256, smem, stream>>>(a);
+    else
+      select_block_kernel<256, kLargeK, kEmitPlain><<<grid, 256, smem, stream>>>(a);
     return cudaGetLastError();
   }
   // short rows: one warp per row; float4 loads when every row is 16-byte aligned
   const bool vec = (a.K % 4 == 0) && ((reinterpret_cast<uintptr_t>(a.scores) & 15u) == 0);
   const int grid = (rows + kSelWarps - 1) / kSelWarps;
   const int threads = 32 * kSelWarps;
-  if (publish) {
-    if (vec) select_warp_kernel<true, true><<<grid, threads, 0, stream>>>(a);
-    else select_warp_kernel<true, false><<<grid, threads, 0, stream>>>(a);
+  if (mode == kEmitLegacy) {
+    if (vec) select_warp_kernel<kEmitLegacy, true><<<grid, threads, 0, stream>>>(a);
+    else select_warp_kernel<kEmitLegacy, false><<<grid, threads, 0, stream>>>(a);
+  } else if (mode == kEmitTagged) {
+    if (vec) select_warp_kernel<kEmitTagged, true><<<grid, threads, 0, stream>>>(a);
+    else select_warp_kernel<kEmitTagged, false><<<grid, threads, 0, stream>>>(a);
   } else {
-    if (vec) select_warp_kernel<false, true><<<grid, threads, 0, stream>>>(a);
-    else select_warp_kernel<false, false><<<grid, threads, 0, stream>>>(a);
+    if (vec) select_warp_kernel<kEmitPlain, true><<<grid, threads, 0, stream>>>(a);
+    else select_warp_kernel<kEmitPlain, false><<<grid, threads, 0, stream>>>(a);
   }
   return cudaGetLastError();
 }
 
-cudaError_t launch_merge(const MergeArgs &a, cudaStream_t stream) {
+cudaError_t launch_merge(const MergeArgs &a, bool tagged, cudaStream_t stream) {
   const int items = a.T * a.heads_per_rank;
   if (items == 0) return cudaSuccess;
-  merge_kernel<<<(items + 3) / 4, 128, 0, stream>>>(a);
+  if (tagged) merge_tagged_kernel<<<(items + 3) / 4, 128, 0, stream>>>(a);
+  else merge_kernel<<<(items + 3) / 4, 128, 0, stream>>>(a);
   return cudaGetLastError();
 }
 

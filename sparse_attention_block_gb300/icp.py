@@ -51,6 +51,12 @@ lib.icp_score_select.argtypes = [_P, _P, _I64, _P, _I64, _P, _I32, _I32, _I32, _
 lib.icp_score_select_noalloc.restype = _I32
 lib.icp_score_select_noalloc.argtypes = [_P, _P, _I64, _P, _I64, _P, _I32, _I32, _I32, _I32,
                                          _I32, _I32, _I32, _P, _I32, _I32, _P, _P, _P, _P]
+lib.icp_publish_rows_tagged.restype = _I32
+lib.icp_publish_rows_tagged.argtypes = [_P, _I32, _I32, _P, _P, _P, _I32, _I32, _I32, _I32,
+                                        _I32, _I32, _I32, _I32, _I32, _P]
+lib.icp_merge_tagged.restype = _I32
+lib.icp_merge_tagged.argtypes = [_P, _P, _P, _I32, _I32, _I32, _I32, _I32, _I32, _I32, _I64,
+                                 _P, _P, _P, _P]
 lib.icp_merge.restype = _I32
 lib.icp_merge.argtypes = [_P, _P, _I32, _I32, _I32, _I32, _I32, _I32, _I32, _I64, _P, _P, _P, _P]
 
@@ -225,6 +231,51 @@ def icp_score_select(index_q, index_k, block_table, seq_lens, num_valid_pages, o
                                 max_decode_query_len, np_, init_blocks, local_blocks, wp,
                                 workspace.numel(), osp, oip, ep, _stream(stream)),
            "icp_score_select")
+
+
+def icp_publish_rows_tagged(scores, num_valid_pages, recv_bases, generations, *, slot: int,
+                            rank: int, world_size: int, heads_per_rank: int, capacity: int,
+                            force_begin_blocks: int, force_end_blocks: int,
+                            index_scale: int = 1, index_offset: int = 0, stream=None):
+    """Top16 select + publish into tagged receive rows (int64 generation << 32 | word)."""
+    sp = _dev(scores, "scores", (torch.float32,), 3)
+    T, H, K = scores.shape
+    if H != world_size * heads_per_rank:
+        raise ValueError("scores must have world_size * heads_per_rank heads")
+    np_ = _dev(num_valid_pages, "num_valid_pages", (torch.int32,), 1)
+    rbp = _dev(recv_bases, "recv_bases", (torch.int64,), 1)
+    if recv_bases.shape[0] != world_size:
+        raise ValueError("recv_bases must be [world_size]")
+    gp = _dev(generations, "generations", (torch.int32,), 3)
+    if tuple(generations.shape) != (3, world_size * heads_per_rank, capacity):
+        raise ValueError("generations must be [3, world_size * heads_per_rank, capacity]")
+    _check(lib.icp_publish_rows_tagged(sp, T, K, np_, rbp, gp, slot, rank, world_size,
+                                       heads_per_rank, capacity, force_begin_blocks,
+                                       force_end_blocks, index_scale, index_offset,
+                                       _stream(stream)), "icp_publish_rows_tagged")
+
+
+def icp_merge_tagged(recv, expected, num_valid_pages, out_scores, out_ids, errors, *, T: int,
+                     slot: int, world_size: int, heads_per_rank: int, capacity: int,
+                     init_blocks: int, local_blocks: int, spin_limit: int = DEFAULT_SPIN_LIMIT,
+                     stream=None):
+    """Owner merge of tagged rows into out_* [T, heads_per_rank, 16]."""
+    rp = _dev(recv, "recv", (torch.int64,), None)
+    if recv.numel() < recv_rows(world_size, heads_per_rank, capacity) * 32:
+        raise ValueError("recv is smaller than [3][ws][hpr][capacity][32]")
+    ep_ = _dev(expected, "expected", (torch.int32,), None)
+    if expected.numel() < recv_rows(world_size, heads_per_rank, capacity):
+        raise ValueError("expected must hold [3][ws][hpr][capacity] counters")
+    np_ = _dev(num_valid_pages, "num_valid_pages", (torch.int32,), 1)
+    osp = _dev(out_scores, "out_scores", (torch.float32,), 3)
+    oip = _dev(out_ids, "out_ids", (torch.int32,), 3)
+    if tuple(out_scores.shape) != (T, heads_per_rank, TOPK) or \
+            tuple(out_ids.shape) != (T, heads_per_rank, TOPK):
+        raise ValueError("out_scores / out_ids must be [T, heads_per_rank, 16]")
+    erp = _dev(errors, "errors", (torch.int32,), 1)
+    _check(lib.icp_merge_tagged(rp, ep_, np_, T, slot, world_size, heads_per_rank, capacity,
+                                init_blocks, local_blocks, spin_limit, erp, osp, oip,
+                                _stream(stream)), "icp_merge_tagged")
 
 
 NOALLOC_SCRATCH_BYTES = 8 * 1024 * 1024
