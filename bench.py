@@ -274,7 +274,8 @@ class DecodeBench:
             icp.icp_score(self.q, self.shards[rank], self.bt, self.sl, self.planes[rank],
                           rank=rank, world_size=ws, page_size=spec.page_size,
                           decode_query_len=spec.decode_query_len,
-                          max_decode_query_len=spec.max_decode_query_len, errors=self.errors)
+                          max_decode_query_len=spec.max_decode_query_len, enable_pdl=True,
+                          errors=self.errors)
             if ev is not None and rank == ws - 1:
                 ev[1].record()
         for rank in range(ws):

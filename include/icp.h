@@ -85,12 +85,22 @@ int icp_score_columns(int max_seq_len, int page_size, int world_size);
  *   1, 2 or 4 (1 is an extension of the documented 2 or 4); 0 <= rank <
  *   world_size; 1 <= decode_query_len <= max_decode_query_len,
  *   4 * max_decode_query_len <= 32; 0 <= batch <= ICP_MAX_BATCH.
+ *   enable_pdl (parameter enable_pdl of the same page): non-zero launches with
+ *   programmatic dependent launch.  The kernel then reads seq_lens and
+ *   block_table and prefetches into L2 the index_k pages that end at or
+ *   before seq_len - decode_query_len before it waits on the preceding
+ *   kernel; it writes nothing and loads nothing else before that wait.  The
+ *   kernel launched just before must not write seq_lens, block_table or
+ *   those pages, and must either be launched without programmatic dependent
+ *   launch or wait on its own predecessor before it triggers its dependents.
+ *   0 removes the requirement.
  *   errors: optional int32 [>= 1] counter for timed-out internal waits.
  */
 int icp_score(const uint8_t *index_q, const uint8_t *index_k, int64_t num_pages,
               const int32_t *block_table, int64_t block_table_stride, const int32_t *seq_lens,
               float *score_out, int batch, int cols, int rank, int world_size, int page_size,
-              int decode_query_len, int max_decode_query_len, int32_t *errors, void *stream);
+              int decode_query_len, int max_decode_query_len, int enable_pdl, int32_t *errors,
+              void *stream);
 
 /*
  * Top16 select of every (token, head) row of a score plane (the selection

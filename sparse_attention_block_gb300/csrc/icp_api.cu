@@ -149,7 +149,8 @@ int icp_score_columns(int max_seq_len, int page_size, int world_size) {
 int icp_score(const uint8_t *index_q, const uint8_t *index_k, int64_t num_pages,
               const int32_t *block_table, int64_t block_table_stride, const int32_t *seq_lens,
               float *score_out, int batch, int cols, int rank, int world_size, int page_size,
-              int decode_query_len, int max_decode_query_len, int32_t *errors, void *stream) {
+              int decode_query_len, int max_decode_query_len, int enable_pdl, int32_t *errors,
+              void *stream) {
   int st = check_score_args(index_q, index_k, num_pages, block_table, block_table_stride,
                             seq_lens, batch, cols, rank, world_size, page_size, decode_query_len,
                             max_decode_query_len);
@@ -174,6 +175,7 @@ int icp_score(const uint8_t *index_q, const uint8_t *index_k, int64_t num_pages,
   a.page_size = page_size;
   a.dql = decode_query_len;
   a.g = make_geom(page_size, world_size, decode_query_len);
+  a.pdl = enable_pdl ? 1 : 0;
 
   CUtensorMap tmk, tmq;
   st = encode_rows(&tmk, index_k, (uint64_t)num_pages * a.g.rows_per_page, (uint32_t)a.g.R);

@@ -30,6 +30,7 @@ struct ScoreArgs {
   int32_t *errors;
   int batch, cols, rank, world_size, page_size, dql;
   ScoreGeom g;
+  int pdl;  // launched with programmatic dependent launch (early start)
   // fused scorer + select only
   const int32_t *nvp;
   int init_blocks, local_blocks, index_scale, index_offset;

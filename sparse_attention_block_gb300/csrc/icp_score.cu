@@ -503,6 +503,30 @@ score_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CU
     SegmentWalker walk(prefix, a.batch, g0, g1);
     int b, t0, t1;
     bool ok = true;
+    if (a.pdl) {
+      // Early start: while the preceding kernel finishes, pull the first
+      // tiles of this CTA into L2, only from pages that end at or before
+      // seq_len - dql (the preceding kernel may still append the newest
+      // keys); every real load below is issued after the wait.
+      SegmentWalker pw(prefix, a.batch, g0, g1);
+      int pb, p0, p1, budget = 2 * kStages;
+      while (budget > 0 && pw.next(pb, p0, p1)) {
+        const int sl = a.seq_lens[pb];
+        const int nunits = units_of(sl, a.page_size, g.split);
+        const int32_t *btrow = a.block_table + (long long)pb * a.bt_stride;
+        const long long safe_end = (long long)sl - a.dql;
+        for (int tl = p0; tl < p1 && budget > 0; ++tl, --budget) {
+          const int c = tl * g.cpt + lane;
+          if (lane < g.cpt && c < nunits) {
+            const int slot = page_slot_of(c, g.split);
+            if ((long long)(slot + 1) * a.page_size <= safe_end)
+              tma_prefetch_l2_2d(&tmk, 0, btrow[slot] * g.rows_per_page + row_off_of(c, g.split));
+          }
+        }
+      }
+      __syncwarp();
+      pdl_wait();
+    }
     while (ok && walk.next(b, t0, t1)) {
       const int nunits = units_of(a.seq_lens[b], a.page_size, g.split);
       const uint32_t qph = qslot ? qph1 : qph0;
@@ -624,6 +648,7 @@ score_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CU
     const int q = warp & 3;      // TMEM lane quarter this warp may access
     const int e = warp - 2;      // owns tiles i with i % 4 == e, accumulator e
     const int et = threadIdx.x - 64;
+    if (a.pdl) pdl_wait();       // no global write before the preceding kernel is done
     for (int b = blockIdx.x; b < a.batch; b += gridDim.x) {
       const int u = units_of(a.seq_lens[b], a.page_size, g.split);
       const int wcols = (u + 3) & ~3;
@@ -755,8 +780,21 @@ cudaError_t score_prepare(int device) {
 
 cudaError_t launch_score(const CUtensorMap &tmk, const CUtensorMap &tmq, const ScoreArgs &a,
                          int grid, cudaStream_t stream) {
-  score_kernel<false><<<grid, kThreads, smem_bytes_for<false>(a.batch), stream>>>(tmk, tmq, a);
-  return cudaGetLastError();
+  if (!a.pdl) {
+    score_kernel<false><<<grid, kThreads, smem_bytes_for<false>(a.batch), stream>>>(tmk, tmq, a);
+    return cudaGetLastError();
+  }
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)grid);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = smem_bytes_for<false>(a.batch);
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, score_kernel<false>, tmk, tmq, a);
 }
 
 size_t fused_workspace_bytes(int batch, int dql) {

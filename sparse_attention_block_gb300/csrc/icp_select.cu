@@ -667,6 +667,9 @@ __device__ __forceinline__ void merge_finish(const MergeArgs &a, int lane, int t
 __global__ void __launch_bounds__(128) merge_kernel(const MergeArgs a) {
   __shared__ int s_id[4][kTopK];
   __shared__ float s_sc[4][kTopK];
+  // a scorer launched next with early start may begin its set-up now: it
+  // reads nothing this kernel writes before waiting for it
+  pdl_launch_dependents();
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int item = blockIdx.x * 4 + warp;

@@ -37,7 +37,7 @@ lib.icp_score_columns.restype = _I32
 lib.icp_score_columns.argtypes = [_I32, _I32, _I32]
 lib.icp_score.restype = _I32
 lib.icp_score.argtypes = [_P, _P, _I64, _P, _I64, _P, _P, _I32, _I32, _I32, _I32, _I32, _I32,
-                          _I32, _P, _P]
+                          _I32, _I32, _P, _P]
 lib.icp_top16_select.restype = _I32
 lib.icp_top16_select.argtypes = [_P, _I32, _I32, _P, _I32, _I32, _I32, _I32, _P, _P, _P]
 lib.icp_publish_rows.restype = _I32
@@ -105,9 +105,11 @@ def icp_score_columns(max_seq_len: int, page_size: int, world_size: int) -> int:
 
 
 def icp_score(index_q, index_k, block_table, seq_lens, score_out, *, rank: int, world_size: int,
-              page_size: int, decode_query_len: int, max_decode_query_len: int, errors=None,
-              stream=None):
-    """Decode index scores into score_out [T, 4, cols] (msa_icp_decode_index_score_sharded)."""
+              page_size: int, decode_query_len: int, max_decode_query_len: int,
+              enable_pdl: bool = False, errors=None, stream=None):
+    """Decode index scores into score_out [T, 4, cols] (msa_icp_decode_index_score_sharded).
+
+    enable_pdl: start early under programmatic dependent launch (see include/icp.h)."""
     B = seq_lens.shape[0]
     T = B * decode_query_len
     qp = _dev(index_q, "index_q", _FP8, 3)
@@ -126,7 +128,8 @@ def icp_score(index_q, index_k, block_table, seq_lens, score_out, *, rank: int, 
     ep = 0 if errors is None else _dev(errors, "errors", (torch.int32,), 1)
     _check(lib.icp_score(qp, kp, index_k.shape[0], btp, block_table.stride(0), slp, sop, B,
                          score_out.shape[2], rank, world_size, page_size, decode_query_len,
-                         max_decode_query_len, ep, _stream(stream)), "icp_score")
+                         max_decode_query_len, 1 if enable_pdl else 0, ep, _stream(stream)),
+           "icp_score")
 
 
 def icp_top16_select(scores, num_valid_pages, out_scores, out_ids, *, init_blocks: int,

@@ -113,7 +113,7 @@ class DecodeInputs:
 
     @property
     def T(self) -> int:
-        return self.spec.T
+        return int(self.seq_lens.numel()) * self.spec.decode_query_len
 
 
 def _gen(device, seed):

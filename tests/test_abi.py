@@ -59,7 +59,7 @@ def test_invalid_arguments_are_rejected_before_any_launch(lib):
     buf = ctypes.create_string_buffer(1 << 16)
     a = ctypes.cast(ctypes.addressof(buf) + (-ctypes.addressof(buf) % 256), P)
     lib.icp_score.argtypes = [P, P, ctypes.c_int64, P, ctypes.c_int64, P, P] + \
-        [ctypes.c_int] * 7 + [P, P]
+        [ctypes.c_int] * 8 + [P, P]
     good = dict(q=a, k=a, n=4, bt=a, st=4, sl=a, out=a, B=1, cols=8, rank=0, ws=1, ps=128,
                 dql=1, maxdql=1)
 
@@ -67,7 +67,7 @@ def test_invalid_arguments_are_rejected_before_any_launch(lib):
         d = dict(good, **kw)
         return lib.icp_score(d["q"], d["k"], d["n"], d["bt"], d["st"], d["sl"], d["out"], d["B"],
                              d["cols"], d["rank"], d["ws"], d["ps"], d["dql"], d["maxdql"],
-                             None, None)
+                             0, None, None)
     INVALID = 1
     assert call(cols=6) == INVALID            # cols % 4 != 0
     assert call(cols=8196) == INVALID         # cols > 8192

@@ -126,3 +126,28 @@ def test_repeated_calls_are_deterministic():
     b = gpu_score(q, k, bt, sl, cols=cols, rank=0, world_size=1, page_size=128, dql=1)
     torch.cuda.synchronize()
     assert torch.equal(a.view(torch.int32), b.view(torch.int32))
+
+
+def test_early_start_under_programmatic_dependent_launch_changes_nothing():
+    # the scorer launched with enable_pdl right after other kernels (here a
+    # merge and a select) gives the same plane as a plain launch
+    inp = W.make_decode_inputs(W.MULTITOKEN, seed=6, batch=12)
+    q, k, bt, sl, nvp = to_dev(inp)
+    spec = W.MULTITOKEN
+    cols = W.columns_for(spec, int(inp.seq_lens.max()))
+    from gpu_util import icp, sentinel_plane
+    ref = gpu_score(q, k, bt, sl, cols=cols, rank=0, world_size=1, page_size=256, dql=4, maxdql=8)
+    T = inp.T
+    for _ in range(3):
+        plane = sentinel_plane(T, cols)
+        # a preceding merge (triggers its dependents early) and a select
+        recv = torch.zeros((icp().recv_rows(1, 4, T), 33), dtype=torch.int32, device="cuda")
+        errors = torch.zeros(1, dtype=torch.int32, device="cuda")
+        s = torch.empty((T, 4, 16), device="cuda")
+        i = torch.empty((T, 4, 16), dtype=torch.int32, device="cuda")
+        icp().icp_merge(recv, nvp, s, i, errors, T=T, slot=0, world_size=1, heads_per_rank=4,
+                        capacity=T, init_blocks=1, local_blocks=1, spin_limit=100)
+        icp().icp_score(q, k, bt, sl, plane, rank=0, world_size=1, page_size=256,
+                        decode_query_len=4, max_decode_query_len=8, enable_pdl=True)
+        torch.cuda.synchronize()
+        assert torch.equal(plane.view(torch.int32), ref.view(torch.int32))
