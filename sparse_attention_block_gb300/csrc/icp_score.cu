@@ -463,19 +463,20 @@ score_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CU
       const int u = units_of(a.seq_lens[b], a.page_size, g.split);
       sum += (u + g.cpt - 1) / g.cpt;
     }
-    partial[threadIdx.x] = sum;
-    __syncthreads();
-    if (threadIdx.x == 0) {
-      int run = 0;
-      for (int i = 0; i < kThreads; ++i) {
-        const int x = partial[i];
-        partial[i] = run;
-        run += x;
-      }
-      prefix[nb] = run;
+    // exclusive scan of the per-thread sums: shuffles inside each warp, then
+    // the warp totals (kThreads / 32 of them) in shared memory
+    int incl = sum;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+      if (lane >= o) incl += y;
     }
+    if (lane == 31) partial[warp] = incl;
     __syncthreads();
-    int run = partial[threadIdx.x];
+    int base = 0;
+    for (int w = 0; w < warp; ++w) base += partial[w];
+    if (threadIdx.x == kThreads - 1) prefix[nb] = base + incl;
+    int run = base + incl - sum;
     for (int b = lo; b < hi; ++b) {
       prefix[b] = run;
       const int u = units_of(a.seq_lens[b], a.page_size, g.split);
