@@ -280,18 +280,30 @@ fused_merge_kernel(const ScoreArgs a, const ReqInfo *info, int grid_a) {
     return total * i / G < total * (i + 1) / G;
   };
 
-  // forced entries: each forced id was seen by exactly one partial list
-  int nf = 0;
-  for (int k0 = 0; k0 < P; k0 += 32) {
+  // one pass over the lists: each list's maximum (to the shared cache) and
+  // its forced-entry count (every forced id was seen by exactly one list)
+  unsigned fmask_all = 0;  // bit j: list lane + 32 * j holds forced entries (j < 32)
+  for (int k0 = 0, j = 0; k0 < P; k0 += 32, ++j) {
     const int k = k0 + lane;
+    unsigned long long mxk = 0;
     int fc = 0;
-    if (k < P && part_valid(k)) fc = __ldcg(&partial_rec(a, pidx_of(k), r)->fcount);
-    unsigned msk = __ballot_sync(0xFFFFFFFFu, fc > 0);
+    if (k < P && part_valid(k)) {
+      const PartialRec *pr = partial_rec(a, pidx_of(k), r);
+      mxk = __ldcg(&pr->max);
+      fc = __ldcg(&pr->fcount);
+    }
+    if (k < P) mx[k] = mxk;
+    if (fc > 0 && j < 32) fmask_all |= 1u << j;
+  }
+  // forced entries, gathered in list order (ids come out ordered later)
+  int nf = 0;
+  for (int k0 = 0, j = 0; k0 < P && j < 32; k0 += 32, ++j) {
+    unsigned msk = __ballot_sync(0xFFFFFFFFu, (fmask_all >> j) & 1u);
     while (msk) {
       const int src = __ffs(msk) - 1;
       msk &= msk - 1;
-      const int cnt = __shfl_sync(0xFFFFFFFFu, fc, src);
       const PartialRec *pr = partial_rec(a, pidx_of(k0 + src), r);
+      const int cnt = __ldcg(&pr->fcount);
       if (lane < cnt && nf + lane < kTopK) {
         fbuf_id[nf + lane] = __ldcg(&pr->fid[lane]);
         fbuf_sc[nf + lane] = __ldcg(&pr->fsc[lane]);
@@ -310,11 +322,9 @@ fused_merge_kernel(const ScoreArgs a, const ReqInfo *info, int grid_a) {
     }
   }
   const int m = kTopK - nf;
+  __syncwarp();
   // tau = m-th largest list maximum; the lists holding keys >= tau are
   // exactly the round winners
-  for (int k = lane; k < P; k += 32)
-    mx[k] = part_valid(k) ? __ldcg(&partial_rec(a, pidx_of(k), r)->max) : 0ull;
-  __syncwarp();
   unsigned long long prev = ~0ull, tau = 0;
   int found = 0, my_winner = -1;
   for (int rd = 0; rd < m; ++rd) {
@@ -337,15 +347,22 @@ fused_merge_kernel(const ScoreArgs a, const ReqInfo *info, int grid_a) {
     ++found;
   }
   if (found < m) tau = 1;  // fewer than m lists hold entries: take all of them
-  int nc = 0;
-  for (int w0 = 0; w0 < found; w0 += 2) {
-    const int wi = w0 + (lane >> 4);
+  // every winner's 16 keys in one round of loads (lane L reads entries
+  // L, L + 32, ... of the found * 16 keys), then compaction
+  unsigned long long kv[8];
+#pragma unroll
+  for (int j = 0; j < 8; ++j) {
+    const int q = lane + 32 * j;
+    const int wi = q >> 4;
     const int k = __shfl_sync(0xFFFFFFFFu, my_winner, wi & 31);
-    unsigned long long key = 0;
-    if (wi < found) key = __ldcg(&partial_rec(a, pidx_of(k), r)->keys[lane & 15]);
-    const bool keep = key != 0 && key >= tau;
+    kv[j] = (wi < found) ? __ldcg(&partial_rec(a, pidx_of(k), r)->keys[q & 15]) : 0ull;
+  }
+  int nc = 0;
+#pragma unroll
+  for (int j = 0; j < 8; ++j) {
+    const bool keep = kv[j] != 0 && kv[j] >= tau;
     const unsigned bal = __ballot_sync(0xFFFFFFFFu, keep);
-    if (keep) cand[nc + __popc(bal & ((1u << lane) - 1u))] = key;
+    if (keep) cand[nc + __popc(bal & ((1u << lane) - 1u))] = kv[j];
     nc += __popc(bal);
   }
   for (int c = nunits; c < wcols; ++c) {

@@ -43,9 +43,27 @@ __device__ __forceinline__ bool poll_flag(const int *flag, int want, long long s
 // generation taken from the publisher's counter for (slot, head, token)).
 enum EmitMode { kEmitPlain = 0, kEmitLegacy = 1, kEmitTagged = 2 };
 
+// Address of the legacy receive row (t, h) of this publish.
+__device__ __forceinline__ int *legacy_row(const SelectArgs &a, int t, int h) {
+  const int hpr = a.heads_per_rank;
+  const long long r =
+      (((long long)a.slot * a.world_size + a.rank) * hpr + h % hpr) * a.capacity + t;
+  return reinterpret_cast<int *>(a.recv_bases[h / hpr]) + r * kRowWords;
+}
+
+// The ready flag of that row, read with acquire when the row's work starts so
+// that the read overlaps the selection; -1 when not a legacy publish.
+template <int MODE>
+__device__ __forceinline__ int early_flag(const SelectArgs &a, int lane, int t, int h) {
+  if constexpr (MODE == kEmitLegacy) {
+    if (lane == 0) return ld_acquire_gpu(legacy_row(a, t, h) + 32);
+  }
+  return -1;
+}
+
 template <int MODE>
 __device__ __forceinline__ void emit_row(const SelectArgs &a, int lane, int row, int t, int h,
-                                         int out_id, float out_sc) {
+                                         int out_id, float out_sc, int flag0) {
   if constexpr (MODE == kEmitPlain) {
     if (lane < kTopK) {
       a.out_scores[(long long)row * kTopK + lane] = out_sc;
@@ -56,9 +74,11 @@ __device__ __forceinline__ void emit_row(const SelectArgs &a, int lane, int row,
     const long long r =
         (((long long)a.slot * a.world_size + a.rank) * hpr + h % hpr) * a.capacity + t;
     if constexpr (MODE == kEmitLegacy) {
-      int *dst = reinterpret_cast<int *>(a.recv_bases[h / hpr]) + r * kRowWords;
+      int *dst = legacy_row(a, t, h);
       int ok = 0;
-      if (lane == 0) ok = poll_flag(dst + 32, 0, a.spin_limit) ? 1 : 0;
+      // the flag read when the row started (acquire) usually shows the row
+      // free already; otherwise poll (bounded)
+      if (lane == 0) ok = (flag0 == 0 || poll_flag(dst + 32, 0, a.spin_limit)) ? 1 : 0;
       ok = __shfl_sync(0xFFFFFFFFu, ok, 0);
       if (!ok) {
         if (lane == 0) atomicAdd(a.errors, 1);
@@ -67,7 +87,8 @@ __device__ __forceinline__ void emit_row(const SelectArgs &a, int lane, int row,
           dst[lane] = __float_as_int(out_sc);
           dst[kTopK + lane] = out_id;
         }
-        __threadfence();
+        // the warp barrier orders every lane's data stores before lane 0's
+        // release store of the flag (release is cumulative)
         __syncwarp();
         if (lane == 0) st_release_gpu(dst + 32, 1);
       }
@@ -158,6 +179,7 @@ __global__ void __launch_bounds__(NT) select_block_kernel(const SelectArgs a) {
     if (tid == 0) s_nc = 0;
     const int t = row >> 2;
     const int h = row & 3;
+    const int flag0 = warp == 0 ? early_flag<MODE>(a, lane, t, h) : -1;
 
     // forced ids, in increasing order: every valid id when nvp <= 16, else
     // [0, init) then [nvp - local, nvp); each exists when it maps to a column
@@ -322,7 +344,7 @@ __global__ void __launch_bounds__(NT) select_block_kernel(const SelectArgs a) {
       int out_id;
       float out_sc;
       sort_by_id_16(lane, n, my_id, my_sc, out_id, out_sc);
-      emit_row<MODE>(a, lane, row, t, h, out_id, out_sc);
+      emit_row<MODE>(a, lane, row, t, h, out_id, out_sc, flag0);
     }
     __syncthreads();  // this row's buffer and scratch may be reused
   }
@@ -456,6 +478,7 @@ __global__ void __launch_bounds__(32 * kSelWarps, 8) select_warp_kernel(const Se
     const int t = row >> 2, h = row & 3;
     const int nvp = __ldg(a.nvp + t);
     const float *src = a.scores + (long long)row * K;
+    const int flag0 = early_flag<MODE>(a, lane, t, h);
 
     // forced ids in increasing order: every valid id when nvp <= 16, else
     // [0, init) then [nvp - local, nvp); lane f < nf holds the f-th
@@ -564,7 +587,7 @@ __global__ void __launch_bounds__(32 * kSelWarps, 8) select_warp_kernel(const Se
     int out_id;
     float out_sc;
     sort_by_id_16(lane, n, my_id, my_sc, out_id, out_sc);
-    emit_row<MODE>(a, lane, row, t, h, out_id, out_sc);
+    emit_row<MODE>(a, lane, row, t, h, out_id, out_sc, flag0);
     __syncwarp();
   }
 }
