@@ -45,10 +45,10 @@ FALLBACK_HBM_GBS = 6800.0
 # streamed), measured for the kernel source with this digest.  When the
 # kernel changes the digest no longer matches and `traffic` is reported null.
 NCU_TRAFFIC = {
-    # dram__bytes_read.sum + dram__bytes_write.sum = 282.52 MB for 278.33 MB of
-    # index-K (first 32 requests of the multitoken workload), see
-    # profiles/icp_score_multitoken.md
-    ("multitoken", "6bd521b5662f04b5"): 282.524928 / 278.330624,
+    # dram__bytes_read.sum + dram__bytes_write.sum = 278818304 + 2935040 bytes for
+    # 278330624 bytes of index-K (first 32 requests of the multitoken workload),
+    # see profiles/icp_score_multitoken.md
+    ("multitoken", "e452aa630b34ba90"): (278818304 + 2935040) / 278330624,
 }
 
 
@@ -97,7 +97,7 @@ def measured_peaks():
 def kernel_digest():
     import hashlib
     h = hashlib.sha256()
-    for f in ["icp_score.cu", "icp_device.cuh"]:
+    for f in ["icp_score.cu", "icp_fused.cuh", "icp_device.cuh"]:
         with open(os.path.join(ROOT, "sparse_attention_block_gb300", "csrc", f), "rb") as fh:
             h.update(fh.read())
     return h.hexdigest()[:16]
@@ -247,6 +247,7 @@ class DecodeBench:
         self.score_bytes, self.select_bytes, self.merge_bytes, self.kbytes = \
             algorithmic_bytes(spec, self.seq_list, self.cols)
         self.launches_per_step = 3 * ws
+        self.kernel_launches_per_step = ws
 
     @property
     def fused_bytes(self):
@@ -362,6 +363,7 @@ class SelectBench:
         self.select_bytes = self.merge_bytes = 0
         self.kbytes = 0
         self.launches_per_step = 1
+        self.kernel_launches_per_step = 1
         # rotate copies so consecutive steps do not hit the 50 MB plane in L2
         self.copies = [self.plane] + [self.plane.clone() for _ in range(5)]
         self.i = 0
@@ -601,6 +603,7 @@ def run_ours(args, spec_name):
                      "kernel_digest": digest},
         "clocks": sampler.summary(),
         "gpu_launches": bench.launches_per_step * args.steps,
+        "kernel_timing_launches": bench.kernel_launches_per_step * args.steps,
     }
     if spec_name != "select":
         for _ in range(max(args.warmup, 3)):

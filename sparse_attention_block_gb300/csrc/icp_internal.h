@@ -75,6 +75,7 @@ size_t score_smem_bytes(int batch);
 cudaError_t score_prepare(int device);  // one-time per-device kernel attributes
 
 size_t fused_workspace_bytes(int batch, int dql);
+cudaError_t launch_fused_merge(const ScoreArgs &a, int grid_a, cudaStream_t stream);
 cudaError_t launch_score_select(const CUtensorMap &tmk, const CUtensorMap &tmq, ScoreArgs a,
                                 int grid, cudaStream_t stream);
 

@@ -36,6 +36,7 @@
 // fp32.  The per-key arithmetic does not depend on where the key sits in the
 // tile, so sharded and unsharded layouts give identical key scores.
 #include "icp_device.cuh"
+#include "icp_fused.cuh"
 #include "icp_internal.h"
 
 namespace icp {
@@ -67,11 +68,6 @@ struct PrefixOffset {
   static constexpr uint32_t value = FUSED ? kOffLists + kFusedExtra : kOffLists;
 };
 
-__device__ __forceinline__ int units_of(int seq_len, int page_size, int split) {
-  const int u = split ? 128 : page_size;
-  return seq_len <= 0 ? 0 : (seq_len + u - 1) / u;
-}
-
 // Walks the CTA's tile range [g0, g1) request by request.
 struct SegmentWalker {
   const int *prefix;  // prefix[b] = tiles of requests < b, prefix[batch] = total
@@ -102,23 +98,6 @@ struct SegmentWalker {
 
 __device__ __forceinline__ int page_slot_of(int c, int split) { return split ? (c >> 1) : c; }
 __device__ __forceinline__ int row_off_of(int c, int split) { return split ? (c & 1) * 128 : 0; }
-
-// ------------------------------------------------------------ fused state
-// Workspace record of one (partial list, query row), 288 bytes:
-//   u64 keys[16]   best non-forced entries seen (unsorted, 0 = empty)
-//   u64 max        largest of keys (0 = none)
-//   i32 fcount     forced entries that follow
-//   i32 fid[16], f32 fsc[16]
-struct alignas(16) PartialRec {
-  unsigned long long keys[16];
-  unsigned long long max;
-  int fcount;
-  int pad_;
-  int fid[16];
-  float fsc[16];
-  int pad2_[4];
-};
-static_assert(sizeof(PartialRec) == 288, "record layout");
 
 // Per-lane running Top16 of one query row over the columns a warp has seen.
 struct LaneTop {
@@ -214,210 +193,6 @@ __device__ __forceinline__ void epilogue_tile(const ScoreArgs &a, uint32_t taddr
         }
       }
     }
-  }
-}
-
-__device__ __forceinline__ PartialRec *partial_rec(const ScoreArgs &a, int pidx, int row) {
-  return reinterpret_cast<PartialRec *>(a.ws_records) + (size_t)pidx * (4 * a.dql) + row;
-}
-
-// Index of the CTA whose tile range contains tile x.
-__device__ __forceinline__ int cta_of(long long total, int grid, long long x) {
-  int lo = 0, hi = grid - 1;
-  while (lo < hi) {
-    const int mid = (lo + hi + 1) >> 1;
-    if (total * mid / grid <= x) lo = mid; else hi = mid - 1;
-  }
-  return lo;
-}
-
-// Per-request facts the fused scorer leaves for the merge kernel.
-struct alignas(16) ReqInfo {
-  int i0, i1;   // first and last CTA whose tile range covers the request (i1 < i0: none)
-  int total;    // tiles of the whole launch
-  int nunits;   // plane columns of the request
-};
-
-// Final Top16 of one (token, head) row from the partial lists that the
-// epilogue warps of every CTA covering the token's request wrote, plus the
-// request's padding columns [units, round_up(units, 4)), which hold -inf.
-// One warp per row; the lists holding the m largest entries are found from
-// the lists' maxima (tau = the m-th largest maximum), so at most m * 16
-// candidates are read.
-__global__ void __launch_bounds__(128)
-fused_merge_kernel(const ScoreArgs a, const ReqInfo *info, int grid_a) {
-  __shared__ unsigned long long s_mx[4][4 * kFusedMaxGrid];
-  __shared__ unsigned long long s_cand[4][kTopK * 16 + 8];
-  __shared__ int s_fid[4][kTopK];
-  __shared__ float s_fsc[4][kTopK];
-  // wait for the fused scorer (programmatic dependent launch)
-  asm volatile("griddepcontrol.wait;" ::: "memory");
-
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int row = blockIdx.x * 4 + warp;   // t * 4 + h
-  const int T = a.batch * a.dql;
-  if (row >= T * 4) return;
-  const int t = row >> 2, h = row & 3;
-  const int b = t / a.dql;
-  const int r = (t - b * a.dql) * 4 + h;   // query row inside the request
-  unsigned long long *mx = s_mx[warp];
-  unsigned long long *cand = s_cand[warp];
-  int *fbuf_id = s_fid[warp];
-  float *fbuf_sc = s_fsc[warp];
-
-  const ReqInfo in = info[b];
-  const long long total = in.total;
-  const int G = grid_a;
-  const int i0 = in.i0;
-  const int P = in.i1 >= in.i0 ? (in.i1 - in.i0 + 1) * 4 : 0;
-  const int nunits = in.nunits;
-  const int wcols = min((nunits + 3) & ~3, a.cols);
-  const int nvp = a.nvp[t];
-  auto pidx_of = [&](int k) { return (i0 + (k >> 2) + b) * 4 + (k & 3); };
-  // a CTA in [i0, i1] with an empty tile range never wrote lists for b
-  auto part_valid = [&](int k) {
-    const int i = i0 + (k >> 2);
-    return total * i / G < total * (i + 1) / G;
-  };
-
-  // one pass over the lists: each list's maximum (to the shared cache) and
-  // its forced-entry count (every forced id was seen by exactly one list)
-  unsigned fmask_all = 0;  // bit j: list lane + 32 * j holds forced entries (j < 32)
-  for (int k0 = 0, j = 0; k0 < P; k0 += 32, ++j) {
-    const int k = k0 + lane;
-    unsigned long long mxk = 0;
-    int fc = 0;
-    if (k < P && part_valid(k)) {
-      const PartialRec *pr = partial_rec(a, pidx_of(k), r);
-      mxk = __ldcg(&pr->max);
-      fc = __ldcg(&pr->fcount);
-    }
-    if (k < P) mx[k] = mxk;
-    if (fc > 0 && j < 32) fmask_all |= 1u << j;
-  }
-  // forced entries, gathered in list order (ids come out ordered later)
-  int nf = 0;
-  for (int k0 = 0, j = 0; k0 < P && j < 32; k0 += 32, ++j) {
-    unsigned msk = __ballot_sync(0xFFFFFFFFu, (fmask_all >> j) & 1u);
-    while (msk) {
-      const int src = __ffs(msk) - 1;
-      msk &= msk - 1;
-      const PartialRec *pr = partial_rec(a, pidx_of(k0 + src), r);
-      const int cnt = __ldcg(&pr->fcount);
-      if (lane < cnt && nf + lane < kTopK) {
-        fbuf_id[nf + lane] = __ldcg(&pr->fid[lane]);
-        fbuf_sc[nf + lane] = __ldcg(&pr->fsc[lane]);
-      }
-      nf = min(nf + cnt, kTopK);
-    }
-  }
-  for (int c = nunits; c < wcols; ++c) {
-    const int id = c * a.index_scale + a.index_offset;
-    if (id < nvp && forced_id(id, nvp, a.init_blocks, a.local_blocks) && nf < kTopK) {
-      if (lane == 0) {
-        fbuf_id[nf] = id;
-        fbuf_sc[nf] = -INFINITY;
-      }
-      ++nf;
-    }
-  }
-  const int m = kTopK - nf;
-  __syncwarp();
-  // tau = m-th largest list maximum; the lists holding keys >= tau are
-  // exactly the round winners
-  unsigned long long prev = ~0ull, tau = 0;
-  int found = 0, my_winner = -1;
-  for (int rd = 0; rd < m; ++rd) {
-    unsigned long long local = 0;
-    int lidx = -1;
-    for (int k = lane; k < P; k += 32) {
-      const unsigned long long x = mx[k];
-      if (x < prev && x > local) {
-        local = x;
-        lidx = k;
-      }
-    }
-    const unsigned long long w = warp_max_key(local);
-    if (w == 0) break;
-    const int src = __ffs(__ballot_sync(0xFFFFFFFFu, local == w)) - 1;
-    const int widx = __shfl_sync(0xFFFFFFFFu, lidx, src);
-    if (lane == rd) my_winner = widx;
-    prev = w;
-    tau = w;
-    ++found;
-  }
-  if (found < m) tau = 1;  // fewer than m lists hold entries: take all of them
-  // every winner's 16 keys in one round of loads (lane L reads entries
-  // L, L + 32, ... of the found * 16 keys), then compaction
-  unsigned long long kv[8];
-#pragma unroll
-  for (int j = 0; j < 8; ++j) {
-    const int q = lane + 32 * j;
-    const int wi = q >> 4;
-    const int k = __shfl_sync(0xFFFFFFFFu, my_winner, wi & 31);
-    kv[j] = (wi < found) ? __ldcg(&partial_rec(a, pidx_of(k), r)->keys[q & 15]) : 0ull;
-  }
-  int nc = 0;
-#pragma unroll
-  for (int j = 0; j < 8; ++j) {
-    const bool keep = kv[j] != 0 && kv[j] >= tau;
-    const unsigned bal = __ballot_sync(0xFFFFFFFFu, keep);
-    if (keep) cand[nc + __popc(bal & ((1u << lane) - 1u))] = kv[j];
-    nc += __popc(bal);
-  }
-  for (int c = nunits; c < wcols; ++c) {
-    const int id = c * a.index_scale + a.index_offset;
-    if (id < nvp && !forced_id(id, nvp, a.init_blocks, a.local_blocks)) {
-      const unsigned long long key = make_key(-INFINITY, id);
-      if (key >= tau) {
-        if (lane == 0) cand[nc] = key;
-        ++nc;
-      }
-    }
-  }
-  __syncwarp();
-  // the m largest candidates; lane nf + rd receives the rd-th
-  unsigned long long cl[9];
-  unsigned long long lmax = 0;
-#pragma unroll
-  for (int j = 0; j < 9; ++j) {
-    const int k = lane + 32 * j;
-    cl[j] = (k < nc) ? cand[k] : 0ull;
-    lmax = cl[j] > lmax ? cl[j] : lmax;
-  }
-  unsigned long long mine = 0;
-  int nch = 0;
-  for (int rd = 0; rd < m; ++rd) {
-    const unsigned long long w = warp_max_key(lmax);
-    if (w == 0) break;
-    if (lane == nf + rd) mine = w;
-    ++nch;
-    if (lmax == w) {
-      lmax = 0;
-#pragma unroll
-      for (int j = 0; j < 9; ++j) {
-        if (cl[j] == w) cl[j] = 0;
-        lmax = cl[j] > lmax ? cl[j] : lmax;
-      }
-    }
-  }
-  const int n = nf + nch;
-  int my_id = 0x7FFFFFFF;
-  float my_sc = -INFINITY;
-  if (lane < nf) {
-    my_id = fbuf_id[lane];
-    my_sc = fbuf_sc[lane];
-  } else if (lane < n) {
-    my_id = key_id(mine);
-    my_sc = unord_float((uint32_t)(mine >> 32));
-  }
-  int out_id;
-  float out_sc;
-  sort_by_id_16(lane, n, my_id, my_sc, out_id, out_sc);
-  if (lane < kTopK) {
-    const long long o = (long long)row * kTopK + lane;
-    a.out_scores[o] = out_sc;
-    a.out_ids[o] = out_id;
   }
 }
 
@@ -815,33 +590,13 @@ cudaError_t launch_score(const CUtensorMap &tmk, const CUtensorMap &tmq, const S
   return cudaLaunchKernelEx(&cfg, score_kernel<false>, tmk, tmq, a);
 }
 
-size_t fused_workspace_bytes(int batch, int dql) {
-  const size_t counters = ((size_t)batch * sizeof(ReqInfo) + 255) / 256 * 256;
-  const size_t records =
-      (size_t)(kFusedMaxGrid + batch) * 4 * (size_t)(4 * dql) * sizeof(PartialRec);
-  return counters + records;
-}
-
 cudaError_t launch_score_select(const CUtensorMap &tmk, const CUtensorMap &tmq, ScoreArgs a,
                                 int grid, cudaStream_t stream) {
   grid = grid > kFusedMaxGrid ? kFusedMaxGrid : grid;
   score_kernel<true><<<grid, kThreads, smem_bytes_for<true>(a.batch), stream>>>(tmk, tmq, a);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  // the merge kernel starts early and waits on griddepcontrol for the scorer
-  const int rows = a.batch * a.dql * 4;
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3((unsigned)((rows + 3) / 4));
-  cfg.blockDim = dim3(128);
-  cfg.dynamicSmemBytes = 0;
-  cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  const ReqInfo *info = reinterpret_cast<const ReqInfo *>(a.ws_counters);
-  return cudaLaunchKernelEx(&cfg, fused_merge_kernel, a, info, grid);
+  return launch_fused_merge(a, grid, stream);
 }
 
 }  // namespace icp
