@@ -7,8 +7,8 @@
 // slots go to the best remaining ids by (score descending, id ascending).
 // Output: ids ascending with their raw scores, then (-1, -inf) padding.
 //
-// Select: one warp per row for rows up to 2048 columns, a CTA per row
-// (persistent, double-buffered in shared memory) for longer rows.  Every
+// Select: one warp per row for rows up to 2048 columns; for longer rows one
+// CTA per row whose eight warps each select from an eighth of it.  Every
 // non-forced valid score
 // becomes a unique 64-bit key (score order, then lower id).  With m free
 // slots, tau = the m-th largest per-thread best is a lower bound of the m-th
@@ -33,10 +33,6 @@ __device__ __forceinline__ bool poll_flag(const int *flag, int want, long long s
   return false;
 }
 
-// Persistent block select (long rows): each CTA takes rows blockIdx.x, blockIdx.x + gridDim.x,
-// ... and stages them in shared memory with bulk async copies into two
-// buffers, so the next row streams in while the current one is processed.
-// MAXK bounds the row length of the variant.
 // Where a selected row goes: the plain output arrays, a legacy receive row
 // (bounded wait for a free row, 32 data words, release-stored ready flag) or
 // a tagged receive row (32 int64 words of generation << 32 | word, the
@@ -112,282 +108,241 @@ __device__ __forceinline__ void emit_row(const SelectArgs &a, int lane, int row,
   }
 }
 
-template <int NT, int MAXK, int MODE>
-__global__ void __launch_bounds__(NT) select_block_kernel(const SelectArgs a) {
-  constexpr int NW = NT / 32;
-  constexpr int EPT = ((MAXK + 4 * NT - 1) / (4 * NT)) * 4;  // row entries per thread
-  constexpr int CAP = kTopK * EPT;           // candidate bound (see the file comment)
-  constexpr int WL = (NW * kTopK + 31) / 32; // per-warp maxima per lane in warp 0
-  constexpr int BUF = ((MAXK + 3) / 4) * 4;  // floats per row buffer
+// Select.  Every non-forced valid score becomes a unique 64-bit key (score
+// order, then the lower id), and a row's m = 16 - (forced ids) free slots go
+// to its m largest keys.  Rows up to 2048 columns: one warp per row; longer
+// rows: kRowWarps warps per row, each taking the top m of its share, then
+// the top m of their lists.  A warp takes the top m of its columns so:
+//   1. every lane scans its strided float4s (or elements), keeps its best key
+//      and records each float4's largest value in shared memory; the first
+//      batch of loads is issued before num_valid_pages is known;
+//   2. tau = a lower bound of the m-th largest lane best (rounds of a warp
+//      max on the score half); only lanes whose best reaches tau can hold
+//      keys >= tau;
+//   3. those lanes re-read the float4s whose recorded maximum reaches tau's
+//      score, all at once, and append the keys >= tau to a candidate buffer;
+//   4. the m largest candidates, placed by rank, in order.
+// If the candidates overflow the buffer (only with very many equal scores),
+// the warp takes the m largest directly from its columns by rounds.  Rows
+// are read with float4 loads when K % 4 == 0 and the plane is 16-byte
+// aligned, else with scalar loads (and a plain rescan in step 3).
+constexpr int kSelWarps = 4;     // warps (rows in flight) per CTA, rows <= 2048 columns
+constexpr int kRowWarps = 4;     // warps per row, longer rows
+constexpr int kChunk = 8;        // float4 loads in flight per lane
+constexpr int kCandCap = 128;    // candidates per warp
+constexpr int kWarpRowMaxK = 2048;  // rows up to this long: one warp per row
+constexpr int kLongRowMaxK = 12287;  // the widest plane
+// float4s per lane: 2048 / 4 / 32 for a warp row, ceil(12287 / 4 / 128) for a long row
+constexpr int kWarpRowChunks = 16;
+constexpr int kLongRowChunks = 24;
+static_assert(kWarpRowChunks * 32 >= kWarpRowMaxK / 4, "warp-row chunk record too small");
 
-  extern __shared__ __align__(16) unsigned char dyn_smem[];
-  float *bufs = reinterpret_cast<float *>(dyn_smem);  // [2][BUF] (bulk) or [1][BUF]
-  __shared__ __align__(8) unsigned long long s_bar[2];
-  __shared__ int s_nc, s_nf, s_abort;
-  __shared__ int s_fid[kTopK];
-  __shared__ float s_fsc[kTopK];
-  __shared__ unsigned long long s_wtop[NW][kTopK];
-  __shared__ unsigned long long s_tau;
-  __shared__ unsigned long long s_cand[CAP];
-  __shared__ unsigned long long s_sel[kTopK];
+// Lane holding the (r+1)-th set bit of mask (r < popc(mask)): a five-step
+// search over halves of the remaining bit range.
+__device__ __forceinline__ int nth_set_lane(unsigned mask, int r) {
+  int pos = 0;
+#pragma unroll
+  for (int w = 16; w > 0; w >>= 1) {
+    const int c = __popc((mask >> pos) & ((1u << w) - 1u));
+    if (r >= c) {
+      r -= c;
+      pos += w;
+    }
+  }
+  return pos;
+}
 
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int K = a.K;
-  const int rows = a.T * 4;
+// Forced ids of a row in increasing order: every valid id when nvp <= 16,
+// else [0, init) then [nvp - local, nvp), each kept only when it is a valid
+// id of a column of the plane.  Every lane gets nf; with keep, lane q < nf
+// also gets the q-th id and its raw score.
+struct Forced {
+  int fid;
+  float fsc;
+  int nf;
+};
+
+__device__ __forceinline__ Forced forced_ids(const SelectArgs &a, const float *src, int nvp,
+                                             int lane, bool keep) {
   const int scale = a.index_scale, off = a.index_offset;
-  const bool bulk = (K % 4 == 0) && ((reinterpret_cast<uintptr_t>(a.scores) & 15u) == 0);
-  const uint32_t bytes = (uint32_t)K * 4u;
-
-  if (tid == 0) {
-    s_abort = 0;
-    if (bulk) {
-      mbar_init(smem_u32(&s_bar[0]), 1);
-      mbar_init(smem_u32(&s_bar[1]), 1);
-      fence_mbarrier_init();
-    }
-  }
-  __syncthreads();
-  if (bulk && tid == 0 && (int)blockIdx.x < rows) {
-    mbar_arrive_expect_tx(smem_u32(&s_bar[0]), bytes);
-    bulk_load(smem_u32(bufs), a.scores + (long long)blockIdx.x * K, bytes, smem_u32(&s_bar[0]));
-  }
-
-  int it = 0;
-  int nvp_next = (int)blockIdx.x < rows ? __ldg(a.nvp + (blockIdx.x >> 2)) : 0;
-  for (int row = blockIdx.x; row < rows; row += gridDim.x, ++it) {
-    const int cur = bulk ? (it & 1) : 0;
-    float *rowv = bufs + cur * BUF;
-    const int nvp = nvp_next;  // loaded one row ahead, off the critical path
-    if (row + (int)gridDim.x < rows) nvp_next = __ldg(a.nvp + ((row + gridDim.x) >> 2));
-    if (bulk) {
-      const int next = row + gridDim.x;
-      if (tid == 0 && next < rows) {
-        const int nb = cur ^ 1;  // freed by the previous iteration's last barrier
-        mbar_arrive_expect_tx(smem_u32(&s_bar[nb]), bytes);
-        bulk_load(smem_u32(bufs + nb * BUF), a.scores + (long long)next * K, bytes,
-                  smem_u32(&s_bar[nb]));
-      }
-      if (!mbar_wait(smem_u32(&s_bar[cur]), (uint32_t)((it >> 1) & 1), &s_abort)) {
-        // a copy did not land in time: report and stop (no trap)
-        if (tid == 0 && a.errors) atomicAdd(a.errors, 1);
-        return;
-      }
+  const bool all = nvp <= kTopK;
+  const int nforced = all ? max(nvp, 0) : a.init_blocks + a.local_blocks;
+  int id = -1, col = 0;
+  bool ok = false;
+  if (lane < nforced && lane < kTopK) {
+    id = all ? lane : (lane < a.init_blocks ? lane : nvp - a.local_blocks + (lane - a.init_blocks));
+    const int d = id - off;
+    if (scale == 1) {
+      col = d;
+      ok = id >= 0 && id < nvp && d >= 0 && d < a.K;
     } else {
-      const float *src = a.scores + (long long)row * K;
-      for (int c = tid; c < K; c += NT) rowv[c] = src[c];
+      col = d / scale;
+      ok = id >= 0 && id < nvp && d >= 0 && d % scale == 0 && col < a.K;
     }
-    if (tid == 0) s_nc = 0;
-    const int t = row >> 2;
-    const int h = row & 3;
-    const int flag0 = warp == 0 ? early_flag<MODE>(a, lane, t, h) : -1;
+  }
+  const unsigned bal = __ballot_sync(0xFFFFFFFFu, ok);
+  Forced f{0x7FFFFFFF, -INFINITY, __popc(bal)};
+  if (keep) {
+    const float v = ok ? __ldg(src + col) : 0.0f;
+    // lane q < nf takes the entry of the lane holding the (q+1)-th set bit
+    const int srcl = nth_set_lane(bal, lane < f.nf ? lane : 0);
+    const int i2 = __shfl_sync(0xFFFFFFFFu, id, srcl);
+    const float v2 = __shfl_sync(0xFFFFFFFFu, v, srcl);
+    if (lane < f.nf) {
+      f.fid = i2;
+      f.fsc = v2;
+    }
+  }
+  return f;
+}
 
-    // forced ids, in increasing order: every valid id when nvp <= 16, else
-    // [0, init) then [nvp - local, nvp); each exists when it maps to a column
-    if (warp == 0) {
-      const bool all = nvp <= kTopK;
-      const int nforced = all ? max(nvp, 0) : a.init_blocks + a.local_blocks;
-      int id = -1;
-      bool ok = false;
-      if (lane < nforced && lane < kTopK) {
-        id = all ? lane
-                 : (lane < a.init_blocks ? lane : nvp - a.local_blocks + (lane - a.init_blocks));
-        const int d = id - off;
-        ok = id >= 0 && id < nvp && d >= 0 &&
-             (scale == 1 ? d < K : (d % scale == 0 && d / scale < K));
-      }
-      const unsigned bal = __ballot_sync(0xFFFFFFFFu, ok);
-      if (ok) s_fid[__popc(bal & ((1u << lane) - 1u))] = id;
-      if (lane == 0) s_nf = __popc(bal);
-    }
-    __syncthreads();  // the row buffer and the forced ids are ready
-    const int nf = s_nf;
-    const int m = kTopK - nf;
-    if (tid < nf) {
-      const int d = s_fid[tid] - off;
-      s_fsc[tid] = rowv[scale == 1 ? d : d / scale];
-    }
+// First free column: ids from init on (valid whenever nvp > 16).
+__device__ __forceinline__ int free_lo(const SelectArgs &a) {
+  const int scale = a.index_scale, off = a.index_offset;
+  const int d = a.init_blocks - off;
+  return d <= 0 ? 0 : min((d + scale - 1) / scale, a.K);
+}
 
-    // free columns: ids in [init, nvp - local) when nvp > 16, else none
-    int c_lo = 0, c_hi = 0;
-    if (nvp > kTopK) {
-      const int id_lo = a.init_blocks, id_hi = nvp - a.local_blocks;   // [id_lo, id_hi)
-      c_lo = id_lo - off <= 0 ? 0 : (id_lo - off + scale - 1) / scale;
-      c_hi = id_hi - off <= 0 ? 0 : (id_hi - off + scale - 1) / scale;
-      c_hi = min(c_hi, K);
-      c_lo = min(c_lo, c_hi);
-    }
-    // phase 1: per-thread best free entry (score, then lower column)
-    float best = 0.0f;
-    int bc = -1;
-    {
-      const float4 *r4 = reinterpret_cast<const float4 *>(rowv);
-      const int f_lo = c_lo >> 2, f_hi = (c_hi + 3) >> 2;
-      for (int f = f_lo + tid; f < f_hi; f += NT) {
-        const float4 x = r4[f];
-        const float vv[4] = {x.x, x.y, x.z, x.w};
-#pragma unroll
-        for (int k = 0; k < 4; ++k) {
-          const int c = 4 * f + k;
-          if ((unsigned)(c - c_lo) < (unsigned)(c_hi - c_lo) && (bc < 0 || vv[k] > best)) {
-            best = vv[k];
-            bc = c;
-          }
-        }
-      }
-    }
-    const unsigned long long tm = bc < 0 ? 0ull : make_key(best, bc * scale + off);
-
-    // tau = m-th largest thread maximum, in two levels: each warp's top m of
-    // its lanes' maxima, then the top m of those lists (1 = fewer than m exist)
-    {
-      unsigned long long my = tm;
-      for (int r = 0; r < m; ++r) {
-        const unsigned long long w = warp_max_key(my);
-        if (lane == 0) s_wtop[warp][r] = w;
-        if (w != 0 && my == w) my = 0;
-      }
-    }
-    __syncthreads();
-    if (warp == 0) {
-      unsigned long long loc[WL];
-      unsigned long long lmax = 0;
-#pragma unroll
-      for (int j = 0; j < WL; ++j) {
-        const int k = lane + 32 * j;
-        const int w = k / kTopK, r = k % kTopK;
-        loc[j] = (w < NW && r < m) ? s_wtop[w][r] : 0ull;
-        lmax = loc[j] > lmax ? loc[j] : lmax;
-      }
-      unsigned long long tau = 0;
-      int found = 0;
-      for (int r = 0; r < m; ++r) {
-        const unsigned long long w = warp_max_key(lmax);
-        if (w == 0) break;
-        tau = w;
-        ++found;
-        if (lmax == w) {
-          lmax = 0;
-#pragma unroll
-          for (int j = 0; j < WL; ++j) {
-            if (loc[j] == w) loc[j] = 0;
-            lmax = loc[j] > lmax ? loc[j] : lmax;
-          }
-        }
-      }
-      if (lane == 0) s_tau = (found < m) ? 1ull : tau;
-    }
-    __syncthreads();
-
-    // candidates: keys >= tau (only the m threads whose maximum reached tau hold any)
-    if (m > 0 && tm != 0 && tm >= s_tau) {
-      const unsigned long long tau = s_tau;
-      // keys >= tau have scores >= tau's score (tau = 1 has none: -inf)
-      const float ts = (tau >> 32) == 0 ? -INFINITY : unord_float((uint32_t)(tau >> 32));
-      const float4 *r4 = reinterpret_cast<const float4 *>(rowv);
-      const int f_lo = c_lo >> 2, f_hi = (c_hi + 3) >> 2;
-      for (int f = f_lo + tid; f < f_hi; f += NT) {
-        const float4 x = r4[f];
-        const float vv[4] = {x.x, x.y, x.z, x.w};
-#pragma unroll
-        for (int k = 0; k < 4; ++k) {
-          const int c = 4 * f + k;
-          if (!(vv[k] >= ts) || (unsigned)(c - c_lo) >= (unsigned)(c_hi - c_lo)) continue;
-          const unsigned long long key = make_key(vv[k], c * scale + off);
-          if (key >= tau) {
-            const int slot = atomicAdd(&s_nc, 1);
-            if (slot < CAP) s_cand[slot] = key;
-          }
-        }
-      }
-    }
-    __syncthreads();
-    const int nc = min(s_nc, CAP);
-    const int nch = min(nc, m);
-
-    // the m largest candidates: by rank when few, else by rounds in warp 0
-    if (nc <= m) {
-      if (tid < nc) s_sel[tid] = s_cand[tid];
-    } else if (nc <= NT) {
-      if (tid < nc) {
-        const unsigned long long my = s_cand[tid];
-        int rank = 0;
-        for (int j = 0; j < nc; ++j) rank += (s_cand[j] > my) ? 1 : 0;
-        if (rank < m) s_sel[rank] = my;
-      }
-    } else if (warp == 0) {
-      unsigned long long prev = ~0ull;
-      for (int r = 0; r < m; ++r) {
-        unsigned long long local = 0;
-        for (int j = lane; j < nc; j += 32) {
-          const unsigned long long x = s_cand[j];
-          if (x < prev && x > local) local = x;
-        }
-        const unsigned long long w = warp_max_key(local);
-        if (lane == 0) s_sel[r] = w;
-        prev = w;
-      }
-    }
-    __syncthreads();
-
-    if (warp == 0) {
-      const int n = nf + nch;
-      int my_id = 0x7FFFFFFF;
-      float my_sc = -INFINITY;
-      if (lane < nf) {
-        my_id = s_fid[lane];
-        my_sc = s_fsc[lane];
-      } else if (lane < n) {
-        my_id = key_id(s_sel[lane - nf]);
-        const int d = my_id - off;
-        my_sc = rowv[scale == 1 ? d : d / scale];  // raw score bits
-      }
-      int out_id;
-      float out_sc;
-      sort_by_id_16(lane, n, my_id, my_sc, out_id, out_sc);
-      emit_row<MODE>(a, lane, row, t, h, out_id, out_sc, flag0);
-    }
-    __syncthreads();  // this row's buffer and scratch may be reused
+// Free columns of a row: ids in [init, nvp - local) when nvp > 16, else none.
+__device__ __forceinline__ void free_range(const SelectArgs &a, int nvp, int &c_lo, int &c_hi) {
+  const int scale = a.index_scale, off = a.index_offset;
+  c_lo = 0;
+  c_hi = 0;
+  if (nvp > kTopK) {
+    const int id_hi = nvp - a.local_blocks;
+    c_hi = id_hi - off <= 0 ? 0 : (id_hi - off + scale - 1) / scale;
+    c_hi = min(c_hi, a.K);
+    c_lo = min(free_lo(a), c_hi);
   }
 }
 
-// Warp-per-row select: each warp owns whole rows (row = global warp index,
-// then + total warps), so no CTA barrier sits between the phases and every
-// row of a launch can be in flight at once.
-//   1. forced ids (at most 16, read directly) go to lanes 0..nf-1;
-//   2. every lane scans its strided float4s of the free column range and
-//      keeps its best entry (score, then lower column);
-//   3. tau = m-th largest lane best (m = 16 - nf, rounds of a warp max);
-//      only the <= m lanes whose best reaches tau hold keys >= tau, and they
-//      rescan their share into a per-warp candidate buffer (a float compare
-//      against tau's score filters first);
-//   4. the m largest candidates (rounds of a warp max), forced + chosen
-//      ordered by id, written or published.
-// If a row has more candidates than the buffer holds (only possible with
-// very many equal scores), the warp picks the m largest directly from the
-// row by rounds instead.  Rows are read with float4 loads when K % 4 == 0 and
-// the plane is 16-byte aligned, else with scalar loads.
-constexpr int kSelWarps = 4;    // warps (rows in flight) per CTA
-constexpr int kCandCap = 256;   // candidates per warp
-constexpr int kChunk = 8;       // float4 loads in flight per lane
+// A lower bound of the m-th largest of the lanes' keys (0 = no key): the
+// score half of that key with the id half 0, found by rounds of a warp max
+// over the score halves (lanes tied on a score leave together); 1 when fewer
+// than m lanes hold a key, 0 when m <= 0.  Every key >= the m-th largest
+// lane key is >= the bound.
+__device__ __forceinline__ unsigned long long tau_lower_bound(unsigned long long k, int m) {
+  if (m <= 0) return 0ull;
+  uint32_t hi = (uint32_t)(k >> 32);  // real keys have a non-zero score half
+  int found = 0;
+  for (;;) {
+    const uint32_t cur = __reduce_max_sync(0xFFFFFFFFu, hi);
+    if (cur == 0u) return 1ull;
+    found += __popc(__ballot_sync(0xFFFFFFFFu, hi == cur));
+    if (found >= m) return (unsigned long long)cur << 32;
+    if (hi == cur) hi = 0u;
+  }
+}
 
-// Best (score, then lower column) over columns [c_lo, c_hi) owned by this
-// lane, and keys >= tau collected into cand[] when collect is set.
+// The m largest keys < prev among this lane's free columns, by rounds (the
+// exact path when the candidate buffer overflows).  Covers columns first,
+// first + stride, ... for the scalar layout, and element indices
+// 4 f .. 4 f + 3 for f = f_lo + first + j * stride with float4 reads.
 template <bool VEC>
-__device__ __forceinline__ void scan_row(const float *src, int c_lo, int c_hi, int lane,
-                                         float &best, int &bc) {
-  if constexpr (VEC) {
-    const float4 *r4 = reinterpret_cast<const float4 *>(src);
-    const int f_lo = c_lo >> 2, f_hi = (c_hi + 3) >> 2;
-    for (int f0 = f_lo + lane; f0 < f_hi; f0 += 32 * kChunk) {
-      float4 x[kChunk];
+__device__ void rounds_from_row(const float *src, int c_lo, int c_hi, int lane, int first,
+                                int stride, int scale, int off, int m, unsigned long long *sel) {
+  unsigned long long prev = ~0ull;
+  for (int r = 0; r < m; ++r) {
+    unsigned long long local = 0;
+    auto look = [&](int c) {
+      if ((unsigned)(c - c_lo) >= (unsigned)(c_hi - c_lo)) return;
+      const unsigned long long key = make_key(__ldg(src + c), c * scale + off);
+      if (key < prev && key > local) local = key;
+    };
+    if constexpr (VEC) {
+      const int f_lo = c_lo >> 2, f_hi = (c_hi + 3) >> 2;
+      for (int f = f_lo + first; f < f_hi; f += stride)
+        for (int k = 0; k < 4; ++k) look(4 * f + k);
+    } else {
+      for (int c = c_lo + first; c < c_hi; c += stride) look(c);
+    }
+    const unsigned long long w = warp_max_key(local);
+    if (lane == 0) sel[r] = w;
+    prev = w;
+    if (w == 0) break;
+  }
+}
+
+// kChunk float4 loads at f0, f0 + stride, ... (those below f_end).
+__device__ __forceinline__ void load_batch(const float4 *r4, int f0, int stride, int f_end,
+                                           float4 (&x)[kChunk]) {
 #pragma unroll
-      for (int u = 0; u < kChunk; ++u) {
-        const int f = f0 + 32 * u;
-        x[u] = f < f_hi ? __ldg(r4 + f) : make_float4(0.f, 0.f, 0.f, 0.f);
-      }
+  for (int u = 0; u < kChunk; ++u) {
+    const int f = f0 + stride * u;
+    x[u] = f < f_end ? __ldg(r4 + f) : make_float4(0.f, 0.f, 0.f, 0.f);
+  }
+}
+
+// Shared state of one warp's selection: its candidate buffer and count,
+// and a column of recorded float4 maxima per lane (entry j at cm[32 j]).
+struct WarpScratch {
+  unsigned long long *cand;
+  int *nc;
+  float *cm;
+};
+
+// Candidates (keys >= tau) from the m largest: placed by rank into sel
+// (descending), or taken by rounds from the columns on overflow.  Returns
+// their number; sel is readable after __syncwarp.
+template <bool VEC>
+__device__ __forceinline__ int place_candidates(const float *src, int c_lo, int c_hi, int first,
+                                                int stride, int scale, int off, int m, int lane,
+                                                const WarpScratch &w, unsigned long long *sel) {
+  __syncwarp();
+  const int nc = *w.nc;
+  if (nc > kCandCap) {
+    rounds_from_row<VEC>(src, c_lo, c_hi, lane, first, stride, scale, off, m, sel);
+    __syncwarp();
+    int n = 0;
+    while (n < m && sel[n] != 0ull) ++n;
+    return n;
+  }
+  for (int j = lane; j < nc; j += 32) {
+    const unsigned long long my = w.cand[j];
+    int rank = 0;
+    for (int i = 0; i < nc; ++i) rank += (w.cand[i] > my) ? 1 : 0;
+    if (rank < m) sel[rank] = my;
+  }
+  return min(nc, m);
+}
+
+// Appends key (v, c) to the candidates when it is >= tau.
+__device__ __forceinline__ void offer_key(float v, int c, float ts, unsigned long long tau,
+                                          int scale, int off, const WarpScratch &w) {
+  if (!(v >= ts)) return;
+  const unsigned long long key = make_key(v, c * scale + off);
+  if (key >= tau) {
+    const int slot = atomicAdd(w.nc, 1);
+    if (slot < kCandCap) w.cand[slot] = key;
+  }
+}
+
+// This warp's m largest keys among float4 chunks f_lo + first + j * stride
+// of the free range [c_lo, c_hi), into sel (descending; readable after
+// __syncwarp); returns how many.  x holds the lane's first batch, loaded
+// from the same chunks before the range was known (and is reused for the
+// later batches).
+__device__ __forceinline__ int warp_top_m_vec(const float *src, float4 (&x)[kChunk],
+                                              int c_lo, int c_hi, int first, int stride,
+                                              int scale, int off, int m, int lane,
+                                              const WarpScratch &w, unsigned long long *sel) {
+  if (m <= 0) return 0;
+  const float4 *r4 = reinterpret_cast<const float4 *>(src);
+  const int f_lo = c_lo >> 2, f_hi = (c_hi + 3) >> 2;
+  const int f_first = f_lo + first;
+  // 1. scan: best key, and every chunk's largest value into cm
+  float best = 0.0f;
+  int bc = -1;
+  int nj = 0;
+  for (int f0 = f_first; f0 < f_hi; f0 += stride * kChunk) {
+    if (f0 != f_first) load_batch(r4, f0, stride, f_hi, x);
 #pragma unroll
-      for (int u = 0; u < kChunk; ++u) {
-        const int f = f0 + 32 * u;
+    for (int u = 0; u < kChunk; ++u) {
+      const int f = f0 + stride * u;
+      if (f >= f_hi) break;
+      const float m4 = fmaxf(fmaxf(x[u].x, x[u].y), fmaxf(x[u].z, x[u].w));
+      w.cm[32 * nj++] = m4;
+      if (bc < 0 || m4 > best) {
         const float vv[4] = {x[u].x, x[u].y, x[u].z, x[u].w};
 #pragma unroll
         for (int k = 0; k < 4; ++k) {
@@ -399,196 +354,222 @@ __device__ __forceinline__ void scan_row(const float *src, int c_lo, int c_hi, i
         }
       }
     }
-  } else {
-    for (int c = c_lo + lane; c < c_hi; c += 32) {
-      const float v = __ldg(src + c);
-      if (bc < 0 || v > best) {
-        best = v;
-        bc = c;
-      }
-    }
   }
-}
-
-// Appends this lane's keys >= tau among columns [c_lo, c_hi) to cand.
-template <bool VEC>
-__device__ __forceinline__ void collect_row(const float *src, int c_lo, int c_hi, int lane,
-                                            int scale, int off, unsigned long long tau,
-                                            unsigned long long *cand, int *ncand) {
-  const float ts = (tau >> 32) == 0 ? -INFINITY : unord_float((uint32_t)(tau >> 32));
-  auto offer = [&](float v, int c) {
-    if (!(v >= ts)) return;
-    const unsigned long long key = make_key(v, c * scale + off);
-    if (key >= tau) {
-      const int slot = atomicAdd(ncand, 1);
-      if (slot < kCandCap) cand[slot] = key;
-    }
-  };
-  if constexpr (VEC) {
-    const float4 *r4 = reinterpret_cast<const float4 *>(src);
-    const int f_lo = c_lo >> 2, f_hi = (c_hi + 3) >> 2;
-    for (int f = f_lo + lane; f < f_hi; f += 32) {
-      const float4 x = __ldg(r4 + f);
-      const float vv[4] = {x.x, x.y, x.z, x.w};
+  // 2. tau
+  const unsigned long long tm = bc < 0 ? 0ull : make_key(best, bc * scale + off);
+  const unsigned long long tau = tau_lower_bound(tm, m);
+  if (lane == 0) *w.nc = 0;
+  __syncwarp();
+  // 3. re-read the chunks whose maximum reaches tau's score, four at a time
+  if (tm != 0ull && tm >= tau) {
+    const float ts = (tau >> 32) == 0 ? -INFINITY : unord_float((uint32_t)(tau >> 32));
+    unsigned mask = 0;
+    for (int j = 0; j < nj; ++j)
+      if (w.cm[32 * j] >= ts) mask |= 1u << j;
+    while (mask != 0u) {
+      int fq[4];
+      float4 y[4];
 #pragma unroll
-      for (int k = 0; k < 4; ++k) {
-        const int c = 4 * f + k;
-        if ((unsigned)(c - c_lo) < (unsigned)(c_hi - c_lo)) offer(vv[k], c);
+      for (int q = 0; q < 4; ++q) {
+        fq[q] = -1;
+        if (mask != 0u) {
+          fq[q] = f_first + stride * (__ffs(mask) - 1);
+          mask &= mask - 1u;
+        }
+      }
+#pragma unroll
+      for (int q = 0; q < 4; ++q)
+        y[q] = fq[q] >= 0 ? __ldg(r4 + fq[q]) : make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        if (fq[q] < 0) continue;
+        const float vv[4] = {y[q].x, y[q].y, y[q].z, y[q].w};
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          const int c = 4 * fq[q] + k;
+          if ((unsigned)(c - c_lo) < (unsigned)(c_hi - c_lo)) offer_key(vv[k], c, ts, tau, scale, off, w);
+        }
       }
     }
-  } else {
-    for (int c = c_lo + lane; c < c_hi; c += 32) offer(__ldg(src + c), c);
   }
+  // 4. the m largest candidates
+  return place_candidates<true>(src, c_lo, c_hi, first, stride, scale, off, m, lane, w, sel);
 }
 
-// The m largest keys < prev among this lane's free columns, by rounds (the
-// exact path for rows whose candidates overflow the buffer).
-template <bool VEC>
-__device__ void rounds_from_row(const float *src, int c_lo, int c_hi, int lane, int scale,
-                                int off, int m, unsigned long long *sel) {
-  unsigned long long prev = ~0ull;
-  for (int r = 0; r < m; ++r) {
-    unsigned long long local = 0;
-    for (int c = c_lo + lane; c < c_hi; c += 32) {
-      const unsigned long long key = make_key(__ldg(src + c), c * scale + off);
-      if (key < prev && key > local) local = key;
+// Same for the scalar layout (columns c_lo + first + j * stride), with a
+// plain rescan of the lane's columns in step 3.
+__device__ __forceinline__ int warp_top_m_scalar(const float *src, int c_lo, int c_hi, int first,
+                                                 int stride, int scale, int off, int m, int lane,
+                                                 const WarpScratch &w, unsigned long long *sel) {
+  if (m <= 0) return 0;
+  float best = 0.0f;
+  int bc = -1;
+  for (int c = c_lo + first; c < c_hi; c += stride) {
+    const float v = __ldg(src + c);
+    if (bc < 0 || v > best) {
+      best = v;
+      bc = c;
     }
-    const unsigned long long w = warp_max_key(local);
-    if (lane == 0) sel[r] = w;
-    prev = w;
-    if (w == 0) break;
   }
-  (void)VEC;
+  const unsigned long long tm = bc < 0 ? 0ull : make_key(best, bc * scale + off);
+  const unsigned long long tau = tau_lower_bound(tm, m);
+  if (lane == 0) *w.nc = 0;
+  __syncwarp();
+  if (tm != 0ull && tm >= tau) {
+    const float ts = (tau >> 32) == 0 ? -INFINITY : unord_float((uint32_t)(tau >> 32));
+    for (int c = c_lo + first; c < c_hi; c += stride)
+      offer_key(__ldg(src + c), c, ts, tau, scale, off, w);
+  }
+  return place_candidates<false>(src, c_lo, c_hi, first, stride, scale, off, m, lane, w, sel);
 }
 
+// Raw score of a selected key: the key's score half is exact for every
+// score but a zero, whose sign is read back from the row.
+__device__ __forceinline__ float key_score(unsigned long long k, const float *row_src, int scale,
+                                           int off) {
+  const uint32_t o = (uint32_t)(k >> 32);
+  if (o != 0x80000000u) return unord_float(o);
+  const int d = key_id(k) - off;
+  return __ldg(row_src + (scale == 1 ? d : d / scale));
+}
+
+// Rows up to 2048 columns: one warp per row (row = global warp index, then
+// + total warps), no CTA barrier.
 template <int MODE, bool VEC>
 __global__ void __launch_bounds__(32 * kSelWarps, 8) select_warp_kernel(const SelectArgs a) {
   __shared__ unsigned long long s_cand[kSelWarps][kCandCap];
   __shared__ unsigned long long s_sel[kSelWarps][kTopK];
+  __shared__ float s_cm[kSelWarps][kWarpRowChunks * 32];
   __shared__ int s_nc[kSelWarps];
 
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  const int K = a.K;
   const int rows = a.T * 4;
   const int scale = a.index_scale, off = a.index_offset;
-  unsigned long long *cand = s_cand[warp];
   unsigned long long *sel = s_sel[warp];
+  const WarpScratch ws{s_cand[warp], &s_nc[warp], &s_cm[warp][lane]};
+  const int f_start = (free_lo(a) >> 2) + lane;
 
   for (int row = blockIdx.x * kSelWarps + warp; row < rows; row += gridDim.x * kSelWarps) {
     const int t = row >> 2, h = row & 3;
+    const float *src = a.scores + (long long)row * a.K;
+    float4 x0[kChunk];
+    if constexpr (VEC) load_batch(reinterpret_cast<const float4 *>(src), f_start, 32, a.K >> 2, x0);
     const int nvp = __ldg(a.nvp + t);
-    const float *src = a.scores + (long long)row * K;
     const int flag0 = early_flag<MODE>(a, lane, t, h);
-
-    // forced ids in increasing order: every valid id when nvp <= 16, else
-    // [0, init) then [nvp - local, nvp); lane f < nf holds the f-th
-    int fid = 0x7FFFFFFF;
-    float fsc = -INFINITY;
-    int nf;
-    {
-      const bool all = nvp <= kTopK;
-      const int nforced = all ? max(nvp, 0) : a.init_blocks + a.local_blocks;
-      int id = -1, col = 0;
-      bool ok = false;
-      if (lane < nforced && lane < kTopK) {
-        id = all ? lane
-                 : (lane < a.init_blocks ? lane : nvp - a.local_blocks + (lane - a.init_blocks));
-        const int d = id - off;
-        if (scale == 1) {
-          col = d;
-          ok = id >= 0 && id < nvp && d >= 0 && d < K;
-        } else {
-          col = d / scale;
-          ok = id >= 0 && id < nvp && d >= 0 && d % scale == 0 && col < K;
-        }
-      }
-      const float v = ok ? __ldg(src + col) : 0.0f;
-      const unsigned bal = __ballot_sync(0xFFFFFFFFu, ok);
-      nf = __popc(bal);
-      // move entry of lane L (pos p) to lane p
-      const int pos = __popc(bal & ((1u << lane) - 1u));
-      for (int p = 0; p < nf; ++p) {
-        const int srcl = __fns(bal, 0, p + 1);
-        const int i2 = __shfl_sync(0xFFFFFFFFu, id, srcl);
-        const float v2 = __shfl_sync(0xFFFFFFFFu, v, srcl);
-        if (lane == p) {
-          fid = i2;
-          fsc = v2;
-        }
-      }
-      (void)pos;
-    }
-    const int m = kTopK - nf;
-
-    // free columns: ids in [init, nvp - local) when nvp > 16, else none
-    int c_lo = 0, c_hi = 0;
-    if (nvp > kTopK) {
-      const int id_lo = a.init_blocks, id_hi = nvp - a.local_blocks;
-      c_lo = id_lo - off <= 0 ? 0 : (id_lo - off + scale - 1) / scale;
-      c_hi = id_hi - off <= 0 ? 0 : (id_hi - off + scale - 1) / scale;
-      c_hi = min(c_hi, K);
-      c_lo = min(c_lo, c_hi);
-    }
-    float best = 0.0f;
-    int bc = -1;
-    scan_row<VEC>(src, c_lo, c_hi, lane, best, bc);
-    const unsigned long long tm = bc < 0 ? 0ull : make_key(best, bc * scale + off);
-
-    // tau = m-th largest lane best (1 = fewer than m lanes hold an entry)
-    unsigned long long tau = 0;
-    {
-      unsigned long long my = tm;
-      int found = 0;
-      for (int r = 0; r < m; ++r) {
-        const unsigned long long w = warp_max_key(my);
-        if (w == 0) break;
-        tau = w;
-        ++found;
-        if (my == w) my = 0;
-      }
-      if (found < m) tau = 1;
-    }
-    if (lane == 0) s_nc[warp] = 0;
+    const Forced f = forced_ids(a, src, nvp, lane, true);
+    const int m = kTopK - f.nf;
+    int c_lo, c_hi;
+    free_range(a, nvp, c_lo, c_hi);
+    int nch;
+    if constexpr (VEC)
+      nch = warp_top_m_vec(src, x0, c_lo, c_hi, lane, 32, scale, off, m, lane, ws, sel);
+    else
+      nch = warp_top_m_scalar(src, c_lo, c_hi, lane, 32, scale, off, m, lane, ws, sel);
     __syncwarp();
-    if (m > 0 && tm != 0 && tm >= tau)
-      collect_row<VEC>(src, c_lo, c_hi, lane, scale, off, tau, cand, &s_nc[warp]);
-    __syncwarp();
-    const int nc = s_nc[warp];
-    int nch = 0;
-    if (m > 0) {
-      if (nc > kCandCap) {
-        rounds_from_row<VEC>(src, c_lo, c_hi, lane, scale, off, m, sel);
-        nch = 0;
-        __syncwarp();
-        for (int r = 0; r < m; ++r) nch += sel[r] != 0 ? 1 : 0;
-      } else if (nc <= m) {
-        for (int j = lane; j < nc; j += 32) sel[j] = cand[j];
-        nch = nc;
-      } else {
-        // rank each candidate among the others (nc <= 256: 8 per lane)
-        for (int j = lane; j < nc; j += 32) {
-          const unsigned long long my = cand[j];
-          int rank = 0;
-          for (int i = 0; i < nc; ++i) rank += (cand[i] > my) ? 1 : 0;
-          if (rank < m) sel[rank] = my;
-        }
-        nch = m;
-      }
-    }
-    __syncwarp();
-    const int n = nf + nch;
-    int my_id = fid;
-    float my_sc = fsc;
-    if (lane >= nf && lane < n) {
-      my_id = key_id(sel[lane - nf]);
-      const int d = my_id - off;
-      my_sc = __ldg(src + (scale == 1 ? d : d / scale));  // raw score bits
+    const int n = f.nf + nch;
+    int my_id = f.fid;
+    float my_sc = f.fsc;
+    if (lane >= f.nf && lane < n) {
+      const unsigned long long k = sel[lane - f.nf];
+      my_id = key_id(k);
+      my_sc = key_score(k, src, scale, off);
     }
     int out_id;
     float out_sc;
     sort_by_id_16(lane, n, my_id, my_sc, out_id, out_sc);
     emit_row<MODE>(a, lane, row, t, h, out_id, out_sc, flag0);
     __syncwarp();
+  }
+}
+
+// Rows longer than 2048 columns: one CTA of RW warps per row (grid-stride
+// over the rows).  Warp w takes the top m of the float4 chunks (or
+// elements) w * 32 + lane + j * 32 * RW of the free range; after one barrier
+// the last warp, which keeps the forced ids, takes the top m of the warps'
+// lists (the m largest keys of the row are the m largest of their union)
+// and emits the row.  lb = the largest m-th entry of a full list bounds the
+// row's m-th largest key from below, so only keys >= lb are ranked.
+template <int RW, int MODE, bool VEC>
+__global__ void __launch_bounds__(32 * RW, 32 / RW) select_row_kernel(const SelectArgs a) {
+  // float4 rows have K % 4 == 0: at most kLongRowMaxK / 4 float4s
+  static_assert(kLongRowChunks * 32 * RW >= kLongRowMaxK / 4, "chunk record too small");
+  __shared__ unsigned long long s_cand[RW][kCandCap];
+  __shared__ unsigned long long s_wsel[RW][kTopK];
+  __shared__ unsigned long long s_surv[RW * kTopK];
+  __shared__ unsigned long long s_mout[kTopK];
+  __shared__ float s_cm[RW][kLongRowChunks * 32];
+  __shared__ int s_nc[RW];
+  __shared__ int s_wn[RW];
+
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int rows = a.T * 4;
+  const int scale = a.index_scale, off = a.index_offset;
+  const bool merger = warp == RW - 1;
+  const int first = warp * 32 + lane, stride = 32 * RW;
+  const WarpScratch ws{s_cand[warp], &s_nc[warp], &s_cm[warp][lane]};
+  const int f_start = (free_lo(a) >> 2) + first;
+  for (int row = blockIdx.x; row < rows; row += gridDim.x) {
+    const int t = row >> 2, h = row & 3;
+    const float *src = a.scores + (long long)row * a.K;
+    float4 x0[kChunk];
+    if constexpr (VEC)
+      load_batch(reinterpret_cast<const float4 *>(src), f_start, stride, a.K >> 2, x0);
+    const int nvp = __ldg(a.nvp + t);
+    const int flag0 = merger ? early_flag<MODE>(a, lane, t, h) : -1;
+    const Forced f = forced_ids(a, src, nvp, lane, merger);
+    const int m = kTopK - f.nf;
+    int c_lo, c_hi;
+    free_range(a, nvp, c_lo, c_hi);
+    int nw;
+    if constexpr (VEC)
+      nw = warp_top_m_vec(src, x0, c_lo, c_hi, first, stride, scale, off, m, lane, ws, s_wsel[warp]);
+    else
+      nw = warp_top_m_scalar(src, c_lo, c_hi, first, stride, scale, off, m, lane, ws, s_wsel[warp]);
+    if (lane == 0) s_wn[warp] = nw;
+    __syncthreads();
+
+    if (merger) {
+      int nch = 0;
+      if (m > 0) {
+        unsigned long long lb = 0;
+        if (lane < RW && s_wn[lane] >= m) lb = s_wsel[lane][m - 1];
+        lb = warp_max_key(lb);
+        constexpr int PL = (RW * kTopK + 31) / 32;
+        int ns = 0;
+#pragma unroll
+        for (int j = 0; j < PL; ++j) {
+          const int q = lane + 32 * j;
+          const int w = q / kTopK, i = q % kTopK;
+          const unsigned long long k = (w < RW && i < s_wn[w]) ? s_wsel[w][i] : 0ull;
+          const bool keep = k != 0ull && k >= lb;
+          const unsigned bal = __ballot_sync(0xFFFFFFFFu, keep);
+          if (keep) s_surv[ns + __popc(bal & ((1u << lane) - 1u))] = k;
+          ns += __popc(bal);
+        }
+        __syncwarp();
+        for (int j = lane; j < ns; j += 32) {
+          const unsigned long long my = s_surv[j];
+          int rank = 0;
+          for (int i = 0; i < ns; ++i) rank += (s_surv[i] > my) ? 1 : 0;
+          if (rank < m) s_mout[rank] = my;
+        }
+        nch = min(m, ns);
+        __syncwarp();
+      }
+      const int n = f.nf + nch;
+      int my_id = f.fid;
+      float my_sc = f.fsc;
+      if (lane >= f.nf && lane < n) {
+        const unsigned long long k = s_mout[lane - f.nf];
+        my_id = key_id(k);
+        my_sc = key_score(k, src, scale, off);
+      }
+      int out_id;
+      float out_sc;
+      sort_by_id_16(lane, n, my_id, my_sc, out_id, out_sc);
+      emit_row<MODE>(a, lane, row, t, h, out_id, out_sc, flag0);
+    }
+    __syncthreads();  // lists are reused by the next row
   }
 }
 
@@ -797,38 +778,28 @@ __global__ void __launch_bounds__(128) merge_tagged_kernel(const MergeArgs a) {
 
 }  // namespace
 
-constexpr int kWarpRowMaxK = 2048;  // rows up to this long: one warp per row
-constexpr int kLargeK = 12288;
 
-cudaError_t select_prepare() {
-  const int big = 2 * kLargeK * 4;
-  cudaError_t e = cudaFuncSetAttribute(select_block_kernel<256, kLargeK, kEmitPlain>,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize, big);
-  if (e != cudaSuccess) return e;
-  e = cudaFuncSetAttribute(select_block_kernel<256, kLargeK, kEmitLegacy>,
-                           cudaFuncAttributeMaxDynamicSharedMemorySize, big);
-  if (e != cudaSuccess) return e;
-  return cudaFuncSetAttribute(select_block_kernel<256, kLargeK, kEmitTagged>,
-                              cudaFuncAttributeMaxDynamicSharedMemorySize, big);
-}
+cudaError_t select_prepare() { return cudaSuccess; }
 
 cudaError_t launch_select(const SelectArgs &a, int mode, int sm_count, cudaStream_t stream) {
   const int rows = a.T * 4;
   if (rows == 0) return cudaSuccess;
+  // float4 rows when every row starts on a 16-byte boundary
+  const bool vec = (a.K % 4 == 0) && ((reinterpret_cast<uintptr_t>(a.scores) & 15u) == 0);
   if (a.K > kWarpRowMaxK) {
-    // long rows: two CTAs per SM, each double-buffering rows in shared memory
-    const size_t smem = 2 * (size_t)kLargeK * 4;
-    const int grid = rows < 2 * sm_count ? rows : 2 * sm_count;
-    if (mode == kEmitLegacy)
-      select_block_kernel<256, kLargeK, kEmitLegacy><<<grid, 256, smem, stream>>>(a);
-    else if (mode == kEmitTagged)
-      select_block_kernel<256, kLargeK, kEmitTagged><<<grid, 256, smem, stream>>>(a);
-    else
-      select_block_kernel<256, kLargeK, kEmitPlain><<<grid, 256, smem, stream>>>(a);
+    const int threads = 32 * kRowWarps;
+    if (mode == kEmitLegacy) {
+      if (vec) select_row_kernel<kRowWarps, kEmitLegacy, true><<<rows, threads, 0, stream>>>(a);
+      else select_row_kernel<kRowWarps, kEmitLegacy, false><<<rows, threads, 0, stream>>>(a);
+    } else if (mode == kEmitTagged) {
+      if (vec) select_row_kernel<kRowWarps, kEmitTagged, true><<<rows, threads, 0, stream>>>(a);
+      else select_row_kernel<kRowWarps, kEmitTagged, false><<<rows, threads, 0, stream>>>(a);
+    } else {
+      if (vec) select_row_kernel<kRowWarps, kEmitPlain, true><<<rows, threads, 0, stream>>>(a);
+      else select_row_kernel<kRowWarps, kEmitPlain, false><<<rows, threads, 0, stream>>>(a);
+    }
     return cudaGetLastError();
   }
-  // short rows: one warp per row; float4 loads when every row is 16-byte aligned
-  const bool vec = (a.K % 4 == 0) && ((reinterpret_cast<uintptr_t>(a.scores) & 15u) == 0);
   const int grid = (rows + kSelWarps - 1) / kSelWarps;
   const int threads = 32 * kSelWarps;
   if (mode == kEmitLegacy) {

@@ -112,3 +112,19 @@ def test_long_rows_with_concentrated_maxima():
     plane[1, :, cols] = 100.0
     nvp = torch.tensor([K, K, K // 3], dtype=torch.int32)
     _check(plane, nvp, 2, 3, what="long rows")
+
+
+def test_long_row_candidate_overflow_in_one_warp_slice():
+    # Rows longer than 2048 columns are split over 8 warps; warp w owns the
+    # float4 chunks w * 32 + lane + 256 j.  Large values over all of warp 0's
+    # chunks overflow that warp's candidate buffer (exact fallback path).
+    K = 12284
+    plane = torch.randn((2, 4, K))
+    f = (torch.arange(32)[:, None] + 256 * torch.arange(K // 1024 + 1)[None, :]).reshape(-1)
+    f = f[4 * f + 3 < K]
+    cols = (4 * f[:, None] + torch.arange(4)[None, :]).reshape(-1)
+    plane[:, :, cols] = 50.0 + torch.rand(cols.numel())
+    plane[1, :, cols] = 50.0
+    nvp = torch.tensor([K, 9000], dtype=torch.int32)
+    for init, local in [(0, 0), (3, 4)]:
+        _check(plane, nvp, init, local, what=f"warp-slice overflow init={init} local={local}")
