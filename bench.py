@@ -359,7 +359,10 @@ class SelectBench:
         self.out_s = torch.empty((self.T, 4, 16), dtype=torch.float32, device=device)
         self.out_i = torch.empty((self.T, 4, 16), dtype=torch.int32, device=device)
         self.init, self.local = W.SELECT_INIT, W.SELECT_LOCAL
-        self.score_bytes = self.T * 4 * self.K * 4 + self.T * 4 + self.T * 4 * 16 * 8
+        # valid columns only (ids < num_valid_pages; index scale 1, offset 0):
+        # the columns past them need not be read
+        valid = self.nvp.clamp(max=self.K).to(torch.int64)
+        self.score_bytes = int(valid.sum().item()) * 4 * 4 + self.T * 4 + self.T * 4 * 16 * 8
         self.select_bytes = self.merge_bytes = 0
         self.kbytes = 0
         self.launches_per_step = 1
