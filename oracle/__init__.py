@@ -66,6 +66,9 @@ def _load():
     lib.icp_orc_publish_tagged.argtypes = [P, i32, i32, P, P, P, i32, i32, i32, i32, i32, i32, i32,
                                            i32, i32]
     lib.icp_orc_merge_tagged.argtypes = [P, P, P, i32, i32, i32, i32, i32, i32, i32, P, P]
+    lib.icp_orc_score_chunks.argtypes = [P, P, i64, P, i64, P, P, i32, i32, i32, i32, i32, P, P]
+    lib.icp_orc_carrier.argtypes = [P, i32, i32, P, i32, i32, i32, i32, i32, i32, P]
+    lib.icp_orc_merge_carrier.argtypes = [P, P, i32, i32, i32, i32, i32, P, P]
     _lib = lib
     return lib
 
@@ -282,3 +285,68 @@ def sharded_merge_equals_unsharded(index_q, index_k_full, block_table, seq_lens,
     assert np.array_equal(out_s.view(np.int32), ref_s.view(np.int32)), \
         "merged scores differ from the unsharded Top16"
     return out_s, out_i, ref_s, ref_i
+
+
+CARRIER_WORDS = 32
+
+
+def score_chunks(index_q, index_k, block_table, seq_lens, qo_indptr, *, cols, rank, world_size,
+                 page_size, fill=np.nan):
+    """Exact score plane of a prefill window (float64 [T, 4, cols]) and its
+    |q.k| scale plane.  Request b's tokens are rows qo_indptr[b] ..
+    qo_indptr[b+1] - 1, the newest positions of its seq_len (the decode plane
+    with a per-request query length; see icp_orc_score_chunks)."""
+    lib = _load()
+    q = _c(index_q, np.uint8)
+    k = _c(index_k, np.uint8)
+    bt = _c(block_table, np.int32)
+    sl = _c(seq_lens, np.int32)
+    qo = _c(qo_indptr, np.int32)
+    B = sl.shape[0]
+    assert qo.shape == (B + 1,)
+    T = int(qo[-1])
+    assert q.shape[0] >= T and q.shape[1:] == (HEADS, DIM), q.shape
+    assert k.ndim == 3 and k.shape[1] == page_size // world_size and k.shape[2] == DIM
+    plane = np.full((T, HEADS, cols), fill, dtype=np.float64)
+    absplane = np.full((T, HEADS, cols), fill, dtype=np.float64)
+    stride = bt.shape[1] if bt.ndim == 2 else 0
+    rc = lib.icp_orc_score_chunks(_ptr(q), _ptr(k), k.shape[0], _ptr(bt), stride, _ptr(sl),
+                                  _ptr(qo), B, cols, rank, world_size, page_size, _ptr(plane),
+                                  _ptr(absplane))
+    if rc != 0:
+        raise ValueError(f"icp_orc_score_chunks failed with {rc}")
+    return plane, absplane
+
+
+def carrier(scores, num_valid_pages, *, world_size, heads_per_rank, init_blocks, local_blocks,
+            index_scale=1, index_offset=0):
+    """One rank's carrier rows int32 [ws, T, hpr, 32] from its plane [T, ws*hpr, K]."""
+    lib = _load()
+    sc = _c(scores, np.float32)
+    nvp = _c(num_valid_pages, np.int32)
+    T, H, K = sc.shape
+    assert H == world_size * heads_per_rank
+    out = np.zeros((world_size, T, heads_per_rank, CARRIER_WORDS), np.int32)
+    rc = lib.icp_orc_carrier(_ptr(sc), T, K, _ptr(nvp), world_size, heads_per_rank, init_blocks,
+                             local_blocks, index_scale, index_offset, _ptr(out))
+    if rc != 0:
+        raise ValueError("icp_orc_carrier failed")
+    return out
+
+
+def merge_carrier(received, num_valid_pages, *, world_size, heads_per_rank, init_blocks,
+                  local_blocks):
+    """Owner merge of received carrier rows int32 [ws, T, hpr, 32] ->
+    (scores [T,hpr,16], ids [T,hpr,16])."""
+    lib = _load()
+    rc_ = _c(received, np.int32)
+    nvp = _c(num_valid_pages, np.int32)
+    ws, T, hpr, w = rc_.shape
+    assert ws == world_size and hpr == heads_per_rank and w == CARRIER_WORDS
+    out_s = np.empty((T, hpr, TOPK), np.float32)
+    out_i = np.empty((T, hpr, TOPK), np.int32)
+    rc = lib.icp_orc_merge_carrier(_ptr(rc_), _ptr(nvp), T, world_size, heads_per_rank,
+                                   init_blocks, local_blocks, _ptr(out_s), _ptr(out_i))
+    if rc != 0:
+        raise ValueError("icp_orc_merge_carrier failed")
+    return out_s, out_i

@@ -126,15 +126,101 @@ static void column_rows(int c, int rank, int world_size, int page_size,
 }
 
 /*
- * Score plane [SCORE].  For every request b, token j, head h and column
- * c < columns_written(seq_len_b):
+ * Score plane rows of one request [SCORE]: its ntok tokens are plane rows
+ * row0 .. row0 + ntok - 1 (index_q rows likewise), token j at position
+ * seq_len - ntok + j.  For every such token, head h and column
+ * c < columns_written(seq_len):
  *   plane[t][h][c]    = max over visible keys of sum_i deq(q[t,h,i]) deq(k[key,i])
  *                       (exact), or -inf when no key of the column is visible;
  *   absplane[t][h][c] = max over the same keys of sum_i |deq(q) deq(k)|
  *                       (0 when none), the scale of the rounding tolerance.
- * Columns c >= columns_written(seq_len_b) are left untouched.
- * Returns 0; -1 on a bad argument; -2 on a NaN input code; -3 on a page id
- * outside [0, num_pages); -4 if a request needs more than `cols` columns.
+ * Columns c >= columns_written(seq_len) are left untouched.  qd holds room
+ * for ntok * 4 * 128 doubles, kd for 128.  Returns 0, -2 on a NaN input
+ * code, -3 on a page id outside [0, num_pages), -4 if the request needs more
+ * than `cols` columns.
+ */
+static int score_request(const uint8_t *index_q, const uint8_t *index_k, int64_t num_pages,
+                         const int32_t *bt_row, int seq_len, int64_t row0, int ntok, int cols,
+                         int rank, int world_size, int page_size, double *qd, double *kd,
+                         double *plane, double *absplane)
+{
+    int rows_per_page = page_size / world_size;
+    int nkeys_cols = icp_orc_columns_with_keys(seq_len, page_size, world_size);
+    int nwritten = icp_orc_columns_written(seq_len, page_size, world_size);
+    if (nwritten > cols)
+        return -4;
+    /* dequantise this request's queries: rows t = row0 + j, heads 0..3 */
+    for (int j = 0; j < ntok; ++j)
+        for (int h = 0; h < ORC_HEADS; ++h)
+            for (int i = 0; i < ORC_DIM; ++i) {
+                int64_t t = row0 + j;
+                double v = icp_orc_e4m3(index_q[(t * ORC_HEADS + h) * ORC_DIM + i]);
+                if (isnan(v))
+                    return -2;
+                qd[((int64_t)j * ORC_HEADS + h) * ORC_DIM + i] = v;
+            }
+
+    /* start every written column at "no visible key" */
+    for (int j = 0; j < ntok; ++j)
+        for (int h = 0; h < ORC_HEADS; ++h)
+            for (int c = 0; c < nwritten; ++c) {
+                int64_t t = row0 + j;
+                int64_t o = (t * ORC_HEADS + h) * cols + c;
+                plane[o] = -INFINITY;
+                if (absplane)
+                    absplane[o] = 0.0;
+            }
+
+    for (int c = 0; c < nkeys_cols; ++c) {
+        int nrows, page_slot, row_in_page;
+        int64_t pos0;
+        int32_t page;
+        column_rows(c, rank, world_size, page_size, &nrows, &page_slot, &row_in_page, &pos0);
+        if (pos0 >= seq_len)
+            continue; /* this rank holds no key of the column below seq_len */
+        page = bt_row[page_slot];
+        if (page < 0 || page >= num_pages)
+            return -3;
+        for (int r = 0; r < nrows; ++r) {
+            int64_t pos = pos0 + r;
+            const uint8_t *krow =
+                index_k + ((int64_t)page * rows_per_page + row_in_page + r) * ORC_DIM;
+            if (pos >= seq_len)
+                break;
+            for (int i = 0; i < ORC_DIM; ++i) {
+                kd[i] = icp_orc_e4m3(krow[i]);
+                if (isnan(kd[i]))
+                    return -2;
+            }
+            for (int j = 0; j < ntok; ++j) {
+                int64_t p_t = (int64_t)seq_len - ntok + j; /* token position */
+                int64_t t = row0 + j;
+                if (pos > p_t)
+                    continue; /* key after the token: masked */
+                for (int h = 0; h < ORC_HEADS; ++h) {
+                    const double *qv = qd + ((int64_t)j * ORC_HEADS + h) * ORC_DIM;
+                    double dot = 0.0, adot = 0.0;
+                    int64_t o = (t * ORC_HEADS + h) * cols + c;
+                    for (int i = 0; i < ORC_DIM; ++i) {
+                        dot += qv[i] * kd[i];
+                        adot += fabs(qv[i] * kd[i]);
+                    }
+                    if (dot > plane[o])
+                        plane[o] = dot;
+                    if (absplane && adot > absplane[o])
+                        absplane[o] = adot;
+                }
+            }
+        }
+    }
+    return 0;
+}
+
+/*
+ * Score plane [SCORE] of a decode batch: request b's tokens are rows
+ * b * decode_query_len + j, at positions seq_len_b - decode_query_len + j
+ * (parameter index_q).  Returns 0; -1 on a bad argument; otherwise the
+ * first error of score_request.
  */
 int icp_orc_score(const uint8_t *index_q, const uint8_t *index_k, int64_t num_pages,
                   const int32_t *block_table, int64_t bt_stride, const int32_t *seq_lens,
@@ -142,7 +228,6 @@ int icp_orc_score(const uint8_t *index_q, const uint8_t *index_k, int64_t num_pa
                   int decode_query_len, double *plane, double *absplane)
 {
     int dql = decode_query_len;
-    int rows_per_page = 0;
     double *qd = NULL, *kd = NULL;
     int rc = 0;
 
@@ -152,7 +237,6 @@ int icp_orc_score(const uint8_t *index_q, const uint8_t *index_k, int64_t num_pa
         return -1;
     if (page_size % world_size != 0)
         return -1;
-    rows_per_page = page_size / world_size;
 
     qd = (double *)malloc(sizeof(double) * (size_t)dql * ORC_HEADS * ORC_DIM);
     kd = (double *)malloc(sizeof(double) * ORC_DIM);
@@ -161,86 +245,64 @@ int icp_orc_score(const uint8_t *index_q, const uint8_t *index_k, int64_t num_pa
         free(kd);
         return -1;
     }
+    for (int b = 0; b < batch && rc == 0; ++b)
+        rc = score_request(index_q, index_k, num_pages, block_table + (int64_t)b * bt_stride,
+                           seq_lens[b], (int64_t)b * dql, dql, cols, rank, world_size,
+                           page_size, qd, kd, plane, absplane);
+    free(qd);
+    free(kd);
+    return rc;
+}
 
+/*
+ * Score plane of a prefill window.  The pages name the prefill chain
+ * (prepare_msa_icp_indexer: prefill_window_plan, prefill_local,
+ * prefill_merge) but its own pages are missing; the reading here is the
+ * decode plane with a per-request query length.  Request b contributes the
+ * tokens qo_indptr[b] .. qo_indptr[b+1] - 1 of the window, the newest
+ * n_b = qo_indptr[b+1] - qo_indptr[b] positions of its seq_len_b (so token
+ * j sits at seq_len_b - n_b + j, exactly as a decode query of length n_b),
+ * and each gets the request's columns_written(seq_len_b) columns.
+ * Returns 0; -1 on a bad argument (qo_indptr not starting at 0 or
+ * decreasing, or a chunk longer than its seq_len); otherwise the first
+ * error of score_request.
+ */
+int icp_orc_score_chunks(const uint8_t *index_q, const uint8_t *index_k, int64_t num_pages,
+                         const int32_t *block_table, int64_t bt_stride, const int32_t *seq_lens,
+                         const int32_t *qo_indptr, int batch, int cols, int rank,
+                         int world_size, int page_size, double *plane, double *absplane)
+{
+    int maxn = 1;
+    double *qd = NULL, *kd = NULL;
+    int rc = 0;
+
+    if (batch < 0 || cols <= 0 || world_size < 1 || rank < 0 || rank >= world_size)
+        return -1;
+    if ((page_size != 128 && page_size != 256) || page_size % world_size != 0)
+        return -1;
+    if (qo_indptr[0] != 0)
+        return -1;
+    for (int b = 0; b < batch; ++b) {
+        int n = qo_indptr[b + 1] - qo_indptr[b];
+        if (n < 0 || n > seq_lens[b])
+            return -1;
+        if (n > maxn)
+            maxn = n;
+    }
+    qd = (double *)malloc(sizeof(double) * (size_t)maxn * ORC_HEADS * ORC_DIM);
+    kd = (double *)malloc(sizeof(double) * ORC_DIM);
+    if (!qd || !kd) {
+        free(qd);
+        free(kd);
+        return -1;
+    }
     for (int b = 0; b < batch && rc == 0; ++b) {
-        int seq_len = seq_lens[b];
-        int nkeys_cols = icp_orc_columns_with_keys(seq_len, page_size, world_size);
-        int nwritten = icp_orc_columns_written(seq_len, page_size, world_size);
-        if (nwritten > cols) {
-            rc = -4;
-            break;
-        }
-        /* dequantise this request's queries: rows t = b*dql + j, heads 0..3 */
-        for (int j = 0; j < dql; ++j)
-            for (int h = 0; h < ORC_HEADS; ++h)
-                for (int i = 0; i < ORC_DIM; ++i) {
-                    int64_t t = (int64_t)b * dql + j;
-                    double v = icp_orc_e4m3(index_q[(t * ORC_HEADS + h) * ORC_DIM + i]);
-                    if (isnan(v)) {
-                        rc = -2;
-                    }
-                    qd[((int64_t)j * ORC_HEADS + h) * ORC_DIM + i] = v;
-                }
-        if (rc)
-            break;
-
-        /* start every written column at "no visible key" */
-        for (int j = 0; j < dql; ++j)
-            for (int h = 0; h < ORC_HEADS; ++h)
-                for (int c = 0; c < nwritten; ++c) {
-                    int64_t t = (int64_t)b * dql + j;
-                    int64_t o = (t * ORC_HEADS + h) * cols + c;
-                    plane[o] = -INFINITY;
-                    if (absplane)
-                        absplane[o] = 0.0;
-                }
-
-        for (int c = 0; c < nkeys_cols && rc == 0; ++c) {
-            int nrows, page_slot, row0;
-            int64_t pos0;
-            int32_t page;
-            column_rows(c, rank, world_size, page_size, &nrows, &page_slot, &row0, &pos0);
-            if (pos0 >= seq_len)
-                continue; /* this rank holds no key of the column below seq_len */
-            page = block_table[(int64_t)b * bt_stride + page_slot];
-            if (page < 0 || page >= num_pages) {
-                rc = -3;
-                break;
-            }
-            for (int r = 0; r < nrows; ++r) {
-                int64_t pos = pos0 + r;
-                const uint8_t *krow =
-                    index_k + ((int64_t)page * rows_per_page + row0 + r) * ORC_DIM;
-                if (pos >= seq_len)
-                    break;
-                for (int i = 0; i < ORC_DIM; ++i) {
-                    kd[i] = icp_orc_e4m3(krow[i]);
-                    if (isnan(kd[i]))
-                        rc = -2;
-                }
-                if (rc)
-                    break;
-                for (int j = 0; j < dql; ++j) {
-                    int64_t p_t = (int64_t)seq_len - dql + j; /* token position */
-                    int64_t t = (int64_t)b * dql + j;
-                    if (pos > p_t)
-                        continue; /* key after the token: masked */
-                    for (int h = 0; h < ORC_HEADS; ++h) {
-                        const double *qv = qd + ((int64_t)j * ORC_HEADS + h) * ORC_DIM;
-                        double dot = 0.0, adot = 0.0;
-                        int64_t o = (t * ORC_HEADS + h) * cols + c;
-                        for (int i = 0; i < ORC_DIM; ++i) {
-                            dot += qv[i] * kd[i];
-                            adot += fabs(qv[i] * kd[i]);
-                        }
-                        if (dot > plane[o])
-                            plane[o] = dot;
-                        if (absplane && adot > absplane[o])
-                            absplane[o] = adot;
-                    }
-                }
-            }
-        }
+        int n = qo_indptr[b + 1] - qo_indptr[b];
+        if (n == 0)
+            continue;
+        rc = score_request(index_q, index_k, num_pages, block_table + (int64_t)b * bt_stride,
+                           seq_lens[b], qo_indptr[b], n, cols, rank, world_size, page_size, qd,
+                           kd, plane, absplane);
     }
     free(qd);
     free(kd);
@@ -507,6 +569,109 @@ int icp_orc_merge(int32_t *recv, const int32_t *num_valid_pages, int T, int slot
                 return -1;
         }
     return missing;
+}
+
+/* ------------------------------------------------------------------------ */
+/* Prefill carrier rows                                                     */
+/* ------------------------------------------------------------------------ */
+/*
+ * prepare_msa_icp_indexer's prefill chain hands each rank's local Top16
+ * lists to a carrier that the caller exchanges once per layer, then merges
+ * what it received (prefill_merge(received, num_valid_pages, output)); the
+ * pages that define the carrier are missing.  The reading here: a carrier
+ * row is the legacy receive row without its ready flag (the caller's
+ * exchange orders it), 32 int32 words: the fp32 bits of the 16 scores, then
+ * the 16 ascending ids.  A rank's carrier is [ws][T][hpr][32], block o going
+ * to owner o, so row (t, h) sits at ((h / hpr) * T + t) * hpr + h % hpr.
+ * After the exchange an owner holds received [ws][T][hpr][32], block s from
+ * source rank s.
+ */
+#define ORC_CARRIER_WORDS 32
+
+/* Carrier of one rank: Top16 of every row of the plane [T, ws*hpr, K].
+ * Returns 0 or -1. */
+int icp_orc_carrier(const float *scores, int T, int K, const int32_t *num_valid_pages,
+                    int world_size, int heads_per_rank, int init_blocks, int local_blocks,
+                    int index_scale, int index_offset, int32_t *carrier)
+{
+    int heads = world_size * heads_per_rank;
+    float *sc = NULL;
+    int32_t *id = NULL;
+    if (T < 0 || world_size < 1 || heads_per_rank < 1)
+        return -1;
+    sc = (float *)malloc(sizeof(float) * ((size_t)T * heads * ORC_TOPK + 1));
+    id = (int32_t *)malloc(sizeof(int32_t) * ((size_t)T * heads * ORC_TOPK + 1));
+    if (!sc || !id) {
+        free(sc);
+        free(id);
+        return -1;
+    }
+    if (icp_orc_select(scores, T, heads, K, num_valid_pages, init_blocks, local_blocks,
+                       index_scale, index_offset, sc, id) != 0) {
+        free(sc);
+        free(id);
+        return -1;
+    }
+    for (int t = 0; t < T; ++t)
+        for (int h = 0; h < heads; ++h) {
+            int32_t *row = carrier + (((int64_t)(h / heads_per_rank) * T + t) * heads_per_rank +
+                                      h % heads_per_rank) *
+                                         ORC_CARRIER_WORDS;
+            const float *s = sc + ((int64_t)t * heads + h) * ORC_TOPK;
+            const int32_t *d = id + ((int64_t)t * heads + h) * ORC_TOPK;
+            for (int i = 0; i < ORC_TOPK; ++i) {
+                memcpy(&row[i], &s[i], sizeof(float));
+                row[ORC_TOPK + i] = d[i];
+            }
+        }
+    free(sc);
+    free(id);
+    return 0;
+}
+
+/* Owner merge of received carrier rows: for every token t and owned head
+ * hl, the union of the world_size source lists (id -1 is padding) with the
+ * maximum score per id, then Top16 with num_valid_pages[t], as the decode
+ * merge.  Output [T, hpr, 16].  Returns 0 or -1. */
+int icp_orc_merge_carrier(const int32_t *received, const int32_t *num_valid_pages, int T,
+                          int world_size, int heads_per_rank, int init_blocks, int local_blocks,
+                          float *out_scores, int32_t *out_ids)
+{
+    int32_t ids[4 * ORC_TOPK];
+    float sc[4 * ORC_TOPK];
+    if (T < 0 || world_size < 1 || world_size > 4 || heads_per_rank < 1)
+        return -1;
+    for (int t = 0; t < T; ++t)
+        for (int hl = 0; hl < heads_per_rank; ++hl) {
+            int n = 0;
+            int64_t o = ((int64_t)t * heads_per_rank + hl) * ORC_TOPK;
+            for (int s = 0; s < world_size; ++s) {
+                const int32_t *row =
+                    received + (((int64_t)s * T + t) * heads_per_rank + hl) * ORC_CARRIER_WORDS;
+                for (int i = 0; i < ORC_TOPK; ++i) {
+                    float v;
+                    int32_t d = row[ORC_TOPK + i];
+                    int found = -1;
+                    memcpy(&v, &row[i], sizeof(float));
+                    if (d == -1)
+                        continue;
+                    for (int e = 0; e < n; ++e)
+                        if (ids[e] == d)
+                            found = e;
+                    if (found < 0) {
+                        ids[n] = d;
+                        sc[n] = v;
+                        n++;
+                    } else if (v > sc[found]) {
+                        sc[found] = v;
+                    }
+                }
+            }
+            if (icp_orc_select_pairs(n, ids, sc, num_valid_pages[t], init_blocks, local_blocks,
+                                     out_scores + o, out_ids + o) < 0)
+                return -1;
+        }
+    return 0;
 }
 
 /* ------------------------------------------------------------------------ */
