@@ -272,6 +272,91 @@ int icp_score_select_noalloc(const uint8_t *index_q, const uint8_t *index_k, int
                              int init_blocks, int local_blocks, float *out_scores,
                              int32_t *out_ids, int32_t *errors, void *stream);
 
+/*
+ * Prefill window (prepare_msa_icp_indexer: prefill_window_plan once per
+ * query window and step, prefill_local per query chunk, the caller's one
+ * exchange per layer, then prefill_merge(received, num_valid_pages,
+ * output)).  The pages that define these calls are missing; the reading
+ * taken:
+ *   - a window holds, for every request b, a chunk of its newest
+ *     n_b = qo_indptr[b+1] - qo_indptr[b] tokens: window tokens
+ *     qo_indptr[b] .. qo_indptr[b+1] - 1, token j at position
+ *     seq_len_b - n_b + j (the decode placement of msa_icp_decode_index_
+ *     score_sharded's index_q with a per-request query length);
+ *   - the window's score plane is the decode plane of those queries: every
+ *     token gets its request's columns (icp_score_columns of seq_len_b),
+ *     -inf where no key at or before its position exists;
+ *   - local Top16 lists go into carrier rows: the legacy receive row
+ *     without its ready flag, 32 int32 words (fp32 bits of the 16 scores,
+ *     then the 16 ascending ids), a rank's carrier int32
+ *     [world_size][T][heads_per_rank][32] with block o bound for owner o
+ *     (row (t, h) at ((h / hpr) * T + t) * hpr + h % hpr);
+ *   - after the caller's exchange, an owner holds received
+ *     [world_size][T][heads_per_rank][32] (block s from rank s) and merges
+ *     it with the decode merge rule (union, maximum score per id, Top16 with
+ *     num_valid_pages[t]).
+ */
+
+/*
+ * int32 words of a prefill plan for a window of T tokens from `batch`
+ * requests: room for ceil(T / 8) + batch records of 8 ints plus an 8-int
+ * header.  Returns -1 when batch or T is negative or the records would
+ * exceed ICP_MAX_BATCH.  Host only.
+ */
+int64_t icp_prefill_plan_words(int batch, int T);
+
+/*
+ * prefill_window_plan: cuts every request's chunk into records of at most 8
+ * consecutive tokens (one kernel, no host synchronisation).
+ *   qo_indptr int32 [batch + 1], seq_lens int32 [batch] (each request's
+ *   length after the window's tokens), both device memory.
+ *   plan      int32 [plan_words] device memory, written whole by the call;
+ *             plan_words >= icp_prefill_plan_words(batch, T).
+ *   errors    int32 [>= 1] or NULL: a request whose chunk is invalid (a
+ *             decreasing qo_indptr, outside [0, T], or longer than its
+ *             seq_len) gets no records and adds 1; its tokens' plane rows
+ *             are then not written.
+ */
+int icp_prefill_plan(const int32_t *qo_indptr, const int32_t *seq_lens, int batch, int T,
+                     int32_t *plan, int64_t plan_words, int32_t *errors, void *stream);
+
+/*
+ * prefill_local, scoring half: the window's score plane float32
+ * [T, 4, cols] (unit last stride) from index_q uint8 [T, 4, 128] (the
+ * window's tokens, 16-byte aligned) against the rank's index-K shard, as
+ * icp_score does for decode (same index_k, block_table, cols, rank,
+ * world_size and page_size rules).  `plan` is icp_prefill_plan's output for
+ * this window.  Columns a token's request does not reach are left
+ * untouched; errors (or NULL) counts a plane narrower than a request needs
+ * and bounded waits that ran out.
+ */
+int icp_prefill_score(const uint8_t *index_q, const uint8_t *index_k, int64_t num_pages,
+                      const int32_t *block_table, int64_t block_table_stride,
+                      const int32_t *plan, int64_t plan_words, float *score_out, int T,
+                      int cols, int rank, int world_size, int page_size, int32_t *errors,
+                      void *stream);
+
+/*
+ * prefill_local, list half: the Top16 of every row of the plane float32
+ * [T, world_size * heads_per_rank, K] (the icp_top16_select rule, with
+ * num_valid_pages int32 [T]) into this rank's carrier int32
+ * [world_size][T][heads_per_rank][32].  Every row is written.  Limits as
+ * icp_top16_select; world_size 1, 2 or 4 and world_size * heads_per_rank = 4.
+ */
+int icp_prefill_select(const float *scores, int T, int K, const int32_t *num_valid_pages,
+                       int world_size, int heads_per_rank, int init_blocks, int local_blocks,
+                       int index_scale, int index_offset, int32_t *carrier, void *stream);
+
+/*
+ * prefill_merge: an owner's Top16 per (token, owned head) from the received
+ * carrier rows int32 [world_size][T][heads_per_rank][32] (all present: the
+ * caller's exchange has completed), out_scores float32 / out_ids int32
+ * [T, heads_per_rank, 16], ids ascending, (-1, -inf) padding.
+ */
+int icp_prefill_merge(const int32_t *received, const int32_t *num_valid_pages, int T,
+                      int world_size, int heads_per_rank, int init_blocks, int local_blocks,
+                      float *out_scores, int32_t *out_ids, void *stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -416,4 +416,124 @@ int icp_score_select(const uint8_t *index_q, const uint8_t *index_k, int64_t num
       icp::launch_score_select(tmk, tmq, a, sms, static_cast<cudaStream_t>(stream)));
 }
 
+int64_t icp_prefill_plan_words(int batch, int T) {
+  if (batch < 0 || T < 0) return -1;
+  const long long records = ((long long)T + icp::kPlanTokens - 1) / icp::kPlanTokens + batch;
+  if (records > icp::kMaxBatchDevice) return -1;
+  return icp::kPlanHeaderInts + (int64_t)icp::kPlanRecordInts * (records > 0 ? records : 1);
+}
+
+int icp_prefill_plan(const int32_t *qo_indptr, const int32_t *seq_lens, int batch, int T,
+                     int32_t *plan, int64_t plan_words, int32_t *errors, void *stream) {
+  const int64_t need = icp_prefill_plan_words(batch, T);
+  if (need < 0 || plan_words < need || !plan) return ICP_ERR_INVALID_ARG;
+  if (batch > 0 && (!qo_indptr || !seq_lens)) return ICP_ERR_INVALID_ARG;
+  int dev = 0, sms = 0;
+  int st = current_device(&dev, &sms);
+  if (st != ICP_OK) return st;
+  const int capacity = (int)((plan_words - icp::kPlanHeaderInts) / icp::kPlanRecordInts);
+  const int cap = capacity < icp::kMaxBatchDevice ? capacity : icp::kMaxBatchDevice;
+  return to_status(icp::launch_prefill_plan(qo_indptr, seq_lens, batch, T, plan, cap, errors,
+                                            static_cast<cudaStream_t>(stream)));
+}
+
+int icp_prefill_score(const uint8_t *index_q, const uint8_t *index_k, int64_t num_pages,
+                      const int32_t *block_table, int64_t block_table_stride,
+                      const int32_t *plan, int64_t plan_words, float *score_out, int T,
+                      int cols, int rank, int world_size, int page_size, int32_t *errors,
+                      void *stream) {
+  if (T < 0 || plan_words < icp::kPlanHeaderInts + icp::kPlanRecordInts)
+    return ICP_ERR_INVALID_ARG;
+  const int64_t records = (plan_words - icp::kPlanHeaderInts) / icp::kPlanRecordInts;
+  const int capacity = (int)(records < icp::kMaxBatchDevice ? records : icp::kMaxBatchDevice);
+  // the decode checks with the plan's records as requests of up to 8 tokens
+  int st = check_score_args(index_q, index_k, num_pages, block_table, block_table_stride, plan,
+                            T > 0 ? capacity : 0, cols, rank, world_size, page_size,
+                            icp::kPlanTokens, icp::kPlanTokens);
+  if (st != ICP_OK) return st;
+  if (T == 0) return ICP_OK;
+  if (!score_out) return ICP_ERR_INVALID_ARG;
+  int dev = 0, sms = 0;
+  st = current_device(&dev, &sms);
+  if (st != ICP_OK) return st;
+
+  icp::ScoreArgs a;
+  memset(&a, 0, sizeof(a));
+  a.block_table = block_table;
+  a.bt_stride = block_table_stride;
+  a.score_out = score_out;
+  a.errors = errors;
+  a.batch = capacity;
+  a.cols = cols;
+  a.rank = rank;
+  a.world_size = world_size;
+  a.page_size = page_size;
+  a.dql = icp::kPlanTokens;
+  a.g = make_geom(page_size, world_size, icp::kPlanTokens);
+  a.vreq = plan;
+  a.vcount = plan;
+
+  CUtensorMap tmk, tmq;
+  st = encode_rows(&tmk, index_k, (uint64_t)num_pages * a.g.rows_per_page, (uint32_t)a.g.R);
+  if (st != ICP_OK) return st;
+  st = encode_rows(&tmq, index_q, (uint64_t)T * ICP_HEADS, (uint32_t)a.g.nq);
+  if (st != ICP_OK) return st;
+  return to_status(icp::launch_score(tmk, tmq, a, sms, static_cast<cudaStream_t>(stream)));
+}
+
+int icp_prefill_select(const float *scores, int T, int K, const int32_t *num_valid_pages,
+                       int world_size, int heads_per_rank, int init_blocks, int local_blocks,
+                       int index_scale, int index_offset, int32_t *carrier, void *stream) {
+  if (!valid_select_common(T, K, init_blocks, local_blocks, index_scale, index_offset))
+    return ICP_ERR_INVALID_ARG;
+  if (world_size != 1 && world_size != 2 && world_size != 4) return ICP_ERR_INVALID_ARG;
+  if (heads_per_rank * world_size != ICP_HEADS) return ICP_ERR_INVALID_ARG;
+  if (T == 0) return ICP_OK;
+  if (!scores || !num_valid_pages || !carrier) return ICP_ERR_INVALID_ARG;
+  int dev = 0, sms = 0;
+  int st = current_device(&dev, &sms);
+  if (st != ICP_OK) return st;
+  icp::SelectArgs a;
+  memset(&a, 0, sizeof(a));
+  a.scores = scores;
+  a.T = T;
+  a.K = K;
+  a.nvp = num_valid_pages;
+  a.init_blocks = init_blocks;
+  a.local_blocks = local_blocks;
+  a.index_scale = index_scale;
+  a.index_offset = index_offset;
+  a.world_size = world_size;
+  a.heads_per_rank = heads_per_rank;
+  a.carrier = carrier;
+  return to_status(icp::launch_select(a, 3, sms, static_cast<cudaStream_t>(stream)));
+}
+
+int icp_prefill_merge(const int32_t *received, const int32_t *num_valid_pages, int T,
+                      int world_size, int heads_per_rank, int init_blocks, int local_blocks,
+                      float *out_scores, int32_t *out_ids, void *stream) {
+  if (world_size != 1 && world_size != 2 && world_size != 4) return ICP_ERR_INVALID_ARG;
+  if (heads_per_rank * world_size != ICP_HEADS) return ICP_ERR_INVALID_ARG;
+  if (T < 0) return ICP_ERR_INVALID_ARG;
+  if (init_blocks < 0 || local_blocks < 0 || init_blocks + local_blocks > ICP_TOPK)
+    return ICP_ERR_INVALID_ARG;
+  if (T == 0) return ICP_OK;
+  if (!received || !num_valid_pages || !out_scores || !out_ids) return ICP_ERR_INVALID_ARG;
+  int dev = 0, sms = 0;
+  int st = current_device(&dev, &sms);
+  if (st != ICP_OK) return st;
+  icp::MergeArgs a;
+  memset(&a, 0, sizeof(a));
+  a.received = received;
+  a.nvp = num_valid_pages;
+  a.T = T;
+  a.world_size = world_size;
+  a.heads_per_rank = heads_per_rank;
+  a.init_blocks = init_blocks;
+  a.local_blocks = local_blocks;
+  a.out_scores = out_scores;
+  a.out_ids = out_ids;
+  return to_status(icp::launch_merge_carrier(a, static_cast<cudaStream_t>(stream)));
+}
+
 }  // extern "C"

@@ -38,7 +38,20 @@ struct ScoreArgs {
   int32_t *out_ids;
   int32_t *ws_counters;  // [batch] 16-byte records: where each request's lists are
   void *ws_records;      // partial Top16 lists
+  // prefill window: requests come from a plan of kPlanRecordInts-int records
+  // (see icp_prefill.cu) instead of seq_lens / dql; batch is then the plan's
+  // capacity and *vcount the records in use
+  const int32_t *vreq;
+  const int32_t *vcount;
 };
+
+// Prefill plan: word 0 = records in use; records from word kPlanHeaderInts,
+// kPlanRecordInts ints each: {first token, block-table row, seq_len seen by
+// the record's tokens (last position + 1), tokens (<= 8), the request's
+// seq_len, 0, 0, 0}.
+constexpr int kPlanHeaderInts = 8;
+constexpr int kPlanRecordInts = 8;
+constexpr int kPlanTokens = 8;  // tokens per record (4 * 8 = 32 staged query rows)
 
 struct SelectArgs {
   const float *scores;
@@ -54,6 +67,7 @@ struct SelectArgs {
   int slot, rank, world_size, heads_per_rank, capacity;
   long long spin_limit;
   int32_t *generations;  // tagged publish: [3][ws * hpr][capacity] counters
+  int32_t *carrier;      // prefill carrier rows [ws][T][hpr][32]
 };
 
 struct MergeArgs {
@@ -66,6 +80,7 @@ struct MergeArgs {
   int32_t *out_ids;
   const unsigned long long *recv64;  // tagged merge: this owner's tagged rows
   int32_t *expected;                 // tagged merge: [3][ws][hpr][capacity] counters
+  const int32_t *received;           // prefill merge: carrier rows [ws][T][hpr][32]
 };
 
 // Launchers (return a cudaError_t from the launch).
@@ -80,8 +95,16 @@ cudaError_t launch_score_select(const CUtensorMap &tmk, const CUtensorMap &tmq, 
                                 int grid, cudaStream_t stream);
 
 cudaError_t select_prepare();  // one-time per-device kernel attributes
-// mode: 0 plain output, 1 legacy receive rows, 2 tagged receive rows
+// mode: 0 plain output, 1 legacy receive rows, 2 tagged receive rows,
+// 3 prefill carrier rows
 cudaError_t launch_select(const SelectArgs &a, int mode, int sm_count, cudaStream_t stream);
 cudaError_t launch_merge(const MergeArgs &a, bool tagged, cudaStream_t stream);
+cudaError_t launch_merge_carrier(const MergeArgs &a, cudaStream_t stream);
+
+// Prefill plan of a window (one CTA): records for `batch` requests into plan
+// (room for `capacity` records); a request with a bad chunk adds 1 to errors.
+cudaError_t launch_prefill_plan(const int32_t *qo_indptr, const int32_t *seq_lens, int batch,
+                                int T, int32_t *plan, int capacity, int32_t *errors,
+                                cudaStream_t stream);
 
 }  // namespace icp

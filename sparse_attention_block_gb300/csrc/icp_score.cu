@@ -97,6 +97,36 @@ struct SegmentWalker {
 };
 
 __device__ __forceinline__ int page_slot_of(int c, int split) { return split ? (c >> 1) : c; }
+
+// What the kernel needs of request b: a decode request (token rows
+// b * dql .. + dql, its own block-table row and seq_len), or a record of a
+// prefill plan (up to 8 consecutive tokens of a request's chunk).
+struct ReqView {
+  int seq_len;   // positions seen by the tokens: the last one is seq_len - 1
+  int tok0;      // first token (index_q / plane rows tok0 * 4 ...)
+  int bt_row;    // block-table row
+  int ntok;      // tokens (queries of positions seq_len - ntok .. seq_len - 1)
+  int full_len;  // the request's seq_len: sets the columns written
+};
+
+// Requests of this call; a plan's count is clamped to the capacity that the
+// shared-memory prefix sums were sized for.
+__device__ __forceinline__ int req_count(const ScoreArgs &a) {
+  return a.vreq ? min(max(*a.vcount, 0), a.batch) : a.batch;
+}
+
+__device__ __forceinline__ int req_seq_len(const ScoreArgs &a, int b) {
+  return a.vreq ? a.vreq[kPlanHeaderInts + kPlanRecordInts * b + 2] : a.seq_lens[b];
+}
+
+__device__ __forceinline__ ReqView req_view(const ScoreArgs &a, int b) {
+  if (a.vreq) {
+    const int *r = a.vreq + kPlanHeaderInts + kPlanRecordInts * b;
+    return ReqView{r[2], r[0], r[1], r[3], r[4]};
+  }
+  const int sl = a.seq_lens[b];
+  return ReqView{sl, b * a.dql, b, a.dql, sl};
+}
 __device__ __forceinline__ int row_off_of(int c, int split) { return split ? (c & 1) * 128 : 0; }
 
 // Per-lane running Top16 of one query row over the columns a warp has seen.
@@ -137,8 +167,9 @@ __device__ __forceinline__ void lane_insert(LaneTop &s, unsigned long long *lk, 
 // (row = token j * 4 + head), columns 0..127 hold the tile's keys in order.
 // R keys feed one plane column, so the tile covers 128 / R columns.
 template <int R, bool FUSED>
-__device__ __forceinline__ void epilogue_tile(const ScoreArgs &a, uint32_t taddr, int lane, int b,
-                                              int tl, int nunits, int seq_len, uint32_t tempty,
+__device__ __forceinline__ void epilogue_tile(const ScoreArgs &a, uint32_t taddr, int lane,
+                                              int tok0, int ntok, int tl, int nunits,
+                                              int seq_len, uint32_t tempty,
                                               LaneTop &lt, unsigned long long *lk, int *lfid,
                                               float *lfsc) {
   constexpr int CPT = 128 / R;
@@ -152,9 +183,9 @@ __device__ __forceinline__ void epilogue_tile(const ScoreArgs &a, uint32_t taddr
   if (lane == 0) mbar_arrive(tempty);
 
   const ScoreGeom &g = a.g;
-  const long long pfirst = (long long)seq_len - a.dql;  // position of token 0
-  const long long p_lane = pfirst + (lane >> 2);        // position of this row's token
-  const bool row_ok = lane < 4 * a.dql;
+  const long long pfirst = (long long)seq_len - ntok;  // position of token 0
+  const long long p_lane = pfirst + (lane >> 2);       // position of this row's token
+  const bool row_ok = lane < 4 * ntok;
 #pragma unroll
   for (int cc = 0; cc < CPT; ++cc) {
     const int c = tl * CPT + cc;
@@ -176,7 +207,7 @@ __device__ __forceinline__ void epilogue_tile(const ScoreArgs &a, uint32_t taddr
     const float val = vc[0] + 0.0f;  // + 0 folds -0 onto +0
     if (row_ok && c < a.cols) {
       if constexpr (!FUSED) {
-        const long long prow = (long long)b * a.dql * 4 + lane;
+        const long long prow = (long long)tok0 * 4 + lane;
         a.score_out[prow * a.cols + c] = val;
       } else {
         const int id = c * a.index_scale + a.index_offset;
@@ -221,6 +252,7 @@ score_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CU
   volatile int *misc = reinterpret_cast<volatile int *>(gb + kOffMisc);
   int *prefix = reinterpret_cast<int *>(gb + PrefixOffset<FUSED>::value);
   int *partial = prefix + a.batch + 1;  // kThreads scratch ints
+  const int nbatch = req_count(a);      // <= a.batch
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
@@ -247,12 +279,12 @@ score_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CU
 
   // Tiles per request and their prefix sums (chunked block scan).
   {
-    const int nb = a.batch;
+    const int nb = nbatch;
     const int chunk = (nb + kThreads - 1) / kThreads;
     const int lo = threadIdx.x * chunk, hi = min(nb, lo + chunk);
     int sum = 0;
     for (int b = lo; b < hi; ++b) {
-      const int u = units_of(a.seq_lens[b], a.page_size, g.split);
+      const int u = units_of(req_seq_len(a, b), a.page_size, g.split);
       sum += (u + g.cpt - 1) / g.cpt;
     }
     // exclusive scan of the per-thread sums: shuffles inside each warp, then
@@ -271,7 +303,7 @@ score_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CU
     int run = base + incl - sum;
     for (int b = lo; b < hi; ++b) {
       prefix[b] = run;
-      const int u = units_of(a.seq_lens[b], a.page_size, g.split);
+      const int u = units_of(req_seq_len(a, b), a.page_size, g.split);
       run += (u + g.cpt - 1) / g.cpt;
     }
   }
@@ -279,7 +311,7 @@ score_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CU
   tc_fence_after();
   const uint32_t tmem_base = (uint32_t)misc[0];
 
-  const long long total = prefix[a.batch];
+  const long long total = prefix[nbatch];
   const int g0 = (int)(total * blockIdx.x / gridDim.x);
   const int g1 = (int)(total * (blockIdx.x + 1) / gridDim.x);
   volatile int *abort_flag = misc + 1;
@@ -293,7 +325,7 @@ score_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CU
     int qslot = 0;
     long long issued = 0;
     int last_qslot = -1;
-    SegmentWalker walk(prefix, a.batch, g0, g1);
+    SegmentWalker walk(prefix, nbatch, g0, g1);
     int b, t0, t1;
     bool ok = true;
     if (a.pdl) {
@@ -301,13 +333,13 @@ score_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CU
       // tiles of this CTA into L2, only from pages that end at or before
       // seq_len - dql (the preceding kernel may still append the newest
       // keys); every real load below is issued after the wait.
-      SegmentWalker pw(prefix, a.batch, g0, g1);
+      SegmentWalker pw(prefix, nbatch, g0, g1);
       int pb, p0, p1, budget = 2 * kStages;
       while (budget > 0 && pw.next(pb, p0, p1)) {
-        const int sl = a.seq_lens[pb];
-        const int nunits = units_of(sl, a.page_size, g.split);
-        const int32_t *btrow = a.block_table + (long long)pb * a.bt_stride;
-        const long long safe_end = (long long)sl - a.dql;
+        const ReqView rv = req_view(a, pb);
+        const int nunits = units_of(rv.seq_len, a.page_size, g.split);
+        const int32_t *btrow = a.block_table + (long long)rv.bt_row * a.bt_stride;
+        const long long safe_end = (long long)rv.seq_len - rv.ntok;
         for (int tl = p0; tl < p1 && budget > 0; ++tl, --budget) {
           const int c = tl * g.cpt + lane;
           if (lane < g.cpt && c < nunits) {
@@ -321,7 +353,8 @@ score_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CU
       pdl_wait();
     }
     while (ok && walk.next(b, t0, t1)) {
-      const int nunits = units_of(a.seq_lens[b], a.page_size, g.split);
+      const ReqView rv = req_view(a, b);
+      const int nunits = units_of(rv.seq_len, a.page_size, g.split);
       const uint32_t qph = qslot ? qph1 : qph0;
       if (lane == 0) ok = mbar_wait(bar_qempty(qslot), qph ^ 1u, abort_flag);
       ok = __shfl_sync(0xFFFFFFFFu, ok, 0) != 0;
@@ -329,7 +362,7 @@ score_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CU
       if (lane == 0) {
         mbar_arrive_expect_tx(bar_qfull(qslot), (uint32_t)kQBytes);
         for (int r = 0; r < 4; ++r)
-          tma_load_2d(sb + kOffQ + qslot * kQBytes + r * kQRows * 128, &tmq, 0, b * a.dql * 4,
+          tma_load_2d(sb + kOffQ + qslot * kQBytes + r * kQRows * 128, &tmq, 0, rv.tok0 * 4,
                       bar_qfull(qslot));
       }
       last_qslot = qslot;
@@ -337,7 +370,7 @@ score_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CU
       qslot ^= 1;
       const int cbeg = t0 * g.cpt;
       const int cend = min(t1 * g.cpt, nunits);
-      const int32_t *btrow = a.block_table + (long long)b * a.bt_stride;
+      const int32_t *btrow = a.block_table + (long long)rv.bt_row * a.bt_stride;
       int grp = cbeg;
       int pg_cur = (cbeg + lane < cend) ? btrow[page_slot_of(cbeg + lane, g.split)] : 0;
       int pg_nxt = (cbeg + 32 + lane < cend) ? btrow[page_slot_of(cbeg + 32 + lane, g.split)] : 0;
@@ -390,7 +423,7 @@ score_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CU
     uint32_t sphase = 0, aphase = 0;
     uint32_t qph0 = 0, qph1 = 0;
     int qslot = 0;
-    SegmentWalker walk(prefix, a.batch, g0, g1);
+    SegmentWalker walk(prefix, nbatch, g0, g1);
     int b, t0, t1;
     bool ok = true;
     while (ok && walk.next(b, t0, t1)) {
@@ -442,17 +475,19 @@ score_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CU
     const int e = warp - 2;      // owns tiles i with i % 4 == e, accumulator e
     const int et = threadIdx.x - 64;
     if (a.pdl) pdl_wait();       // no global write before the preceding kernel is done
-    for (int b = blockIdx.x; b < a.batch; b += gridDim.x) {
-      const int u = units_of(a.seq_lens[b], a.page_size, g.split);
-      const int wcols = (u + 3) & ~3;
+    for (int b = blockIdx.x; b < nbatch; b += gridDim.x) {
+      const ReqView rv = req_view(a, b);
+      const int u = units_of(rv.seq_len, a.page_size, g.split);
+      const int wcols = (units_of(rv.full_len, a.page_size, g.split) + 3) & ~3;
       if (wcols > a.cols && et == 0 && a.errors) atomicAdd(a.errors, 1);  // plane too narrow
-      const int rows = 4 * a.dql;
+      const int rows = 4 * rv.ntok;
       if constexpr (!FUSED) {
-        // padding columns [units, round_up(units, 4)) of the requests this CTA owns
+        // columns [units, round_up(the request's units, 4)) of the rows this
+        // CTA owns: padding, or blocks past every one of the rows' tokens
         const int npad = min(wcols, a.cols) - min(u, a.cols);
         for (int k = et; k < npad * rows; k += 128) {
           const int r = k / npad, c = u + k % npad;
-          a.score_out[((long long)b * a.dql * 4 + r) * a.cols + c] = -INFINITY;
+          a.score_out[((long long)rv.tok0 * 4 + r) * a.cols + c] = -INFINITY;
         }
       } else if (et == 0) {
         // where the merge kernel finds this request's partial lists
@@ -482,12 +517,13 @@ score_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CU
       lfid = reinterpret_cast<int *>(wl + 16 * 32 * 8);
       lfsc = reinterpret_cast<float *>(wl + 16 * 32 * 8 + 16 * 32 * 4);
     }
-    SegmentWalker walk(prefix, a.batch, g0, g1);
+    SegmentWalker walk(prefix, nbatch, g0, g1);
     int b, t0, t1;
     bool ok = true;
     while (walk.next(b, t0, t1)) {
       if (!FUSED && !ok) break;
-      const int seq_len = a.seq_lens[b];
+      const ReqView rv = req_view(a, b);
+      const int seq_len = rv.seq_len;
       const int nunits = units_of(seq_len, a.page_size, g.split);
       LaneTop lt;
       lt.cnt = 0;
@@ -495,7 +531,7 @@ score_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CU
       lt.fcnt = 0;
       lt.nvp = 0;
       if constexpr (FUSED) {
-        if (lane < 4 * a.dql) lt.nvp = a.nvp[b * a.dql + (lane >> 2)];
+        if (lane < 4 * rv.ntok) lt.nvp = a.nvp[rv.tok0 + (lane >> 2)];
 #pragma unroll
         for (int j = 0; j < kTopK; ++j) lk[j * 32 + lane] = 0ull;
       }
@@ -509,13 +545,13 @@ score_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CU
         if (!ok) break;
         tc_fence_after();
         if (g.R == 128)
-          epilogue_tile<128, FUSED>(a, taddr, lane, b, tl, nunits, seq_len, bar_tempty(e), lt,
+          epilogue_tile<128, FUSED>(a, taddr, lane, rv.tok0, rv.ntok, tl, nunits, seq_len, bar_tempty(e), lt,
                                     lk, lfid, lfsc);
         else if (g.R == 64)
-          epilogue_tile<64, FUSED>(a, taddr, lane, b, tl, nunits, seq_len, bar_tempty(e), lt,
+          epilogue_tile<64, FUSED>(a, taddr, lane, rv.tok0, rv.ntok, tl, nunits, seq_len, bar_tempty(e), lt,
                                    lk, lfid, lfsc);
         else
-          epilogue_tile<32, FUSED>(a, taddr, lane, b, tl, nunits, seq_len, bar_tempty(e), lt,
+          epilogue_tile<32, FUSED>(a, taddr, lane, rv.tok0, rv.ntok, tl, nunits, seq_len, bar_tempty(e), lt,
                                    lk, lfid, lfsc);
         aphase ^= 1u;
       }
@@ -523,7 +559,7 @@ score_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CU
         // publish this warp's lists of the segment, then count the segment's
         // tiles; the CTA that completes the request merges it
         const int pidx = (blockIdx.x + b) * 4 + e;
-        if (lane < 4 * a.dql) {
+        if (lane < 4 * rv.ntok) {
           PartialRec *pr = partial_rec(a, pidx, lane);
           unsigned long long mxk = 0;
 #pragma unroll

@@ -34,10 +34,12 @@ __device__ __forceinline__ bool poll_flag(const int *flag, int want, long long s
 }
 
 // Where a selected row goes: the plain output arrays, a legacy receive row
-// (bounded wait for a free row, 32 data words, release-stored ready flag) or
-// a tagged receive row (32 int64 words of generation << 32 | word, the
-// generation taken from the publisher's counter for (slot, head, token)).
-enum EmitMode { kEmitPlain = 0, kEmitLegacy = 1, kEmitTagged = 2 };
+// (bounded wait for a free row, 32 data words, release-stored ready flag), a
+// tagged receive row (32 int64 words of generation << 32 | word, the
+// generation taken from the publisher's counter for (slot, head, token)), or
+// a prefill carrier row (the 32 data words, no flag: the caller's exchange
+// orders it), row ((h / hpr) * T + t) * hpr + h % hpr of the carrier.
+enum EmitMode { kEmitPlain = 0, kEmitLegacy = 1, kEmitTagged = 2, kEmitCarrier = 3 };
 
 // Address of the legacy receive row (t, h) of this publish.
 __device__ __forceinline__ int *legacy_row(const SelectArgs &a, int t, int h) {
@@ -64,6 +66,13 @@ __device__ __forceinline__ void emit_row(const SelectArgs &a, int lane, int row,
     if (lane < kTopK) {
       a.out_scores[(long long)row * kTopK + lane] = out_sc;
       a.out_ids[(long long)row * kTopK + lane] = out_id;
+    }
+  } else if constexpr (MODE == kEmitCarrier) {
+    const int hpr = a.heads_per_rank;
+    int *dst = a.carrier + (((long long)(h / hpr) * a.T + t) * hpr + h % hpr) * 32;
+    if (lane < kTopK) {
+      dst[lane] = __float_as_int(out_sc);
+      dst[kTopK + lane] = out_id;
     }
   } else {
     const int hpr = a.heads_per_rank;
@@ -776,8 +785,35 @@ __global__ void __launch_bounds__(128) merge_tagged_kernel(const MergeArgs a) {
   merge_finish(a, lane, t, hl, nvp, ids, scs, s_id[warp], s_sc[warp]);
 }
 
-}  // namespace
+// Owner merge of received prefill carrier rows [ws][T][hpr][32]: every
+// source row is there already (the caller's exchange has completed), so
+// there is nothing to wait for.
+__global__ void __launch_bounds__(128) merge_carrier_kernel(const MergeArgs a) {
+  __shared__ int s_id[4][kTopK];
+  __shared__ float s_sc[4][kTopK];
 
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int item = blockIdx.x * 4 + warp;
+  const int hpr = a.heads_per_rank;
+  if (item >= a.T * hpr) return;
+  const int t = item / hpr, hl = item % hpr;
+  const int nvp = a.nvp[t];
+  int ids[4];
+  float scs[4];
+#pragma unroll
+  for (int s = 0; s < 4; ++s) {
+    ids[s] = -1;
+    scs[s] = -INFINITY;
+    if (s < a.world_size && lane < kTopK) {
+      const int *row = a.received + (((long long)s * a.T + t) * hpr + hl) * 32;
+      scs[s] = __int_as_float(row[lane]);
+      ids[s] = row[kTopK + lane];
+    }
+  }
+  merge_finish(a, lane, t, hl, nvp, ids, scs, s_id[warp], s_sc[warp]);
+}
+
+}  // namespace
 
 cudaError_t select_prepare() { return cudaSuccess; }
 
@@ -788,7 +824,10 @@ cudaError_t launch_select(const SelectArgs &a, int mode, int sm_count, cudaStrea
   const bool vec = (a.K % 4 == 0) && ((reinterpret_cast<uintptr_t>(a.scores) & 15u) == 0);
   if (a.K > kWarpRowMaxK) {
     const int threads = 32 * kRowWarps;
-    if (mode == kEmitLegacy) {
+    if (mode == kEmitCarrier) {
+      if (vec) select_row_kernel<kRowWarps, kEmitCarrier, true><<<rows, threads, 0, stream>>>(a);
+      else select_row_kernel<kRowWarps, kEmitCarrier, false><<<rows, threads, 0, stream>>>(a);
+    } else if (mode == kEmitLegacy) {
       if (vec) select_row_kernel<kRowWarps, kEmitLegacy, true><<<rows, threads, 0, stream>>>(a);
       else select_row_kernel<kRowWarps, kEmitLegacy, false><<<rows, threads, 0, stream>>>(a);
     } else if (mode == kEmitTagged) {
@@ -802,7 +841,10 @@ cudaError_t launch_select(const SelectArgs &a, int mode, int sm_count, cudaStrea
   }
   const int grid = (rows + kSelWarps - 1) / kSelWarps;
   const int threads = 32 * kSelWarps;
-  if (mode == kEmitLegacy) {
+  if (mode == kEmitCarrier) {
+    if (vec) select_warp_kernel<kEmitCarrier, true><<<grid, threads, 0, stream>>>(a);
+    else select_warp_kernel<kEmitCarrier, false><<<grid, threads, 0, stream>>>(a);
+  } else if (mode == kEmitLegacy) {
     if (vec) select_warp_kernel<kEmitLegacy, true><<<grid, threads, 0, stream>>>(a);
     else select_warp_kernel<kEmitLegacy, false><<<grid, threads, 0, stream>>>(a);
   } else if (mode == kEmitTagged) {
@@ -812,6 +854,13 @@ cudaError_t launch_select(const SelectArgs &a, int mode, int sm_count, cudaStrea
     if (vec) select_warp_kernel<kEmitPlain, true><<<grid, threads, 0, stream>>>(a);
     else select_warp_kernel<kEmitPlain, false><<<grid, threads, 0, stream>>>(a);
   }
+  return cudaGetLastError();
+}
+
+cudaError_t launch_merge_carrier(const MergeArgs &a, cudaStream_t stream) {
+  const int items = a.T * a.heads_per_rank;
+  if (items == 0) return cudaSuccess;
+  merge_carrier_kernel<<<(items + 3) / 4, 128, 0, stream>>>(a);
   return cudaGetLastError();
 }
 

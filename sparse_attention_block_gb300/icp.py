@@ -59,6 +59,18 @@ lib.icp_merge_tagged.argtypes = [_P, _P, _P, _I32, _I32, _I32, _I32, _I32, _I32,
                                  _P, _P, _P, _P]
 lib.icp_merge.restype = _I32
 lib.icp_merge.argtypes = [_P, _P, _I32, _I32, _I32, _I32, _I32, _I32, _I32, _I64, _P, _P, _P, _P]
+lib.icp_prefill_plan_words.restype = _I64
+lib.icp_prefill_plan_words.argtypes = [_I32, _I32]
+lib.icp_prefill_plan.restype = _I32
+lib.icp_prefill_plan.argtypes = [_P, _P, _I32, _I32, _P, _I64, _P, _P]
+lib.icp_prefill_score.restype = _I32
+lib.icp_prefill_score.argtypes = [_P, _P, _I64, _P, _I64, _P, _I64, _P, _I32, _I32, _I32, _I32,
+                                  _I32, _P, _P]
+lib.icp_prefill_select.restype = _I32
+lib.icp_prefill_select.argtypes = [_P, _I32, _I32, _P, _I32, _I32, _I32, _I32, _I32, _I32, _P,
+                                   _P]
+lib.icp_prefill_merge.restype = _I32
+lib.icp_prefill_merge.argtypes = [_P, _P, _I32, _I32, _I32, _I32, _I32, _P, _P, _P]
 
 
 class IcpError(RuntimeError):
@@ -315,3 +327,84 @@ def icp_score_select_noalloc(index_q, index_k, block_table, seq_lens, num_valid_
                                         decode_query_len, max_decode_query_len, np_,
                                         init_blocks, local_blocks, osp, oip, ep,
                                         _stream(stream)), "icp_score_select_noalloc")
+
+
+# ------------------------------------------------------------------ prefill
+CARRIER_WORDS = 32
+
+
+def icp_prefill_plan_words(batch: int, T: int) -> int:
+    """int32 words of a prefill plan for a window of T tokens from batch requests."""
+    n = lib.icp_prefill_plan_words(int(batch), int(T))
+    if n < 0:
+        raise ValueError("invalid arguments for icp_prefill_plan_words (too many records?)")
+    return n
+
+
+def icp_prefill_plan(qo_indptr, seq_lens, plan, *, T: int, errors=None, stream=None):
+    """prefill_window_plan: records of up to 8 tokens of every request's chunk into plan."""
+    B = seq_lens.shape[0]
+    qp = _dev(qo_indptr, "qo_indptr", (torch.int32,), 1)
+    if qo_indptr.shape[0] != B + 1:
+        raise ValueError("qo_indptr must be [batch + 1]")
+    slp = _dev(seq_lens, "seq_lens", (torch.int32,), 1)
+    pp = _dev(plan, "plan", (torch.int32,), 1)
+    ep = 0 if errors is None else _dev(errors, "errors", (torch.int32,), 1)
+    _check(lib.icp_prefill_plan(qp, slp, B, int(T), pp, plan.numel(), ep, _stream(stream)),
+           "icp_prefill_plan")
+
+
+def icp_prefill_score(index_q, index_k, block_table, plan, score_out, *, rank: int,
+                      world_size: int, page_size: int, errors=None, stream=None):
+    """prefill_local, scoring half: the window's plane score_out [T, 4, cols]."""
+    T = index_q.shape[0]
+    qp = _dev(index_q, "index_q", _FP8, 3)
+    kp = _dev(index_k, "index_k", _FP8, 3)
+    if tuple(index_q.shape[1:]) != (HEADS, DIM):
+        raise ValueError("index_q must be [T, 4, 128]")
+    if tuple(index_k.shape[1:]) != (page_size // world_size, DIM):
+        raise ValueError(f"index_k must be [pages, {page_size // world_size}, 128]")
+    if block_table.dim() != 2 or block_table.stride(1) != 1:
+        raise ValueError("block_table must be 2-D with unit last stride")
+    btp = _dev(block_table, "block_table", (torch.int32,), 2, contiguous=False)
+    pp = _dev(plan, "plan", (torch.int32,), 1)
+    sop = _dev(score_out, "score_out", (torch.float32,), 3)
+    if score_out.shape[0] != T or score_out.shape[1] != HEADS:
+        raise ValueError(f"score_out must be [{T}, 4, cols]")
+    ep = 0 if errors is None else _dev(errors, "errors", (torch.int32,), 1)
+    _check(lib.icp_prefill_score(qp, kp, index_k.shape[0], btp, block_table.stride(0), pp,
+                                 plan.numel(), sop, T, score_out.shape[2], rank, world_size,
+                                 page_size, ep, _stream(stream)), "icp_prefill_score")
+
+
+def icp_prefill_select(scores, num_valid_pages, carrier, *, world_size: int,
+                       heads_per_rank: int, init_blocks: int, local_blocks: int,
+                       index_scale: int = 1, index_offset: int = 0, stream=None):
+    """prefill_local, list half: Top16 per row into carrier [ws, T, hpr, 32]."""
+    sp = _dev(scores, "scores", (torch.float32,), 3)
+    T, H, K = scores.shape
+    if H != world_size * heads_per_rank:
+        raise ValueError("scores must be [T, world_size * heads_per_rank, K]")
+    np_ = _dev(num_valid_pages, "num_valid_pages", (torch.int32,), 1)
+    cp = _dev(carrier, "carrier", (torch.int32,), 4)
+    if tuple(carrier.shape) != (world_size, T, heads_per_rank, CARRIER_WORDS):
+        raise ValueError("carrier must be [world_size, T, heads_per_rank, 32]")
+    _check(lib.icp_prefill_select(sp, T, K, np_, world_size, heads_per_rank, init_blocks,
+                                  local_blocks, index_scale, index_offset, cp, _stream(stream)),
+           "icp_prefill_select")
+
+
+def icp_prefill_merge(received, num_valid_pages, out_scores, out_ids, *, world_size: int,
+                      heads_per_rank: int, init_blocks: int, local_blocks: int, stream=None):
+    """prefill_merge: received carrier rows [ws, T, hpr, 32] -> out_* [T, hpr, 16]."""
+    rp = _dev(received, "received", (torch.int32,), 4)
+    ws, T, hpr, w = received.shape
+    if ws != world_size or hpr != heads_per_rank or w != CARRIER_WORDS:
+        raise ValueError("received must be [world_size, T, heads_per_rank, 32]")
+    np_ = _dev(num_valid_pages, "num_valid_pages", (torch.int32,), 1)
+    osp = _dev(out_scores, "out_scores", (torch.float32,), 3)
+    oip = _dev(out_ids, "out_ids", (torch.int32,), 3)
+    if tuple(out_scores.shape) != (T, hpr, TOPK) or tuple(out_ids.shape) != (T, hpr, TOPK):
+        raise ValueError("out_scores / out_ids must be [T, heads_per_rank, 16]")
+    _check(lib.icp_prefill_merge(rp, np_, T, world_size, heads_per_rank, init_blocks,
+                                 local_blocks, osp, oip, _stream(stream)), "icp_prefill_merge")
