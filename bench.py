@@ -94,6 +94,18 @@ def measured_peaks():
     return FALLBACK_HBM_GBS, "fallback"
 
 
+def measured_tensor_peak_fp8():
+    """Dense fp8 tensor peak: the measured bf16 burst figure times the
+    nominal fp8 / bf16 ratio (4.5 / 2.25 PFLOP/s)."""
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(p) as f:
+            d = json.load(f)
+        return 2.0 * float(d["bf16_tflops"]), "measured bf16 burst x 2 (nominal fp8/bf16)"
+    except Exception:
+        return 2.0 * 1900.0, "fallback 1.9 PFLOP/s bf16 x 2 (nominal fp8/bf16)"
+
+
 def kernel_digest():
     import hashlib
     h = hashlib.sha256()
@@ -389,6 +401,82 @@ class SelectBench:
             ev[1].record()
 
 
+class PrefillBench:
+    """One prefill window: plan, scorer over the plan's records, Top16 into
+    carrier rows, and the merge of the (single-rank) carrier."""
+    graph_period = 1
+
+    def __init__(self, spec, seed, device):
+        from sparse_attention_block_gb300 import icp
+        from sparse_attention_block_gb300 import workloads as W
+        self.icp = icp
+        self.spec = spec
+        inp = W.make_decode_inputs(spec, seed=seed, device=device)
+        self.q, self.k, self.bt, self.sl, self.nvp = (inp.index_q, inp.index_k,
+                                                      inp.block_table, inp.seq_lens,
+                                                      inp.num_valid_pages)
+        B, n = len(self.sl), spec.decode_query_len
+        self.T = B * n
+        self.qo = torch.arange(0, (B + 1) * n, n, dtype=torch.int32, device=device)
+        self.cols = W.columns_for(spec, int(self.sl.max()))
+        self.plan = torch.empty((icp.icp_prefill_plan_words(B, self.T),), dtype=torch.int32,
+                                device=device)
+        self.plane = torch.empty((self.T, 4, self.cols), dtype=torch.float32, device=device)
+        self.carrier = torch.empty((1, self.T, 4, 32), dtype=torch.int32, device=device)
+        self.out_s = torch.empty((self.T, 4, 16), dtype=torch.float32, device=device)
+        self.out_i = torch.empty((self.T, 4, 16), dtype=torch.int32, device=device)
+        self.errors = torch.zeros(1, dtype=torch.int32, device=device)
+        self.shards = [self.k]
+        sl = [int(x) for x in self.sl.tolist()]
+        self.score_bytes, self.select_bytes, self.merge_bytes, self.kbytes = \
+            prefill_bytes(sl, n, self.cols)
+        # useful MMA work: every (token, head) against every key at or
+        # before its position, 2 * 128 flops per key
+        self.flops = sum(4 * 256 * (sum(range(L - n + 1, L + 1))) for L in sl)
+        self.launches_per_step = 4
+        self.kernel_launches_per_step = 1
+
+    step_bytes = property(lambda self: self.score_bytes + self.select_bytes + self.merge_bytes)
+    rows = property(lambda self: self.T * 4)
+
+    def kernel_only(self):
+        self.icp.icp_prefill_score(self.q, self.k, self.bt, self.plan, self.plane, rank=0,
+                                   world_size=1, page_size=self.spec.page_size,
+                                   errors=self.errors)
+
+    def step(self, ev=None):
+        if ev is not None:
+            ev[0].record()
+        self.icp.icp_prefill_plan(self.qo, self.sl, self.plan, T=self.T, errors=self.errors)
+        self.kernel_only()
+        self.icp.icp_prefill_select(self.plane, self.nvp, self.carrier, world_size=1,
+                                    heads_per_rank=4, init_blocks=self.spec.init_blocks,
+                                    local_blocks=self.spec.local_blocks)
+        self.icp.icp_prefill_merge(self.carrier, self.nvp, self.out_s, self.out_i, world_size=1,
+                                   heads_per_rank=4, init_blocks=self.spec.init_blocks,
+                                   local_blocks=self.spec.local_blocks)
+        if ev is not None:
+            ev[1].record()
+
+
+def prefill_bytes(seq_lens, n, cols):
+    """Per window (unsharded): (scorer bytes, select bytes, merge bytes, index-K bytes).
+
+    Scorer: index-K rows needed once (sum seq_len * 128) + queries (T * 512) +
+    plane columns written (T * 16 * cols_b) + block table.  Select: the plane
+    read back + 128 B per carrier row.  Merge: 128 B per carrier row read +
+    128 B per output row written."""
+    T = len(seq_lens) * n
+    kbytes = sum(L * 128 for L in seq_lens)
+    cols_b = [((L + 127) // 128 + 3) // 4 * 4 for L in seq_lens]
+    plane = sum(16 * c * n for c in cols_b)
+    bt = sum(4 * ((L + 127) // 128) for L in seq_lens)
+    score = kbytes + T * 512 + plane + bt
+    select = plane + T * 4 * 128 + T * 4
+    merge = T * 4 * 128 + T * 4 * 128 + T * 4
+    return score, select, merge, kbytes
+
+
 # ------------------------------------------------------------ CPU baselines
 def oracle_sample(bench, budget_s):
     """Runs the oracle's chain (score, select+publish, merge) on the first
@@ -452,7 +540,52 @@ def oracle_select_sample(bench, budget_s):
     return spent, nbytes, rows, t
 
 
+def oracle_prefill_sample(bench, budget_s):
+    """The oracle's prefill chain (window plane, carrier, merge) on growing
+    leading parts of request 0's chunk until about budget_s seconds."""
+    import numpy as np
+    import oracle
+    spec = bench.spec
+    n = spec.decode_query_len
+    L = int(bench.sl[0].item())
+    q = bench.q[:n].cpu().numpy()
+    k = bench.k.cpu().numpy()
+    bt = bench.bt[:1].cpu().numpy()
+    nvp = bench.nvp[:n].cpu().numpy()
+    spent, nbytes, rows, m = 0.0, 0, 0, 0
+    step = 16
+    while m < n and (spent < budget_s or rows == 0):
+        # tokens m .. m + step - 1 of the chunk: a window of its own whose
+        # request length ends at the last of them
+        m1 = min(n, m + step)
+        Lm = L - n + m1
+        qo = np.array([0, m1 - m], np.int32)
+        t0 = time.perf_counter()
+        plane, _ = oracle.score_chunks(q[m:m1], k, bt, np.array([Lm], np.int32), qo,
+                                       cols=bench.cols, rank=0, world_size=1,
+                                       page_size=spec.page_size, fill=-np.inf)
+        car = oracle.carrier(plane.astype(np.float32), nvp[m:m1], world_size=1,
+                             heads_per_rank=4, init_blocks=spec.init_blocks,
+                             local_blocks=spec.local_blocks)
+        oracle.merge_carrier(car, nvp[m:m1], world_size=1, heads_per_rank=4,
+                             init_blocks=spec.init_blocks, local_blocks=spec.local_blocks)
+        spent += time.perf_counter() - t0
+        s, se, me, _ = prefill_bytes([Lm], m1 - m, bench.cols)
+        nbytes += s + se + me
+        rows += (m1 - m) * 4
+        m = m1
+    return spent, nbytes, rows, m
+
+
 def workload_config(name, bench):
+    if name == "prefill":
+        spec = bench.spec
+        return {"workload": spec.description, "batch": spec.batch, "T": bench.T,
+                "cols": bench.cols, "page_size": spec.page_size, "world_size": 1,
+                "chunk_tokens": spec.decode_query_len, "index_k_bytes_per_step": bench.kbytes,
+                "l2": "index-K cache smaller than L2 (re-read from L2 by every 32-token record)",
+                "step": "icp_prefill_plan -> icp_prefill_score -> icp_prefill_select -> "
+                        "icp_prefill_merge, replayed as a CUDA graph"}
     if name == "select":
         return {"workload": "standalone Top16 select: float32 plane [256, 4, 12284] N(0,1) "
                             "with 2% tied duplicates, num_valid_pages U[1, 12284], init 4, "
@@ -504,6 +637,8 @@ def run_reference(args, spec_name):
 def oracle_step(bench, name, budget):
     if name == "select":
         return oracle_select_sample(bench, budget)
+    if name == "prefill":
+        return oracle_prefill_sample(bench, budget)
     return oracle_sample(bench, budget)
 
 
@@ -513,6 +648,8 @@ def make_bench(name, seed, device, batch=0):
     from sparse_attention_block_gb300 import workloads as W
     if name == "select":
         return SelectBench(seed, device)
+    if name == "prefill":
+        return PrefillBench(W.PREFILL, seed, device)
     spec = W.DECODE_SPECS[name]
     if batch:
         spec = dataclasses.replace(spec, batch=batch, seq_lens=spec.seq_lens[:batch],
@@ -590,6 +727,21 @@ def run_ours(args, spec_name):
     if tr is not None:
         traffic = int(tr * bench.kbytes) if bench.kbytes else int(tr)
 
+    roofline = {"bound": "hbm", "kernel": kernel_name, "achieved": round(achieved, 1),
+                "peak": peak, "unit": "GB/s", "frac": round(achieved / peak, 4),
+                "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)"
+                if peak_kind == "measured" else "fallback 6.8 TB/s",
+                "traffic": traffic, "algorithmic_bytes_per_launch": kernel_bytes,
+                "kernel_digest": digest}
+    if spec_name == "prefill":
+        # many query rows against the same keys: a dense fp8 contraction
+        tpeak, tkind = measured_tensor_peak_fp8()
+        t_achieved = bench.flops / (kernel_ms / 1e3) / 1e12
+        roofline = {"bound": "tensor", "kernel": kernel_name, "achieved": round(t_achieved, 1),
+                    "peak": tpeak, "unit": "TFLOP/s", "frac": round(t_achieved / tpeak, 4),
+                    "peak_source": tkind, "traffic": None,
+                    "algorithmic_flops_per_launch": bench.flops,
+                    "hbm_achieved_gbs": round(achieved, 1), "kernel_digest": digest}
     line = {
         "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": n,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 5),
@@ -598,17 +750,12 @@ def run_ours(args, spec_name):
         "config": workload_config(spec_name, bench),
         "rows_per_s": round(rows_per_s, 1),
         "kernels": {kernel_name + "_ms": round(kernel_ms, 5)},
-        "roofline": {"bound": "hbm", "kernel": kernel_name, "achieved": round(achieved, 1),
-                     "peak": peak, "unit": "GB/s", "frac": round(achieved / peak, 4),
-                     "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)"
-                     if peak_kind == "measured" else "fallback 6.8 TB/s",
-                     "traffic": traffic, "algorithmic_bytes_per_launch": kernel_bytes,
-                     "kernel_digest": digest},
+        "roofline": roofline,
         "clocks": sampler.summary(),
         "gpu_launches": bench.launches_per_step * args.steps,
         "kernel_timing_launches": bench.kernel_launches_per_step * args.steps,
     }
-    if spec_name != "select":
+    if spec_name not in ("select", "prefill"):
         for _ in range(max(args.warmup, 3)):
             bench.fused_step()
         torch.cuda.synchronize()
@@ -646,6 +793,9 @@ def run_ours(args, spec_name):
         if spec_name == "select":
             s, b, r, nreq = oracle_select_sample(bench, budget)
             sample = f"first {nreq} token rows x 4 heads of the plane"
+        elif spec_name == "prefill":
+            s, b, r, nreq = oracle_prefill_sample(bench, budget)
+            sample = f"first {nreq} tokens of request 0's chunk, full chain"
         else:
             s, b, r, nreq = oracle_sample(bench, budget)
             sample = f"first {nreq} requests of the batch, full chain"
@@ -666,7 +816,8 @@ def main(argv=None):
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default="multitoken",
-                    choices=["tiny", "batched", "multitoken", "sharded", "longctx", "select"])
+                    choices=["tiny", "batched", "multitoken", "sharded", "longctx", "select",
+                             "prefill"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--batch", type=int, default=0,
                     help="use only the first B requests (smaller profiling cases)")

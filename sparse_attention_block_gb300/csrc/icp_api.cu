@@ -446,10 +446,10 @@ int icp_prefill_score(const uint8_t *index_q, const uint8_t *index_k, int64_t nu
     return ICP_ERR_INVALID_ARG;
   const int64_t records = (plan_words - icp::kPlanHeaderInts) / icp::kPlanRecordInts;
   const int capacity = (int)(records < icp::kMaxBatchDevice ? records : icp::kMaxBatchDevice);
-  // the decode checks with the plan's records as requests of up to 8 tokens
+  // the decode checks on layout, pointers and sizes (query length 1: the
+  // records carry their own)
   int st = check_score_args(index_q, index_k, num_pages, block_table, block_table_stride, plan,
-                            T > 0 ? capacity : 0, cols, rank, world_size, page_size,
-                            icp::kPlanTokens, icp::kPlanTokens);
+                            T > 0 ? capacity : 0, cols, rank, world_size, page_size, 1, 1);
   if (st != ICP_OK) return st;
   if (T == 0) return ICP_OK;
   if (!score_out) return ICP_ERR_INVALID_ARG;
@@ -472,11 +472,13 @@ int icp_prefill_score(const uint8_t *index_q, const uint8_t *index_k, int64_t nu
   a.g = make_geom(page_size, world_size, icp::kPlanTokens);
   a.vreq = plan;
   a.vcount = plan;
+  a.wide = 1;
 
   CUtensorMap tmk, tmq;
   st = encode_rows(&tmk, index_k, (uint64_t)num_pages * a.g.rows_per_page, (uint32_t)a.g.R);
   if (st != ICP_OK) return st;
-  st = encode_rows(&tmq, index_q, (uint64_t)T * ICP_HEADS, (uint32_t)a.g.nq);
+  // one box of a record's 4 * 32 query rows
+  st = encode_rows(&tmq, index_q, (uint64_t)T * ICP_HEADS, (uint32_t)(4 * icp::kPlanTokens));
   if (st != ICP_OK) return st;
   return to_status(icp::launch_score(tmk, tmq, a, sms, static_cast<cudaStream_t>(stream)));
 }

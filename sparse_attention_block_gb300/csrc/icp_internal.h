@@ -43,15 +43,16 @@ struct ScoreArgs {
   // capacity and *vcount the records in use
   const int32_t *vreq;
   const int32_t *vcount;
+  int wide;  // prefill scorer: 128 distinct query rows per request (records of <= 32 tokens)
 };
 
 // Prefill plan: word 0 = records in use; records from word kPlanHeaderInts,
 // kPlanRecordInts ints each: {first token, block-table row, seq_len seen by
-// the record's tokens (last position + 1), tokens (<= 8), the request's
+// the record's tokens (last position + 1), tokens (<= 32), the request's
 // seq_len, 0, 0, 0}.
 constexpr int kPlanHeaderInts = 8;
 constexpr int kPlanRecordInts = 8;
-constexpr int kPlanTokens = 8;  // tokens per record (4 * 8 = 32 staged query rows)
+constexpr int kPlanTokens = 32;  // tokens per record: 4 * 32 = 128 query rows, one MMA tile
 
 struct SelectArgs {
   const float *scores;

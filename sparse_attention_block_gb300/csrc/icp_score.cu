@@ -162,13 +162,15 @@ __device__ __forceinline__ void lane_insert(LaneTop &s, unsigned long long *lk, 
   }
 }
 
-// Epilogue of one tile for the warp that owns it.  taddr addresses the
-// warp's lane quarter of the tile's accumulator: lane l holds query row l
-// (row = token j * 4 + head), columns 0..127 hold the tile's keys in order.
-// R keys feed one plane column, so the tile covers 128 / R columns.
+// Epilogue of one tile for a warp.  taddr addresses the warp's lane quarter
+// of the tile's accumulator: lane l holds query row rowq + l of the request
+// (row = token j * 4 + head; rowq = 0 with the replicated queries, 32 times
+// the quarter with 128 distinct rows), columns 0..127 hold the tile's keys
+// in order.  R keys feed one plane column, so the tile covers 128 / R
+// columns.
 template <int R, bool FUSED>
 __device__ __forceinline__ void epilogue_tile(const ScoreArgs &a, uint32_t taddr, int lane,
-                                              int tok0, int ntok, int tl, int nunits,
+                                              int rowq, int tok0, int ntok, int tl, int nunits,
                                               int seq_len, uint32_t tempty,
                                               LaneTop &lt, unsigned long long *lk, int *lfid,
                                               float *lfsc) {
@@ -183,9 +185,10 @@ __device__ __forceinline__ void epilogue_tile(const ScoreArgs &a, uint32_t taddr
   if (lane == 0) mbar_arrive(tempty);
 
   const ScoreGeom &g = a.g;
+  const int row = rowq + lane;                         // the lane's query row
   const long long pfirst = (long long)seq_len - ntok;  // position of token 0
-  const long long p_lane = pfirst + (lane >> 2);       // position of this row's token
-  const bool row_ok = lane < 4 * ntok;
+  const long long p_lane = pfirst + (row >> 2);        // position of this row's token
+  const bool row_ok = row < 4 * ntok;
 #pragma unroll
   for (int cc = 0; cc < CPT; ++cc) {
     const int c = tl * CPT + cc;
@@ -207,7 +210,7 @@ __device__ __forceinline__ void epilogue_tile(const ScoreArgs &a, uint32_t taddr
     const float val = vc[0] + 0.0f;  // + 0 folds -0 onto +0
     if (row_ok && c < a.cols) {
       if constexpr (!FUSED) {
-        const long long prow = (long long)tok0 * 4 + lane;
+        const long long prow = (long long)tok0 * 4 + row;
         a.score_out[prow * a.cols + c] = val;
       } else {
         const int id = c * a.index_scale + a.index_offset;
@@ -227,7 +230,11 @@ __device__ __forceinline__ void epilogue_tile(const ScoreArgs &a, uint32_t taddr
   }
 }
 
-template <bool FUSED>
+// WIDE: the prefill scorer.  A request (a plan record of up to 32 tokens)
+// stages 128 distinct query rows in one box, and every tile goes to all four
+// epilogue warps, each finishing its lane quarter (8 of the tokens); the
+// accumulator is free again after four arrivals.
+template <bool FUSED, bool WIDE>
 __global__ void __launch_bounds__(kThreads, 1)
 score_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmq,
              const ScoreArgs a) {
@@ -261,7 +268,7 @@ score_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CU
     }
     for (int i = 0; i < kAcc; ++i) {
       mbar_init(bar_tfull(i), 1);
-      mbar_init(bar_tempty(i), 1);
+      mbar_init(bar_tempty(i), WIDE ? 4 : 1);
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(bar_qfull(i), 1);
@@ -361,9 +368,13 @@ score_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CU
       if (!ok) break;
       if (lane == 0) {
         mbar_arrive_expect_tx(bar_qfull(qslot), (uint32_t)kQBytes);
-        for (int r = 0; r < 4; ++r)
-          tma_load_2d(sb + kOffQ + qslot * kQBytes + r * kQRows * 128, &tmq, 0, rv.tok0 * 4,
-                      bar_qfull(qslot));
+        if constexpr (WIDE) {
+          tma_load_2d(sb + kOffQ + qslot * kQBytes, &tmq, 0, rv.tok0 * 4, bar_qfull(qslot));
+        } else {
+          for (int r = 0; r < 4; ++r)
+            tma_load_2d(sb + kOffQ + qslot * kQBytes + r * kQRows * 128, &tmq, 0, rv.tok0 * 4,
+                        bar_qfull(qslot));
+        }
       }
       last_qslot = qslot;
       if (qslot) qph1 ^= 1u; else qph0 ^= 1u;
@@ -507,6 +518,8 @@ score_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CU
     }
     uint32_t aphase = 0;
     int idx = 0;
+    int wacc = 0;        // WIDE: accumulator of the next tile, and its phase
+    uint32_t wph = 0;
     const uint32_t taddr = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)e * kAccCols;
     unsigned long long *lk = nullptr;
     int *lfid = nullptr;
@@ -535,25 +548,49 @@ score_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CU
 #pragma unroll
         for (int j = 0; j < kTopK; ++j) lk[j * 32 + lane] = 0ull;
       }
-      // first tile of this segment that belongs to this warp
-      int tl = t0 + ((e - idx) % 4 + 4) % 4;
-      const int seg_tiles = t1 - t0;
-      idx += seg_tiles;
-      for (; ok && tl < t1; tl += 4) {
-        if (lane == 0) ok = mbar_wait(bar_tfull(e), aphase, abort_flag);
-        ok = __shfl_sync(0xFFFFFFFFu, ok, 0) != 0;
-        if (!ok) break;
-        tc_fence_after();
-        if (g.R == 128)
-          epilogue_tile<128, FUSED>(a, taddr, lane, rv.tok0, rv.ntok, tl, nunits, seq_len, bar_tempty(e), lt,
-                                    lk, lfid, lfsc);
-        else if (g.R == 64)
-          epilogue_tile<64, FUSED>(a, taddr, lane, rv.tok0, rv.ntok, tl, nunits, seq_len, bar_tempty(e), lt,
-                                   lk, lfid, lfsc);
-        else
-          epilogue_tile<32, FUSED>(a, taddr, lane, rv.tok0, rv.ntok, tl, nunits, seq_len, bar_tempty(e), lt,
-                                   lk, lfid, lfsc);
-        aphase ^= 1u;
+      if constexpr (WIDE) {
+        // every tile, this warp's lane quarter (tokens 8 q .. 8 q + 7)
+        for (int tl = t0; ok && tl < t1; ++tl) {
+          if (lane == 0) ok = mbar_wait(bar_tfull(wacc), wph, abort_flag);
+          ok = __shfl_sync(0xFFFFFFFFu, ok, 0) != 0;
+          if (!ok) break;
+          tc_fence_after();
+          const uint32_t ta = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)wacc * kAccCols;
+          if (g.R == 128)
+            epilogue_tile<128, false>(a, ta, lane, q * 32, rv.tok0, rv.ntok, tl, nunits,
+                                      seq_len, bar_tempty(wacc), lt, lk, lfid, lfsc);
+          else if (g.R == 64)
+            epilogue_tile<64, false>(a, ta, lane, q * 32, rv.tok0, rv.ntok, tl, nunits,
+                                     seq_len, bar_tempty(wacc), lt, lk, lfid, lfsc);
+          else
+            epilogue_tile<32, false>(a, ta, lane, q * 32, rv.tok0, rv.ntok, tl, nunits,
+                                     seq_len, bar_tempty(wacc), lt, lk, lfid, lfsc);
+          if (++wacc == kAcc) {
+            wacc = 0;
+            wph ^= 1u;
+          }
+        }
+      } else {
+        // first tile of this segment that belongs to this warp
+        int tl = t0 + ((e - idx) % 4 + 4) % 4;
+        const int seg_tiles = t1 - t0;
+        idx += seg_tiles;
+        for (; ok && tl < t1; tl += 4) {
+          if (lane == 0) ok = mbar_wait(bar_tfull(e), aphase, abort_flag);
+          ok = __shfl_sync(0xFFFFFFFFu, ok, 0) != 0;
+          if (!ok) break;
+          tc_fence_after();
+          if (g.R == 128)
+            epilogue_tile<128, FUSED>(a, taddr, lane, 0, rv.tok0, rv.ntok, tl, nunits, seq_len,
+                                      bar_tempty(e), lt, lk, lfid, lfsc);
+          else if (g.R == 64)
+            epilogue_tile<64, FUSED>(a, taddr, lane, 0, rv.tok0, rv.ntok, tl, nunits, seq_len,
+                                     bar_tempty(e), lt, lk, lfid, lfsc);
+          else
+            epilogue_tile<32, FUSED>(a, taddr, lane, 0, rv.tok0, rv.ntok, tl, nunits, seq_len,
+                                     bar_tempty(e), lt, lk, lfid, lfsc);
+          aphase ^= 1u;
+        }
       }
       if constexpr (FUSED) {
         // publish this warp's lists of the segment, then count the segment's
@@ -589,6 +626,7 @@ score_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CU
 
 template <bool FUSED>
 size_t smem_bytes_for(int batch) {
+  static_assert(PrefixOffset<FUSED>::value % 16 == 0, "prefix alignment");
   return 1024 + PrefixOffset<FUSED>::value + sizeof(int) * (size_t)(batch + 1 + kThreads);
 }
 
@@ -599,18 +637,28 @@ size_t score_smem_bytes(int batch) { return smem_bytes_for<false>(batch); }
 
 cudaError_t score_prepare(int device) {
   (void)device;
-  cudaError_t e = cudaFuncSetAttribute(score_kernel<false>,
+  cudaError_t e = cudaFuncSetAttribute(score_kernel<false, false>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        (int)smem_bytes_for<false>(kMaxBatchDevice));
   if (e != cudaSuccess) return e;
-  return cudaFuncSetAttribute(score_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  e = cudaFuncSetAttribute(score_kernel<false, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           (int)smem_bytes_for<false>(kMaxBatchDevice));
+  if (e != cudaSuccess) return e;
+  return cudaFuncSetAttribute(score_kernel<true, false>,
+                              cudaFuncAttributeMaxDynamicSharedMemorySize,
                               (int)smem_bytes_for<true>(kMaxBatchDevice));
 }
 
 cudaError_t launch_score(const CUtensorMap &tmk, const CUtensorMap &tmq, const ScoreArgs &a,
                          int grid, cudaStream_t stream) {
+  if (a.wide) {
+    score_kernel<false, true><<<grid, kThreads, smem_bytes_for<false>(a.batch), stream>>>(
+        tmk, tmq, a);
+    return cudaGetLastError();
+  }
   if (!a.pdl) {
-    score_kernel<false><<<grid, kThreads, smem_bytes_for<false>(a.batch), stream>>>(tmk, tmq, a);
+    score_kernel<false, false><<<grid, kThreads, smem_bytes_for<false>(a.batch), stream>>>(
+        tmk, tmq, a);
     return cudaGetLastError();
   }
   cudaLaunchConfig_t cfg = {};
@@ -623,13 +671,14 @@ cudaError_t launch_score(const CUtensorMap &tmk, const CUtensorMap &tmq, const S
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, score_kernel<false>, tmk, tmq, a);
+  return cudaLaunchKernelEx(&cfg, score_kernel<false, false>, tmk, tmq, a);
 }
 
 cudaError_t launch_score_select(const CUtensorMap &tmk, const CUtensorMap &tmq, ScoreArgs a,
                                 int grid, cudaStream_t stream) {
   grid = grid > kFusedMaxGrid ? kFusedMaxGrid : grid;
-  score_kernel<true><<<grid, kThreads, smem_bytes_for<true>(a.batch), stream>>>(tmk, tmq, a);
+  score_kernel<true, false><<<grid, kThreads, smem_bytes_for<true>(a.batch), stream>>>(tmk, tmq,
+                                                                                       a);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   return launch_fused_merge(a, grid, stream);

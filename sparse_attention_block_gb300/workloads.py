@@ -95,6 +95,14 @@ LONGCTX = DecodeSpec(
 
 DECODE_SPECS = {s.name: s for s in (TINY, BATCHED, MULTITOKEN, SHARDED, LONGCTX)}
 
+# Prefill window: every request brings a chunk of decode_query_len new tokens
+# (its newest positions), drawn with the same recipe.
+PREFILL = DecodeSpec(
+    "prefill", batch=4, page_size=128, world_size=1, decode_query_len=2048,
+    max_decode_query_len=2048, init_blocks=1, local_blocks=4, seq_range=(4096, 32768),
+    description="prefill window: B=4 requests, chunks of 2048 new tokens (T=8192), "
+                "seq_len U[4096, 32768] after the chunk, P128, init 1, local 4")
+
 # standalone Top16 select on a [T=256, 4, K=12284] plane
 SELECT_T, SELECT_K, SELECT_INIT, SELECT_LOCAL, SELECT_DUP = 256, 12284, 4, 8, 0.02
 
