@@ -59,17 +59,40 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   return ok != 0;
 }
 
+// Same with a suspend-time hint: a thread whose phase is not complete may
+// sleep up to `ns` nanoseconds; it resumes as soon as the phase completes.
+__device__ __forceinline__ bool mbar_try_wait_sleep(uint32_t bar, uint32_t parity, uint32_t ns) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity), "r"(ns)
+      : "memory");
+  return ok != 0;
+}
+
+// A waiting thread sleeps in the barrier rather than polling, so that the
+// warps sharing its scheduler keep the issue slots.
+constexpr uint32_t kWaitSleepNs = 20000;
+
 // Waits for the phase with the given parity to complete.  Gives up (returns
 // false) when *abort becomes non-zero or after kWaitTimeoutNs; in the
 // latter case it sets *abort so that the other roles of the CTA stop too.
+// The global timer is first read after 64 sleeping retries (reading it can
+// stall the warp, and most waits end long before).
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int *abort) {
   if (mbar_try_wait(bar, parity)) return true;
-  const unsigned long long t0 = globaltimer_ns();
+  unsigned long long t0 = 0;
   for (uint32_t it = 1;; ++it) {
-    if (mbar_try_wait(bar, parity)) return true;
+    if (mbar_try_wait_sleep(bar, parity, kWaitSleepNs)) return true;
     if ((it & 63u) == 0u) {
       if (*abort) return false;
-      if (globaltimer_ns() - t0 > kWaitTimeoutNs) {
+      const unsigned long long now = globaltimer_ns();
+      if (t0 == 0) {
+        t0 = now;
+      } else if (now - t0 > kWaitTimeoutNs) {
         *abort = 1;
         return false;
       }

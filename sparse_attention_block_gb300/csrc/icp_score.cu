@@ -48,6 +48,13 @@ constexpr int kTileBytes = 128 * 128;  // 128 K rows x 128 fp8
 constexpr int kQRows = 32;             // query rows staged per request (4 * dql <= 32)
 constexpr int kQBytes = 4 * kQRows * 128;  // four copies -> the 128-row A operand
 constexpr int kThreads = 192;
+// prefill scorer: two sets of four epilogue warps take alternate tiles
+constexpr int kEpiSetsWide = 2;
+constexpr int kThreadsWide = 64 + 128 * kEpiSetsWide;
+template <bool WIDE>
+struct BlockThreads {
+  static constexpr int value = WIDE ? kThreadsWide : kThreads;
+};
 constexpr uint32_t kAccCols = 128;     // N = 128 keys per accumulator
 constexpr uint32_t kTmemCols = kAcc * kAccCols;
 constexpr int kNumBars = 2 * kStages + 2 * kAcc + 4 + 1;
@@ -230,12 +237,72 @@ __device__ __forceinline__ void epilogue_tile(const ScoreArgs &a, uint32_t taddr
   }
 }
 
+// Epilogue of one tile of the prefill scorer for one warp of the set that
+// owns it: lane l holds query row rowq + l of the record (128 distinct rows).
+// The accumulator is read 32 keys at a time, each chunk reduced while the
+// next one is loaded; a column that reaches past the record's first token is
+// masked per chunk with 32-bit compares.
+template <int R>
+__device__ __forceinline__ void epilogue_tile_wide(const ScoreArgs &a, uint32_t ta, int lane,
+                                                   int rowq, int tok0, int ntok, int tl,
+                                                   int nunits, int seq_len, uint32_t tempty) {
+  constexpr int CPT = 128 / R;  // plane columns in the tile
+  constexpr int KPC = R / 32;   // 32-key chunks per column
+  const ScoreGeom &g = a.g;
+  const int row = rowq + lane;
+  const long long pfirst = (long long)seq_len - ntok;  // position of token 0
+  const long long p_lane = pfirst + (row >> 2);        // position of this row's token
+  const bool row_ok = row < 4 * ntok;
+  float x0[32], x1[32];
+  float m = -INFINITY;
+  tmem_ld32(ta, x0);
+  tmem_wait_ld();
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    float *cur = (k & 1) ? x1 : x0;
+    float *nxt = (k & 1) ? x0 : x1;
+    if (k < 3) {
+      tmem_ld32(ta + 32u * (k + 1), nxt);
+    } else {
+      // all four chunks are in registers: hand the accumulator back
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(tempty);
+    }
+    const int c = tl * CPT + k / KPC;
+    const long long pos0 = g.split ? (long long)c * 128
+                                   : (long long)c * a.page_size +
+                                         (long long)a.rank * g.rows_per_page;
+    if (pos0 + R - 1 > pfirst) {
+      // keys j <= lim of this chunk are at or before the row's token
+      const long long d = p_lane - pos0 - 32 * (k % KPC);
+      const int lim = (int)(d < -1 ? -1 : (d > 31 ? 31 : d));
+#pragma unroll
+      for (int j = 0; j < 32; ++j)
+        if (j > lim) cur[j] = -INFINITY;
+    }
+#pragma unroll
+    for (int st = 16; st >= 1; st >>= 1) {
+#pragma unroll
+      for (int j = 0; j < st; ++j) cur[j] = fmaxf(cur[j], cur[j + st]);
+    }
+    m = fmaxf(m, cur[0]);
+    if (k % KPC == KPC - 1) {
+      if (c < nunits && c < a.cols && row_ok)
+        a.score_out[((long long)tok0 * 4 + row) * a.cols + c] = m + 0.0f;  // + 0 folds -0
+      m = -INFINITY;
+    }
+    if (k < 3) tmem_wait_ld();
+  }
+}
+
 // WIDE: the prefill scorer.  A request (a plan record of up to 32 tokens)
-// stages 128 distinct query rows in one box, and every tile goes to all four
-// epilogue warps, each finishing its lane quarter (8 of the tokens); the
-// accumulator is free again after four arrivals.
+// stages 128 distinct query rows in one box.  The epilogue warps form
+// kEpiSetsWide sets of four; tile i of the CTA goes to set i % kEpiSetsWide,
+// whose four warps each finish their lane quarter (8 of the tokens), and the
+// accumulator is free again after those four arrivals.
 template <bool FUSED, bool WIDE>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(BlockThreads<WIDE>::value, 1)
 score_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmq,
              const ScoreArgs a) {
   extern __shared__ uint8_t smem_raw[];
@@ -243,6 +310,7 @@ score_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CU
   const uint32_t sb = (raw + 1023u) & ~1023u;
   uint8_t *gb = smem_raw + (sb - raw);
 
+  constexpr int NT = BlockThreads<WIDE>::value;
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const ScoreGeom g = a.g;
@@ -258,7 +326,7 @@ score_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CU
   // [0] TMEM base, [1] abort flag
   volatile int *misc = reinterpret_cast<volatile int *>(gb + kOffMisc);
   int *prefix = reinterpret_cast<int *>(gb + PrefixOffset<FUSED>::value);
-  int *partial = prefix + a.batch + 1;  // kThreads scratch ints
+  int *partial = prefix + a.batch + 1;  // NT / 32 scratch ints
   const int nbatch = req_count(a);      // <= a.batch
 
   if (threadIdx.x == 0) {
@@ -287,7 +355,7 @@ score_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CU
   // Tiles per request and their prefix sums (chunked block scan).
   {
     const int nb = nbatch;
-    const int chunk = (nb + kThreads - 1) / kThreads;
+    const int chunk = (nb + NT - 1) / NT;
     const int lo = threadIdx.x * chunk, hi = min(nb, lo + chunk);
     int sum = 0;
     for (int b = lo; b < hi; ++b) {
@@ -295,7 +363,7 @@ score_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CU
       sum += (u + g.cpt - 1) / g.cpt;
     }
     // exclusive scan of the per-thread sums: shuffles inside each warp, then
-    // the warp totals (kThreads / 32 of them) in shared memory
+    // the warp totals (NT / 32 of them) in shared memory
     int incl = sum;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
@@ -306,7 +374,7 @@ score_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CU
     __syncthreads();
     int base = 0;
     for (int w = 0; w < warp; ++w) base += partial[w];
-    if (threadIdx.x == kThreads - 1) prefix[nb] = base + incl;
+    if (threadIdx.x == NT - 1) prefix[nb] = base + incl;
     int run = base + incl - sum;
     for (int b = lo; b < hi; ++b) {
       prefix[b] = run;
@@ -496,7 +564,7 @@ score_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CU
         // columns [units, round_up(the request's units, 4)) of the rows this
         // CTA owns: padding, or blocks past every one of the rows' tokens
         const int npad = min(wcols, a.cols) - min(u, a.cols);
-        for (int k = et; k < npad * rows; k += 128) {
+        for (int k = et; k < npad * rows; k += NT - 64) {
           const int r = k / npad, c = u + k % npad;
           a.score_out[((long long)rv.tok0 * 4 + r) * a.cols + c] = -INFINITY;
         }
@@ -518,8 +586,7 @@ score_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CU
     }
     uint32_t aphase = 0;
     int idx = 0;
-    int wacc = 0;        // WIDE: accumulator of the next tile, and its phase
-    uint32_t wph = 0;
+    int gi = 0;          // WIDE: the CTA's tile counter
     const uint32_t taddr = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)e * kAccCols;
     unsigned long long *lk = nullptr;
     int *lfid = nullptr;
@@ -549,26 +616,27 @@ score_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CU
         for (int j = 0; j < kTopK; ++j) lk[j * 32 + lane] = 0ull;
       }
       if constexpr (WIDE) {
-        // every tile, this warp's lane quarter (tokens 8 q .. 8 q + 7)
-        for (int tl = t0; ok && tl < t1; ++tl) {
+        // the tiles of this warp's set, this warp's lane quarter (tokens
+        // 8 q .. 8 q + 7); gi counts the CTA's tiles as the MMA warp does
+        const int set = (warp - 2) >> 2;
+        for (int tl = t0; ok && tl < t1; ++tl, ++gi) {
+          if (gi % kEpiSetsWide != set) continue;
+          const int wacc = gi % kAcc;
+          const uint32_t wph = (uint32_t)(gi / kAcc) & 1u;
           if (lane == 0) ok = mbar_wait(bar_tfull(wacc), wph, abort_flag);
           ok = __shfl_sync(0xFFFFFFFFu, ok, 0) != 0;
           if (!ok) break;
           tc_fence_after();
           const uint32_t ta = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)wacc * kAccCols;
           if (g.R == 128)
-            epilogue_tile<128, false>(a, ta, lane, q * 32, rv.tok0, rv.ntok, tl, nunits,
-                                      seq_len, bar_tempty(wacc), lt, lk, lfid, lfsc);
+            epilogue_tile_wide<128>(a, ta, lane, q * 32, rv.tok0, rv.ntok, tl, nunits, seq_len,
+                                    bar_tempty(wacc));
           else if (g.R == 64)
-            epilogue_tile<64, false>(a, ta, lane, q * 32, rv.tok0, rv.ntok, tl, nunits,
-                                     seq_len, bar_tempty(wacc), lt, lk, lfid, lfsc);
+            epilogue_tile_wide<64>(a, ta, lane, q * 32, rv.tok0, rv.ntok, tl, nunits, seq_len,
+                                   bar_tempty(wacc));
           else
-            epilogue_tile<32, false>(a, ta, lane, q * 32, rv.tok0, rv.ntok, tl, nunits,
-                                     seq_len, bar_tempty(wacc), lt, lk, lfid, lfsc);
-          if (++wacc == kAcc) {
-            wacc = 0;
-            wph ^= 1u;
-          }
+            epilogue_tile_wide<32>(a, ta, lane, q * 32, rv.tok0, rv.ntok, tl, nunits, seq_len,
+                                   bar_tempty(wacc));
         }
       } else {
         // first tile of this segment that belongs to this warp
@@ -627,7 +695,7 @@ score_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CU
 template <bool FUSED>
 size_t smem_bytes_for(int batch) {
   static_assert(PrefixOffset<FUSED>::value % 16 == 0, "prefix alignment");
-  return 1024 + PrefixOffset<FUSED>::value + sizeof(int) * (size_t)(batch + 1 + kThreads);
+  return 1024 + PrefixOffset<FUSED>::value + sizeof(int) * (size_t)(batch + 1 + kThreadsWide / 32);
 }
 
 }  // namespace
@@ -652,7 +720,7 @@ cudaError_t score_prepare(int device) {
 cudaError_t launch_score(const CUtensorMap &tmk, const CUtensorMap &tmq, const ScoreArgs &a,
                          int grid, cudaStream_t stream) {
   if (a.wide) {
-    score_kernel<false, true><<<grid, kThreads, smem_bytes_for<false>(a.batch), stream>>>(
+    score_kernel<false, true><<<grid, kThreadsWide, smem_bytes_for<false>(a.batch), stream>>>(
         tmk, tmq, a);
     return cudaGetLastError();
   }
