@@ -45,10 +45,10 @@ FALLBACK_HBM_GBS = 6800.0
 # streamed), measured for the kernel source with this digest.  When the
 # kernel changes the digest no longer matches and `traffic` is reported null.
 NCU_TRAFFIC = {
-    # dram__bytes_read.sum + dram__bytes_write.sum = 278818304 + 2935040 bytes for
+    # dram__bytes_read.sum + dram__bytes_write.sum = 278832384 + 3027968 bytes for
     # 278330624 bytes of index-K (first 32 requests of the multitoken workload),
     # see profiles/icp_score_multitoken.md
-    ("multitoken", "e452aa630b34ba90"): (278818304 + 2935040) / 278330624,
+    ("multitoken", "809ecc4d550565cc"): (278832384 + 3027968) / 278330624,
 }
 
 
