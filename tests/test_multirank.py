@@ -60,3 +60,48 @@ def test_workloads_differ_per_rank_seed():
     a = W.make_decode_inputs(W.TINY, seed=0)
     b = W.make_decode_inputs(W.TINY, seed=1)
     assert not torch.equal(a.index_k, b.index_k)
+
+
+def _prefill_exchange_worker(rank, world, port, out):
+    """One prefill window on a world_size-2 key shard: oracle plane and
+    carrier on this rank, the caller's one exchange per layer as an
+    equal-split all_to_all of the carrier, then this owner's merge."""
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port))
+    sys.path.insert(0, ROOT)
+    sys.path.insert(0, os.path.join(ROOT, "tests"))
+    import numpy as np
+    import oracle
+    from test_oracle_prefill import _window
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    seq_lens, chunks = [900, 2000, 300], [12, 33, 7]
+    inp, q, qo = _window(seq_lens, chunks, world_size=world, seed=31)
+    pos = np.concatenate([np.arange(L - n, L) for L, n in zip(seq_lens, chunks)])
+    nvp = ((pos + 1 + 127) // 128).astype(np.int32)
+    cols = oracle.columns_written(max(seq_lens), 128, 1)
+    rp, hpr = 128 // world, 4 // world
+    shard = inp.index_k.numpy()[:, rank * rp:(rank + 1) * rp].copy()
+    plane, _ = oracle.score_chunks(q, shard, inp.block_table.numpy(), inp.seq_lens.numpy(), qo,
+                                   cols=cols, rank=rank, world_size=world, page_size=128,
+                                   fill=-np.inf)
+    car = oracle.carrier(plane.astype(np.float32), nvp, world_size=world, heads_per_rank=hpr,
+                         init_blocks=1, local_blocks=3)
+    send = torch.from_numpy(car).contiguous()          # block o is bound for owner o
+    recv = torch.empty_like(send)                      # block s comes from rank s
+    dist.all_to_all_single(recv, send)
+    ms, mi = oracle.merge_carrier(recv.numpy(), nvp, world_size=world, heads_per_rank=hpr,
+                                  init_blocks=1, local_blocks=3)
+    full, _ = oracle.score_chunks(q, inp.index_k.numpy(), inp.block_table.numpy(),
+                                  inp.seq_lens.numpy(), qo, cols=cols, rank=0, world_size=1,
+                                  page_size=128, fill=-np.inf)
+    rs, ri = oracle.select(full.astype(np.float32), nvp, init_blocks=1, local_blocks=3)
+    heads = slice(rank * hpr, (rank + 1) * hpr)
+    out[rank] = bool(np.array_equal(mi, ri[:, heads]) and
+                     np.array_equal(ms.view(np.int32), rs[:, heads].view(np.int32)))
+    dist.destroy_process_group()
+
+
+def test_prefill_carrier_exchange_with_gloo():
+    port = _free_port()
+    out = mp.Manager().dict()
+    mp.spawn(_prefill_exchange_worker, args=(2, port, out), nprocs=2, join=True)
+    assert out[0] and out[1]
