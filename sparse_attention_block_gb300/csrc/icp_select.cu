@@ -442,6 +442,103 @@ __device__ __forceinline__ float key_score(unsigned long long k, const float *ro
   return __ldg(row_src + (scale == 1 ? d : d / scale));
 }
 
+// Rows of at most 256 columns with float4 loads: a lane's share of a row
+// (two float4s) stays in registers, so the candidate pass re-reads nothing,
+// and the loads of the warp's next row (with its num_valid_pages) are in
+// flight while the current row is selected.
+constexpr int kShortMaxK = 256;
+constexpr int kShortF4 = kShortMaxK / 4 / 32;
+
+template <int MODE>
+__global__ void __launch_bounds__(32 * kSelWarps, 8) select_short_kernel(const SelectArgs a) {
+  __shared__ unsigned long long s_cand[kSelWarps][kCandCap];
+  __shared__ unsigned long long s_sel[kSelWarps][kTopK];
+  __shared__ int s_nc[kSelWarps];
+
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int rows = a.T * 4;
+  const int scale = a.index_scale, off = a.index_offset;
+  const int nf4 = a.K >> 2;
+  unsigned long long *sel = s_sel[warp];
+  const WarpScratch ws{s_cand[warp], &s_nc[warp], nullptr};
+  const int step = gridDim.x * kSelWarps;
+
+  float4 cur[kShortF4], nxt[kShortF4];
+  int nvp_cur = 0, nvp_nxt = 0;
+  auto load_row = [&](int row, float4 (&x)[kShortF4], int &nvp) {
+    const float4 *r4 = reinterpret_cast<const float4 *>(a.scores + (long long)row * a.K);
+#pragma unroll
+    for (int u = 0; u < kShortF4; ++u) {
+      const int f = lane + 32 * u;
+      x[u] = f < nf4 ? __ldg(r4 + f) : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+    nvp = __ldg(a.nvp + (row >> 2));
+  };
+
+  int row = blockIdx.x * kSelWarps + warp;
+  if (row < rows) load_row(row, cur, nvp_cur);
+  for (; row < rows; row += step) {
+    if (row + step < rows) load_row(row + step, nxt, nvp_nxt);
+    const int t = row >> 2, h = row & 3;
+    const int nvp = nvp_cur;
+    const float *src = a.scores + (long long)row * a.K;
+    const int flag0 = early_flag<MODE>(a, lane, t, h);
+    const Forced f = forced_ids(a, src, nvp, lane, true);
+    const int m = kTopK - f.nf;
+    int c_lo, c_hi;
+    free_range(a, nvp, c_lo, c_hi);
+    // best key of the lane's columns 4 (lane + 32 u) + k, ascending
+    float best = 0.0f;
+    int bc = -1;
+#pragma unroll
+    for (int u = 0; u < kShortF4; ++u) {
+      const float vv[4] = {cur[u].x, cur[u].y, cur[u].z, cur[u].w};
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        const int c = 4 * (lane + 32 * u) + k;
+        if ((unsigned)(c - c_lo) < (unsigned)(c_hi - c_lo) && (bc < 0 || vv[k] > best)) {
+          best = vv[k];
+          bc = c;
+        }
+      }
+    }
+    const unsigned long long tm = bc < 0 ? 0ull : make_key(best, bc * scale + off);
+    const unsigned long long tau = tau_lower_bound(tm, m);
+    if (lane == 0) *ws.nc = 0;
+    __syncwarp();
+    if (m > 0 && tm != 0ull && tm >= tau) {
+      const float ts = (tau >> 32) == 0 ? -INFINITY : unord_float((uint32_t)(tau >> 32));
+#pragma unroll
+      for (int u = 0; u < kShortF4; ++u) {
+        const float vv[4] = {cur[u].x, cur[u].y, cur[u].z, cur[u].w};
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          const int c = 4 * (lane + 32 * u) + k;
+          if ((unsigned)(c - c_lo) < (unsigned)(c_hi - c_lo)) offer_key(vv[k], c, ts, tau, scale, off, ws);
+        }
+      }
+    }
+    const int nch = m > 0 ? place_candidates<true>(src, c_lo, c_hi, lane, 32, scale, off, m, lane, ws, sel) : 0;
+    __syncwarp();
+    const int n = f.nf + nch;
+    int my_id = f.fid;
+    float my_sc = f.fsc;
+    if (lane >= f.nf && lane < n) {
+      const unsigned long long k = sel[lane - f.nf];
+      my_id = key_id(k);
+      my_sc = key_score(k, src, scale, off);
+    }
+    int out_id;
+    float out_sc;
+    sort_by_id_16(lane, n, my_id, my_sc, out_id, out_sc);
+    emit_row<MODE>(a, lane, row, t, h, out_id, out_sc, flag0);
+    __syncwarp();
+#pragma unroll
+    for (int u = 0; u < kShortF4; ++u) cur[u] = nxt[u];
+    nvp_cur = nvp_nxt;
+  }
+}
+
 // Rows up to 2048 columns: one warp per row (row = global warp index, then
 // + total warps), no CTA barrier.
 template <int MODE, bool VEC>
@@ -839,8 +936,19 @@ cudaError_t launch_select(const SelectArgs &a, int mode, int sm_count, cudaStrea
     }
     return cudaGetLastError();
   }
-  const int grid = (rows + kSelWarps - 1) / kSelWarps;
   const int threads = 32 * kSelWarps;
+  if (vec && a.K <= kShortMaxK) {
+    // persistent: eight CTAs per SM, each warp a row at a time with the next
+    // row's loads in flight
+    const int need = (rows + kSelWarps - 1) / kSelWarps;
+    const int g2 = need < 8 * sm_count ? need : 8 * sm_count;
+    if (mode == kEmitCarrier) select_short_kernel<kEmitCarrier><<<g2, threads, 0, stream>>>(a);
+    else if (mode == kEmitLegacy) select_short_kernel<kEmitLegacy><<<g2, threads, 0, stream>>>(a);
+    else if (mode == kEmitTagged) select_short_kernel<kEmitTagged><<<g2, threads, 0, stream>>>(a);
+    else select_short_kernel<kEmitPlain><<<g2, threads, 0, stream>>>(a);
+    return cudaGetLastError();
+  }
+  const int grid = (rows + kSelWarps - 1) / kSelWarps;
   if (mode == kEmitCarrier) {
     if (vec) select_warp_kernel<kEmitCarrier, true><<<grid, threads, 0, stream>>>(a);
     else select_warp_kernel<kEmitCarrier, false><<<grid, threads, 0, stream>>>(a);

@@ -128,3 +128,27 @@ def test_long_row_candidate_overflow_in_one_warp_slice():
     nvp = torch.tensor([K, 9000], dtype=torch.int32)
     for init, local in [(0, 0), (3, 4)]:
         _check(plane, nvp, init, local, what=f"warp-slice overflow init={init} local={local}")
+
+
+@pytest.mark.parametrize("K", [4, 128, 204, 252, 256])
+def test_short_rows_many_per_warp(K):
+    # rows of at most 256 columns stay in registers and each warp takes a
+    # row after another (5000 tokens: more rows than the grid's warps)
+    plane, nvp = W.make_select_plane(T=1300, K=K, seed=K + 7)
+    for init, local in [(1, 4), (0, 0), (4, 8)]:
+        _check(plane, nvp, init, local, what=f"short K={K} init={init} local={local}")
+
+
+def test_short_rows_candidate_overflow_and_ties():
+    # all-equal and heavily tied short rows overflow the 128-key candidate
+    # buffer, which takes the exact fallback
+    T, K = 6, 256
+    plane = torch.zeros((T, 4, K))
+    plane[1] = 7.0
+    plane[2, :, ::2] = 3.0
+    plane[3] = torch.randn(4, K).round()
+    plane[4] = -float("inf")
+    plane[5, :, :200] = 1.0
+    nvp = torch.tensor([K, K, K, 100, K, 230], dtype=torch.int32)
+    for init, local in [(0, 0), (2, 3)]:
+        _check(plane, nvp, init, local, what=f"short ties init={init} local={local}")
