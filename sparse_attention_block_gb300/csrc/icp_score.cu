@@ -497,57 +497,55 @@ score_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CU
     }
   } else if (warp == 1) {
     // ---------------------------------------------------------- MMA issuer
-    const uint32_t idesc = idesc_f8_f32(128, (int)kAccCols);
-    int stage = 0, acc = 0;
-    uint32_t sphase = 0, aphase = 0;
-    uint32_t qph0 = 0, qph1 = 0;
-    int qslot = 0;
-    SegmentWalker walk(prefix, nbatch, g0, g1);
-    int b, t0, t1;
-    bool ok = true;
-    while (ok && walk.next(b, t0, t1)) {
-      if (lane == 0) ok = mbar_wait(bar_qfull(qslot), qslot ? qph1 : qph0, abort_flag);
-      ok = __shfl_sync(0xFFFFFFFFu, ok, 0) != 0;
-      if (!ok) break;
-      const uint32_t qaddr = sb + kOffQ + qslot * kQBytes;
-      for (int tl = t0; tl < t1; ++tl) {
-        if (lane == 0) {
+    // One thread issues every MMA and runs the loop alone: no per-tile
+    // reconvergence of the warp.
+    if (lane == 0) {
+      const uint32_t idesc = idesc_f8_f32(128, (int)kAccCols);
+      int stage = 0, acc = 0;
+      uint32_t sphase = 0, aphase = 0;
+      uint32_t qph0 = 0, qph1 = 0;
+      int qslot = 0;
+      SegmentWalker walk(prefix, nbatch, g0, g1);
+      int b, t0, t1;
+      bool ok = true;
+      while (ok && walk.next(b, t0, t1)) {
+        ok = mbar_wait(bar_qfull(qslot), qslot ? qph1 : qph0, abort_flag);
+        if (!ok) break;
+        const uint32_t qaddr = sb + kOffQ + qslot * kQBytes;
+        for (int tl = t0; tl < t1; ++tl) {
           ok = mbar_wait(bar_full(stage), sphase, abort_flag) &&
                mbar_wait(bar_tempty(acc), aphase ^ 1u, abort_flag);
-          if (ok) {
-            tc_fence_after();
-            const uint32_t kaddr = sb + kOffStages + stage * kTileBytes;
-            const uint32_t d = tmem_base + (uint32_t)acc * kAccCols;
+          if (!ok) break;
+          tc_fence_after();
+          const uint32_t kaddr = sb + kOffStages + stage * kTileBytes;
+          const uint32_t d = tmem_base + (uint32_t)acc * kAccCols;
 #pragma unroll
-            for (int k = 0; k < 4; ++k)
-              mma_f8(d, smem_desc_sw128(qaddr + 32 * k), smem_desc_sw128(kaddr + 32 * k), idesc,
-                     k > 0 ? 1u : 0u);
-            mma_commit(bar_empty(stage));
-            mma_commit(bar_tfull(acc));
+          for (int k = 0; k < 4; ++k)
+            mma_f8(d, smem_desc_sw128(qaddr + 32 * k), smem_desc_sw128(kaddr + 32 * k), idesc,
+                   k > 0 ? 1u : 0u);
+          mma_commit(bar_empty(stage));
+          mma_commit(bar_tfull(acc));
+          if (++stage == kStages) {
+            stage = 0;
+            sphase ^= 1u;
+          }
+          if (++acc == kAcc) {
+            acc = 0;
+            aphase ^= 1u;
           }
         }
-        ok = __shfl_sync(0xFFFFFFFFu, ok, 0) != 0;
         if (!ok) break;
-        if (++stage == kStages) {
-          stage = 0;
-          sphase ^= 1u;
-        }
-        if (++acc == kAcc) {
-          acc = 0;
-          aphase ^= 1u;
-        }
+        mma_commit(bar_qempty(qslot));
+        if (qslot) qph1 ^= 1u; else qph0 ^= 1u;
+        qslot ^= 1;
       }
-      if (!ok) break;
-      if (lane == 0) mma_commit(bar_qempty(qslot));
-      __syncwarp();
-      if (qslot) qph1 ^= 1u; else qph0 ^= 1u;
-      qslot ^= 1;
+      if (*abort_flag) {
+        // every MMA issued so far must finish before TMEM is released
+        mma_commit(bar_done);
+        mbar_wait_drain(bar_done, 0);
+      }
     }
-    if (*abort_flag && lane == 0) {
-      // every MMA issued so far must finish before TMEM is released
-      mma_commit(bar_done);
-      mbar_wait_drain(bar_done, 0);
-    }
+    __syncwarp();
   } else {
     // ------------------------------------------------------------ epilogue
     const int q = warp & 3;      // TMEM lane quarter this warp may access
