@@ -239,68 +239,64 @@ __device__ __forceinline__ void epilogue_tile(const ScoreArgs &a, uint32_t taddr
 
 // Epilogue of one tile of the prefill scorer for one warp of the set that
 // owns it: lane l holds query row rowq + l of the record (128 distinct rows).
-// The accumulator is read 32 keys at a time, each chunk reduced while the
-// next one is loaded; a column that reaches past the record's first token is
-// masked per chunk with 32-bit compares.
+// A column that reaches past the record's first token is masked with 32-bit
+// compares.  With release, the warp hands the accumulator back once the tile
+// is in registers (the pair's last tile).
 template <int R>
 __device__ __forceinline__ void epilogue_tile_wide(const ScoreArgs &a, uint32_t ta, int lane,
                                                    int rowq, int tok0, int ntok, int tl,
-                                                   int nunits, int seq_len, uint32_t tempty) {
+                                                   int nunits, int seq_len, uint32_t tempty,
+                                                   bool release) {
   constexpr int CPT = 128 / R;  // plane columns in the tile
-  constexpr int KPC = R / 32;   // 32-key chunks per column
   const ScoreGeom &g = a.g;
   const int row = rowq + lane;
   const long long pfirst = (long long)seq_len - ntok;  // position of token 0
   const long long p_lane = pfirst + (row >> 2);        // position of this row's token
   const bool row_ok = row < 4 * ntok;
-  float x0[32], x1[32];
-  float m = -INFINITY;
-  tmem_ld32(ta, x0);
-  tmem_wait_ld();
+  // the whole tile in registers with one wait, then reductions with the most
+  // independent work first
+  float v[128];
 #pragma unroll
-  for (int k = 0; k < 4; ++k) {
-    float *cur = (k & 1) ? x1 : x0;
-    float *nxt = (k & 1) ? x0 : x1;
-    if (k < 3) {
-      tmem_ld32(ta + 32u * (k + 1), nxt);
-    } else {
-      // all four chunks are in registers: hand the accumulator back
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(tempty);
-    }
-    const int c = tl * CPT + k / KPC;
+  for (int k = 0; k < 4; ++k) tmem_ld32(ta + 32u * k, v + 32 * k);
+  tmem_wait_ld();
+  if (release) {
+    tc_fence_before();
+    __syncwarp();
+    if (lane == 0) mbar_arrive(tempty);
+  }
+#pragma unroll
+  for (int cc = 0; cc < CPT; ++cc) {
+    const int c = tl * CPT + cc;
+    float *vc = v + cc * R;
     const long long pos0 = g.split ? (long long)c * 128
                                    : (long long)c * a.page_size +
                                          (long long)a.rank * g.rows_per_page;
     if (pos0 + R - 1 > pfirst) {
-      // keys j <= lim of this chunk are at or before the row's token
-      const long long d = p_lane - pos0 - 32 * (k % KPC);
-      const int lim = (int)(d < -1 ? -1 : (d > 31 ? 31 : d));
+      // keys i <= lim of the column are at or before the row's token
+      const long long d = p_lane - pos0;
+      const int lim = (int)(d < -1 ? -1 : (d > R - 1 ? R - 1 : d));
 #pragma unroll
-      for (int j = 0; j < 32; ++j)
-        if (j > lim) cur[j] = -INFINITY;
+      for (int i = 0; i < R; ++i)
+        if (i > lim) vc[i] = -INFINITY;
     }
 #pragma unroll
-    for (int st = 16; st >= 1; st >>= 1) {
+    for (int st = R / 2; st >= 1; st >>= 1) {
 #pragma unroll
-      for (int j = 0; j < st; ++j) cur[j] = fmaxf(cur[j], cur[j + st]);
+      for (int i = 0; i < st; ++i) vc[i] = fmaxf(vc[i], vc[i + st]);
     }
-    m = fmaxf(m, cur[0]);
-    if (k % KPC == KPC - 1) {
-      if (c < nunits && c < a.cols && row_ok)
-        a.score_out[((long long)tok0 * 4 + row) * a.cols + c] = m + 0.0f;  // + 0 folds -0
-      m = -INFINITY;
-    }
-    if (k < 3) tmem_wait_ld();
+    if (c < nunits && c < a.cols && row_ok)
+      a.score_out[((long long)tok0 * 4 + row) * a.cols + c] = vc[0] + 0.0f;  // + 0 folds -0
   }
 }
 
 // WIDE: the prefill scorer.  A request (a plan record of up to 32 tokens)
-// stages 128 distinct query rows in one box.  The epilogue warps form
-// kEpiSetsWide sets of four; tile i of the CTA goes to set i % kEpiSetsWide,
-// whose four warps each finish their lane quarter (8 of the tokens), and the
-// accumulator is free again after those four arrivals.
+// stages 128 distinct query rows in one box.  Its tiles go in pairs: two
+// adjacent ring stages form one 256-row B operand and one N = 256 MMA group
+// (N = 128 for a segment's odd last tile) fills one of two 256-column
+// accumulators, pairs alternating.  The epilogue warps form two sets of
+// four, set s finishing tile s of every pair; each warp takes its lane
+// quarter (8 of the tokens) and the accumulator is free again after all
+// eight warps have arrived.
 template <bool FUSED, bool WIDE>
 __global__ void __launch_bounds__(BlockThreads<WIDE>::value, 1)
 score_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmq,
@@ -336,7 +332,7 @@ score_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CU
     }
     for (int i = 0; i < kAcc; ++i) {
       mbar_init(bar_tfull(i), 1);
-      mbar_init(bar_tempty(i), WIDE ? 4 : 1);
+      mbar_init(bar_tempty(i), WIDE ? 4 * kEpiSetsWide : 1);
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(bar_qfull(i), 1);
@@ -461,17 +457,28 @@ score_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CU
           pg_nxt = (grp + 32 + lane < cend) ? btrow[page_slot_of(grp + 32 + lane, g.split)] : 0;
         }
         const int ncol = min(g.cpt, cend - c0);
-        if (lane == 0) ok = mbar_wait(bar_empty(stage), sphase ^ 1u, abort_flag);
-        ok = __shfl_sync(0xFFFFFFFFu, ok, 0) != 0;
-        if (!ok) break;
+        // WIDE: tiles go in pairs (t0, t0 + 1), ... into slots of two
+        // adjacent stages, one barrier per slot; j is the tile in its pair
+        const int j = WIDE ? ((tl - t0) & 1) : 0;
+        if (j == 0) {
+          if (lane == 0) ok = mbar_wait(bar_empty(stage), sphase ^ 1u, abort_flag);
+          ok = __shfl_sync(0xFFFFFFFFu, ok, 0) != 0;
+          if (!ok) break;
+        }
         const int p0 = __shfl_sync(0xFFFFFFFFu, pg_cur, (c0 - grp) & 31);
         const int p1 = __shfl_sync(0xFFFFFFFFu, pg_cur, (c0 - grp + 1) & 31);
         const int p2 = __shfl_sync(0xFFFFFFFFu, pg_cur, (c0 - grp + 2) & 31);
         const int p3 = __shfl_sync(0xFFFFFFFFu, pg_cur, (c0 - grp + 3) & 31);
         if (lane == 0) {
           const uint32_t bar = bar_full(stage);
-          mbar_arrive_expect_tx(bar, (uint32_t)(ncol * g.R * 128));
-          const uint32_t dst = sb + kOffStages + stage * kTileBytes;
+          if (j == 0) {
+            uint32_t bytes = (uint32_t)(ncol * g.R * 128);
+            if (WIDE && tl + 1 < t1)
+              bytes += (uint32_t)(min(g.cpt, cend - c0 - g.cpt) * g.R * 128);
+            mbar_arrive_expect_tx(bar, bytes);
+          }
+          const uint32_t dst = WIDE ? sb + kOffStages + (stage * 2 + j) * kTileBytes
+                                    : sb + kOffStages + stage * kTileBytes;
           for (int k = 0; k < ncol; ++k) {
             const int c = c0 + k;
             const int pg = k == 0 ? p0 : (k == 1 ? p1 : (k == 2 ? p2 : p3));
@@ -480,18 +487,21 @@ score_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CU
           }
         }
         __syncwarp();
-        ++issued;
-        if (++stage == kStages) {
-          stage = 0;
-          sphase ^= 1u;
+        if (!WIDE || j == 1 || tl + 1 == t1) {
+          ++issued;
+          if (++stage == (WIDE ? kStages / 2 : kStages)) {
+            stage = 0;
+            sphase ^= 1u;
+          }
         }
       }
     }
     if (*abort_flag && lane == 0) {
       // let copies still in flight land before the CTA exits
-      const long long first = issued > kStages ? issued - kStages : 0;
+      constexpr int nst = WIDE ? kStages / 2 : kStages;
+      const long long first = issued > nst ? issued - nst : 0;
       for (long long n = first; n < issued; ++n)
-        mbar_wait_drain(bar_full((int)(n % kStages)), (uint32_t)((n / kStages) & 1));
+        mbar_wait_drain(bar_full((int)(n % nst)), (uint32_t)((n / nst) & 1));
       if (last_qslot >= 0)
         mbar_wait_drain(bar_qfull(last_qslot), (last_qslot ? qph1 : qph0) ^ 1u);
     }
@@ -512,26 +522,55 @@ score_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CU
         ok = mbar_wait(bar_qfull(qslot), qslot ? qph1 : qph0, abort_flag);
         if (!ok) break;
         const uint32_t qaddr = sb + kOffQ + qslot * kQBytes;
-        for (int tl = t0; tl < t1; ++tl) {
-          ok = mbar_wait(bar_full(stage), sphase, abort_flag) &&
-               mbar_wait(bar_tempty(acc), aphase ^ 1u, abort_flag);
-          if (!ok) break;
-          tc_fence_after();
-          const uint32_t kaddr = sb + kOffStages + stage * kTileBytes;
-          const uint32_t d = tmem_base + (uint32_t)acc * kAccCols;
+        if constexpr (WIDE) {
+          // a pair of tiles is one 256-row B operand (N = 256; N = 128 for a
+          // segment's odd last tile) into one of two 256-column accumulators
+          for (int tl = t0; tl < t1; tl += 2) {
+            const int np = min(2, t1 - tl);
+            ok = mbar_wait(bar_full(stage), sphase, abort_flag) &&
+                 mbar_wait(bar_tempty(acc), aphase ^ 1u, abort_flag);
+            if (!ok) break;
+            tc_fence_after();
+            const uint32_t kaddr = sb + kOffStages + stage * 2 * kTileBytes;
+            const uint32_t d = tmem_base + (uint32_t)acc * (2 * kAccCols);
+            const uint32_t id = np == 2 ? idesc_f8_f32(128, 2 * (int)kAccCols) : idesc;
 #pragma unroll
-          for (int k = 0; k < 4; ++k)
-            mma_f8(d, smem_desc_sw128(qaddr + 32 * k), smem_desc_sw128(kaddr + 32 * k), idesc,
-                   k > 0 ? 1u : 0u);
-          mma_commit(bar_empty(stage));
-          mma_commit(bar_tfull(acc));
-          if (++stage == kStages) {
-            stage = 0;
-            sphase ^= 1u;
+            for (int k = 0; k < 4; ++k)
+              mma_f8(d, smem_desc_sw128(qaddr + 32 * k), smem_desc_sw128(kaddr + 32 * k), id,
+                     k > 0 ? 1u : 0u);
+            mma_commit(bar_empty(stage));
+            mma_commit(bar_tfull(acc));
+            if (++stage == kStages / 2) {
+              stage = 0;
+              sphase ^= 1u;
+            }
+            if (++acc == 2) {
+              acc = 0;
+              aphase ^= 1u;
+            }
           }
-          if (++acc == kAcc) {
-            acc = 0;
-            aphase ^= 1u;
+        } else {
+          for (int tl = t0; tl < t1; ++tl) {
+            ok = mbar_wait(bar_full(stage), sphase, abort_flag) &&
+                 mbar_wait(bar_tempty(acc), aphase ^ 1u, abort_flag);
+            if (!ok) break;
+            tc_fence_after();
+            const uint32_t kaddr = sb + kOffStages + stage * kTileBytes;
+            const uint32_t d = tmem_base + (uint32_t)acc * kAccCols;
+#pragma unroll
+            for (int k = 0; k < 4; ++k)
+              mma_f8(d, smem_desc_sw128(qaddr + 32 * k), smem_desc_sw128(kaddr + 32 * k), idesc,
+                     k > 0 ? 1u : 0u);
+            mma_commit(bar_empty(stage));
+            mma_commit(bar_tfull(acc));
+            if (++stage == kStages) {
+              stage = 0;
+              sphase ^= 1u;
+            }
+            if (++acc == kAcc) {
+              acc = 0;
+              aphase ^= 1u;
+            }
           }
         }
         if (!ok) break;
@@ -584,7 +623,7 @@ score_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CU
     }
     uint32_t aphase = 0;
     int idx = 0;
-    int gi = 0;          // WIDE: the CTA's tile counter
+    int pi = 0;          // WIDE: the CTA's tile-pair counter
     const uint32_t taddr = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)e * kAccCols;
     unsigned long long *lk = nullptr;
     int *lfid = nullptr;
@@ -614,27 +653,36 @@ score_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CU
         for (int j = 0; j < kTopK; ++j) lk[j * 32 + lane] = 0ull;
       }
       if constexpr (WIDE) {
-        // the tiles of this warp's set, this warp's lane quarter (tokens
-        // 8 q .. 8 q + 7); gi counts the CTA's tiles as the MMA warp does
+        // every pair: set s finishes the pair's tile s, this warp's lane
+        // quarter (tokens 8 q .. 8 q + 7); pi counts the CTA's pairs as the
+        // MMA thread does, pair pi sits in accumulator pi & 1
         const int set = (warp - 2) >> 2;
-        for (int tl = t0; ok && tl < t1; ++tl, ++gi) {
-          if (gi % kEpiSetsWide != set) continue;
-          const int wacc = gi % kAcc;
-          const uint32_t wph = (uint32_t)(gi / kAcc) & 1u;
-          if (lane == 0) ok = mbar_wait(bar_tfull(wacc), wph, abort_flag);
+        for (int tl = t0; ok && tl < t1; tl += 2, ++pi) {
+          const int np = min(2, t1 - tl);
+          const int acc = pi & 1;
+          const uint32_t wph = (uint32_t)(pi >> 1) & 1u;
+          if (lane == 0) ok = mbar_wait(bar_tfull(acc), wph, abort_flag);
           ok = __shfl_sync(0xFFFFFFFFu, ok, 0) != 0;
           if (!ok) break;
           tc_fence_after();
-          const uint32_t ta = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)wacc * kAccCols;
-          if (g.R == 128)
-            epilogue_tile_wide<128>(a, ta, lane, q * 32, rv.tok0, rv.ntok, tl, nunits, seq_len,
-                                    bar_tempty(wacc));
-          else if (g.R == 64)
-            epilogue_tile_wide<64>(a, ta, lane, q * 32, rv.tok0, rv.ntok, tl, nunits, seq_len,
-                                   bar_tempty(wacc));
-          else
-            epilogue_tile_wide<32>(a, ta, lane, q * 32, rv.tok0, rv.ntok, tl, nunits, seq_len,
-                                   bar_tempty(wacc));
+          if (set < np) {
+            const uint32_t tj = tmem_base + ((uint32_t)(q * 32) << 16) +
+                                (uint32_t)acc * (2 * kAccCols) + (uint32_t)set * kAccCols;
+            if (g.R == 128)
+              epilogue_tile_wide<128>(a, tj, lane, q * 32, rv.tok0, rv.ntok, tl + set, nunits,
+                                      seq_len, bar_tempty(acc), true);
+            else if (g.R == 64)
+              epilogue_tile_wide<64>(a, tj, lane, q * 32, rv.tok0, rv.ntok, tl + set, nunits,
+                                     seq_len, bar_tempty(acc), true);
+            else
+              epilogue_tile_wide<32>(a, tj, lane, q * 32, rv.tok0, rv.ntok, tl + set, nunits,
+                                     seq_len, bar_tempty(acc), true);
+          } else {
+            // a segment's odd last tile: nothing for this set to read
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar_tempty(acc));
+          }
         }
       } else {
         // first tile of this segment that belongs to this warp
