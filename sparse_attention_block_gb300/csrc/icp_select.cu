@@ -1,4 +1,5 @@
-// icp_select.cu - Top16 select, legacy receive-row publish and owner merge.
+// icp_select.cu - Top16 select; its outputs (plain lists, legacy and tagged
+// receive rows, prefill carrier rows); the owner merges.
 //
 // Top16 rule (msa_icp_topk_select_publish with the forced blocks of
 // prepare_msa_icp_indexer): valid ids are c * index_scale + index_offset <
@@ -7,13 +8,9 @@
 // slots go to the best remaining ids by (score descending, id ascending).
 // Output: ids ascending with their raw scores, then (-1, -inf) padding.
 //
-// Select: one warp per row for rows up to 2048 columns; for longer rows one
-// CTA per row whose eight warps each select from an eighth of it.  Every
-// non-forced valid score
-// becomes a unique 64-bit key (score order, then lower id).  With m free
-// slots, tau = the m-th largest per-thread best is a lower bound of the m-th
-// largest key, and only the m threads whose best reaches tau can hold keys
-// >= tau; those are collected and the m largest picked exactly.
+// Select kernels by row length: rows of at most 256 columns with the row in
+// registers; one warp per row up to 2048 columns; longer rows on a CTA of
+// four warps.  The steps they share are described below, above kSelWarps.
 #include "icp_device.cuh"
 #include "icp_internal.h"
 
