@@ -19,13 +19,19 @@ namespace {
 
 constexpr int kRowWords = 33;
 
-// Bounded poll of a ready flag until it equals `want`.  Returns false after
-// spin_limit polls or kWaitTimeoutNs, whichever comes first.
+// Bounded poll of a ready flag until it equals `want` (acquire loads).
+// Returns false after spin_limit polls or kWaitTimeoutNs, whichever comes
+// first; the global timer is first read after 256 polls (reading it can
+// stall the warp, and most polls succeed at once).
 __device__ __forceinline__ bool poll_flag(const int *flag, int want, long long spin_limit) {
-  const unsigned long long t0 = globaltimer_ns();
+  unsigned long long t0 = 0;
   for (long long it = 0; it < spin_limit; ++it) {
     if (ld_acquire_gpu(flag) == want) return true;
-    if ((it & 255) == 255 && globaltimer_ns() - t0 > kWaitTimeoutNs) return false;
+    if ((it & 255) == 255) {
+      const unsigned long long now = globaltimer_ns();
+      if (t0 == 0) t0 = now;
+      else if (now - t0 > kWaitTimeoutNs) return false;
+    }
   }
   return false;
 }
@@ -786,39 +792,36 @@ __global__ void __launch_bounds__(128) merge_kernel(const MergeArgs a) {
   const int nvp = a.nvp[t];
   const int ws = a.world_size;
 
+  // lane s < ws polls source s's flag (acquire); the warp barrier then
+  // orders every lane's reads of the rows after those acquires, so all the
+  // rows are read at once (gpu-scope loads: the rows are reused every step)
+  int *row_of_lane = nullptr;
+  int ok = 1;
+  if (lane < ws) {
+    const long long r = (((long long)a.slot * ws + lane) * hpr + hl) * a.capacity + t;
+    row_of_lane = a.recv + r * kRowWords;
+    ok = poll_flag(row_of_lane + 32, 1, a.spin_limit) ? 1 : 0;
+  }
+  const unsigned read_mask = __ballot_sync(0xFFFFFFFFu, ok) & ((1u << ws) - 1u);
+  __syncwarp();
+  if (lane == 0 && read_mask != (1u << ws) - 1u)
+    atomicAdd(a.errors, ws - __popc(read_mask));
   int ids[4];
   float scs[4];
-  unsigned read_mask = 0;
 #pragma unroll
   for (int s = 0; s < 4; ++s) {
     ids[s] = -1;
     scs[s] = -INFINITY;
-    if (s >= ws) continue;
-    const long long r = (((long long)a.slot * ws + s) * hpr + hl) * a.capacity + t;
-    int *row = a.recv + r * kRowWords;
-    int ok = 0;
-    if (lane == 0) ok = poll_flag(row + 32, 1, a.spin_limit) ? 1 : 0;
-    ok = __shfl_sync(0xFFFFFFFFu, ok, 0);
-    if (!ok) {
-      if (lane == 0) atomicAdd(a.errors, 1);
-      continue;
-    }
-    read_mask |= 1u << s;
-    if (lane < kTopK) {
-      (void)ld_acquire_gpu(row + 32);  // order this lane's reads after the flag
-      scs[s] = __int_as_float(row[lane]);
-      ids[s] = row[kTopK + lane];
+    if (((read_mask >> s) & 1u) && lane < kTopK) {
+      const long long r = (((long long)a.slot * ws + s) * hpr + hl) * a.capacity + t;
+      const int *row = a.recv + r * kRowWords;
+      scs[s] = __int_as_float(ld_relaxed_gpu(row + lane));
+      ids[s] = ld_relaxed_gpu(row + kTopK + lane);
     }
   }
+  // free the rows that were read, after every lane's reads
   __syncwarp();
-  // free the rows that were read
-  if (lane == 0) {
-    for (int s = 0; s < ws; ++s)
-      if (read_mask & (1u << s)) {
-        const long long r = (((long long)a.slot * ws + s) * hpr + hl) * a.capacity + t;
-        st_release_gpu(a.recv + r * kRowWords + 32, 0);
-      }
-  }
+  if (lane < ws && ok) st_release_gpu(row_of_lane + 32, 0);
 
   merge_finish(a, lane, t, hl, nvp, ids, scs, s_id[warp], s_sc[warp]);
 }
