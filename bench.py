@@ -1,13 +1,15 @@
 """Benchmark of the decode-time ICP block indexer on GB300.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                    [--workload multitoken|batched|sharded|longctx|tiny|select]
+                    [--workload multitoken|batched|sharded|longctx|tiny|select|prefill]
 
 One step is one pass of the decode chain over one batch: the score plane
 (icp_score, one launch per shard), the Top16 select + publish into legacy
 receive rows (icp_publish_rows, one per shard) and the owner merge
 (icp_merge, one per owner).  The `select` workload times icp_top16_select
-alone on the standalone [256, 4, 12284] plane.
+alone on the standalone [256, 4, 12284] plane; the `prefill` workload times
+one prefill window (plan, scorer, carrier select, carrier merge) and reports
+the scorer against the fp8 tensor peak.
 
 Metric: index-K scoring throughput as algorithmic HBM bytes per second
 (index-K rows needed + queries + plane written + block table, then the

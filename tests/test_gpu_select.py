@@ -104,7 +104,7 @@ def test_candidate_overflow_takes_the_exact_fallback():
 
 
 def test_long_rows_with_concentrated_maxima():
-    # the same concentration on rows long enough for the block-per-row kernel
+    # the same concentration on rows long enough for the CTA-per-row kernel
     K = 12284
     plane = torch.randn((3, 4, K))
     cols = torch.arange(0, K, 256)
@@ -115,12 +115,12 @@ def test_long_rows_with_concentrated_maxima():
 
 
 def test_long_row_candidate_overflow_in_one_warp_slice():
-    # Rows longer than 2048 columns are split over 8 warps; warp w owns the
-    # float4 chunks w * 32 + lane + 256 j.  Large values over all of warp 0's
+    # Rows longer than 2048 columns are split over 4 warps; warp w owns the
+    # float4 chunks w * 32 + lane + 128 j.  Large values over all of warp 0's
     # chunks overflow that warp's candidate buffer (exact fallback path).
     K = 12284
     plane = torch.randn((2, 4, K))
-    f = (torch.arange(32)[:, None] + 256 * torch.arange(K // 1024 + 1)[None, :]).reshape(-1)
+    f = (torch.arange(32)[:, None] + 128 * torch.arange(K // 512 + 1)[None, :]).reshape(-1)
     f = f[4 * f + 3 < K]
     cols = (4 * f[:, None] + torch.arange(4)[None, :]).reshape(-1)
     plane[:, :, cols] = 50.0 + torch.rand(cols.numel())
