@@ -21,6 +21,8 @@ fused_merge_kernel(const ScoreArgs a, const ReqInfo *info, int grid_a) {
   __shared__ unsigned long long s_cand[4][kTopK * 16 + 8];
   __shared__ int s_fid[4][kTopK];
   __shared__ float s_fsc[4][kTopK];
+  __shared__ int s_flist[4][kTopK];   // lists holding forced entries, in list order
+  __shared__ int s_ffirst[4][kTopK];  // slot of each such list's first forced entry
   // wait for the fused scorer (programmatic dependent launch)
   asm volatile("griddepcontrol.wait;" ::: "memory");
 
@@ -35,6 +37,8 @@ fused_merge_kernel(const ScoreArgs a, const ReqInfo *info, int grid_a) {
   unsigned long long *cand = s_cand[warp];
   int *fbuf_id = s_fid[warp];
   float *fbuf_sc = s_fsc[warp];
+  int *flist = s_flist[warp];
+  int *ffirst = s_ffirst[warp];
 
   const ReqInfo in = info[b];
   const long long total = in.total;
@@ -51,10 +55,11 @@ fused_merge_kernel(const ScoreArgs a, const ReqInfo *info, int grid_a) {
     return total * i / G < total * (i + 1) / G;
   };
 
-  // one pass over the lists: each list's maximum (to the shared cache) and
-  // its forced-entry count (every forced id was seen by exactly one list)
-  unsigned fmask_all = 0;  // bit j: list lane + 32 * j holds forced entries (j < 32)
-  for (int k0 = 0, j = 0; k0 < P; k0 += 32, ++j) {
+  // one pass over the lists: each list's maximum (to the shared cache),
+  // and the lists holding forced entries (every forced id was seen by
+  // exactly one list) with the slot of their first entry, in list order
+  int nfl = 0, nfe = 0;  // lists with forced entries, forced entries so far
+  for (int k0 = 0; k0 < P; k0 += 32) {
     const int k = k0 + lane;
     unsigned long long mxk = 0;
     int fc = 0;
@@ -64,24 +69,27 @@ fused_merge_kernel(const ScoreArgs a, const ReqInfo *info, int grid_a) {
       fc = __ldcg(&pr->fcount);
     }
     if (k < P) mx[k] = mxk;
-    if (fc > 0 && j < 32) fmask_all |= 1u << j;
-  }
-  // forced entries, gathered in list order (ids come out ordered later)
-  int nf = 0;
-  for (int k0 = 0, j = 0; k0 < P && j < 32; k0 += 32, ++j) {
-    unsigned msk = __ballot_sync(0xFFFFFFFFu, (fmask_all >> j) & 1u);
-    while (msk) {
-      const int src = __ffs(msk) - 1;
-      msk &= msk - 1;
-      const PartialRec *pr = partial_rec(a, pidx_of(k0 + src), r);
-      const int cnt = __ldcg(&pr->fcount);
-      if (lane < cnt && nf + lane < kTopK) {
-        fbuf_id[nf + lane] = __ldcg(&pr->fid[lane]);
-        fbuf_sc[nf + lane] = __ldcg(&pr->fsc[lane]);
-      }
-      nf = min(nf + cnt, kTopK);
+    int incl = fc;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+      if (lane >= o) incl += y;
     }
+    const unsigned bal = __ballot_sync(0xFFFFFFFFu, fc > 0);
+    if (fc > 0) {
+      const int pos = nfl + __popc(bal & ((1u << lane) - 1u));
+      if (pos < kTopK) {
+        flist[pos] = k;
+        ffirst[pos] = nfe + incl - fc;
+      }
+    }
+    nfl += __popc(bal);
+    nfe += __shfl_sync(0xFFFFFFFFu, incl, 31);
   }
+  nfl = min(nfl, kTopK);
+  const int nf_lists = min(nfe, kTopK);
+  // forced ids among the padding columns (no key: score -inf) come after
+  int nf = nf_lists;
   for (int c = nunits; c < wcols; ++c) {
     const int id = c * a.index_scale + a.index_offset;
     if (id < nvp && forced_id(id, nvp, a.init_blocks, a.local_blocks) && nf < kTopK) {
@@ -118,8 +126,18 @@ fused_merge_kernel(const ScoreArgs a, const ReqInfo *info, int grid_a) {
     ++found;
   }
   if (found < m) tau = 1;  // fewer than m lists hold entries: take all of them
-  // every winner's 16 keys in one round of loads (lane L reads entries
-  // L, L + 32, ... of the found * 16 keys), then compaction
+  // one round of loads: forced entry `lane` (lane < nf_lists) from its list,
+  // and every winner's 16 keys (lane L reads entries L, L + 32, ... of the
+  // found * 16 keys)
+  int f_id = 0;
+  float f_sc = -INFINITY;
+  if (lane < nf_lists) {
+    int li = 0;
+    while (li + 1 < nfl && ffirst[li + 1] <= lane) ++li;
+    const PartialRec *pr = partial_rec(a, pidx_of(flist[li]), r);
+    f_id = __ldcg(&pr->fid[lane - ffirst[li]]);
+    f_sc = __ldcg(&pr->fsc[lane - ffirst[li]]);
+  }
   unsigned long long kv[8];
 #pragma unroll
   for (int j = 0; j < 8; ++j) {
@@ -127,6 +145,10 @@ fused_merge_kernel(const ScoreArgs a, const ReqInfo *info, int grid_a) {
     const int wi = q >> 4;
     const int k = __shfl_sync(0xFFFFFFFFu, my_winner, wi & 31);
     kv[j] = (wi < found) ? __ldcg(&partial_rec(a, pidx_of(k), r)->keys[q & 15]) : 0ull;
+  }
+  if (lane < nf_lists) {
+    fbuf_id[lane] = f_id;
+    fbuf_sc[lane] = f_sc;
   }
   int nc = 0;
 #pragma unroll
