@@ -336,29 +336,37 @@ __device__ __forceinline__ bool forced_id(int id, int nvp, int init, int local) 
   return nvp <= kTopK || id < init || id >= nvp - local;
 }
 
-// Sorts the n <= 16 entries held by lanes 0..n-1 by id and writes the 16
-// output slots: lane r < 16 ends up owning slot r.
+// Sorts the n <= 16 entries held by lanes 0..n-1 by id (ids distinct) and
+// writes the 16 output slots: lane r < 16 ends up owning slot r, (-1, -inf)
+// past n.
 __device__ __forceinline__ void sort_by_id_16(int lane, int n, int my_id, float my_sc, int &out_id,
-                                              float &out_sc) {
+                                              float &out_sc, int *sid, float *ssc) {
+  // sid / ssc: 16 ints and 16 floats of warp-private scratch, which the
+  // caller may have just read (the barrier below orders those reads first)
+  __syncwarp();
+  // entries already ascending in lane order (a merged single list, for
+  // one) pass through
+  const int nxt = __shfl_down_sync(0xFFFFFFFFu, my_id, 1);
+  if (__all_sync(0xFFFFFFFFu, lane >= n - 1 || my_id < nxt)) {
+    out_id = lane < n ? my_id : -1;
+    out_sc = lane < n ? my_sc : -INFINITY;
+    return;
+  }
   int rank = 0;
 #pragma unroll
   for (int j = 0; j < kTopK; ++j) {
     const int oid = __shfl_sync(0xFFFFFFFFu, my_id, j);
     if (j < n && lane < n && oid < my_id) ++rank;
   }
-  // scatter through shuffles: slot r takes the entry of rank r
-  out_id = -1;
-  out_sc = -INFINITY;
-#pragma unroll
-  for (int j = 0; j < kTopK; ++j) {
-    const int r = __shfl_sync(0xFFFFFFFFu, rank, j);
-    const int id = __shfl_sync(0xFFFFFFFFu, my_id, j);
-    const float sc = __shfl_sync(0xFFFFFFFFu, my_sc, j);
-    if (j < n && r == lane) {
-      out_id = id;
-      out_sc = sc;
-    }
+  // slot r takes the entry of rank r
+  if (lane < n) {
+    sid[rank] = my_id;
+    ssc[rank] = my_sc;
   }
+  __syncwarp();
+  out_id = lane < n ? sid[lane] : -1;
+  out_sc = lane < n ? ssc[lane] : -INFINITY;
+  __syncwarp();
 }
 
 }  // namespace icp

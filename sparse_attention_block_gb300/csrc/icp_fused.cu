@@ -206,7 +206,7 @@ fused_merge_kernel(const ScoreArgs a, const ReqInfo *info, int grid_a) {
   }
   int out_id;
   float out_sc;
-  sort_by_id_16(lane, n, my_id, my_sc, out_id, out_sc);
+  sort_by_id_16(lane, n, my_id, my_sc, out_id, out_sc, fbuf_id, fbuf_sc);
   if (lane < kTopK) {
     const long long o = (long long)row * kTopK + lane;
     a.out_scores[o] = out_sc;

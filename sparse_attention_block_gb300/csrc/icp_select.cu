@@ -533,7 +533,8 @@ __global__ void __launch_bounds__(32 * kSelWarps, 8) select_short_kernel(const S
     }
     int out_id;
     float out_sc;
-    sort_by_id_16(lane, n, my_id, my_sc, out_id, out_sc);
+    sort_by_id_16(lane, n, my_id, my_sc, out_id, out_sc, reinterpret_cast<int *>(sel),
+                  reinterpret_cast<float *>(sel) + kTopK);
     emit_row<MODE>(a, lane, row, t, h, out_id, out_sc, flag0);
     __syncwarp();
 #pragma unroll
@@ -585,7 +586,8 @@ __global__ void __launch_bounds__(32 * kSelWarps, 8) select_warp_kernel(const Se
     }
     int out_id;
     float out_sc;
-    sort_by_id_16(lane, n, my_id, my_sc, out_id, out_sc);
+    sort_by_id_16(lane, n, my_id, my_sc, out_id, out_sc, reinterpret_cast<int *>(sel),
+                  reinterpret_cast<float *>(sel) + kTopK);
     emit_row<MODE>(a, lane, row, t, h, out_id, out_sc, flag0);
     __syncwarp();
   }
@@ -675,7 +677,8 @@ __global__ void __launch_bounds__(32 * RW, 32 / RW) select_row_kernel(const Sele
       }
       int out_id;
       float out_sc;
-      sort_by_id_16(lane, n, my_id, my_sc, out_id, out_sc);
+      sort_by_id_16(lane, n, my_id, my_sc, out_id, out_sc, reinterpret_cast<int *>(s_mout),
+                    reinterpret_cast<float *>(s_mout) + kTopK);
       emit_row<MODE>(a, lane, row, t, h, out_id, out_sc, flag0);
     }
     __syncthreads();  // lists are reused by the next row
@@ -765,7 +768,7 @@ __device__ __forceinline__ void merge_finish(const MergeArgs &a, int lane, int t
   }
   int out_id;
   float out_sc;
-  sort_by_id_16(lane, n, my_id, my_sc, out_id, out_sc);
+  sort_by_id_16(lane, n, my_id, my_sc, out_id, out_sc, s_idw, s_scw);
   if (lane < kTopK) {
     const long long o = ((long long)t * hpr + hl) * kTopK + lane;
     a.out_scores[o] = out_sc;
