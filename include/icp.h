@@ -311,8 +311,8 @@ int64_t icp_prefill_plan_words(int batch, int T);
  * synchronisation).
  *   qo_indptr int32 [batch + 1], seq_lens int32 [batch] (each request's
  *   length after the window's tokens), both device memory.
- *   plan      int32 [plan_words] device memory, written whole by the call;
- *             plan_words >= icp_prefill_plan_words(batch, T).
+ *   plan      int32 [plan_words] device memory, 16-byte aligned, written
+ *             by the call; plan_words >= icp_prefill_plan_words(batch, T).
  *   errors    int32 [>= 1] or NULL: a request whose chunk is invalid (a
  *             decreasing qo_indptr, outside [0, T], or longer than its
  *             seq_len) gets no records and adds 1; its tokens' plane rows

@@ -426,7 +426,7 @@ int64_t icp_prefill_plan_words(int batch, int T) {
 int icp_prefill_plan(const int32_t *qo_indptr, const int32_t *seq_lens, int batch, int T,
                      int32_t *plan, int64_t plan_words, int32_t *errors, void *stream) {
   const int64_t need = icp_prefill_plan_words(batch, T);
-  if (need < 0 || plan_words < need || !plan) return ICP_ERR_INVALID_ARG;
+  if (need < 0 || plan_words < need || !plan || !aligned16(plan)) return ICP_ERR_INVALID_ARG;
   if (batch > 0 && (!qo_indptr || !seq_lens)) return ICP_ERR_INVALID_ARG;
   int dev = 0, sms = 0;
   int st = current_device(&dev, &sms);
@@ -442,7 +442,7 @@ int icp_prefill_score(const uint8_t *index_q, const uint8_t *index_k, int64_t nu
                       const int32_t *plan, int64_t plan_words, float *score_out, int T,
                       int cols, int rank, int world_size, int page_size, int32_t *errors,
                       void *stream) {
-  if (T < 0 || plan_words < icp::kPlanHeaderInts + icp::kPlanRecordInts)
+  if (T < 0 || plan_words < icp::kPlanHeaderInts + icp::kPlanRecordInts || !aligned16(plan))
     return ICP_ERR_INVALID_ARG;
   const int64_t records = (plan_words - icp::kPlanHeaderInts) / icp::kPlanRecordInts;
   const int capacity = (int)(records < icp::kMaxBatchDevice ? records : icp::kMaxBatchDevice);

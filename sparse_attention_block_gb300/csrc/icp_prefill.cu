@@ -33,6 +33,7 @@ __global__ void __launch_bounds__(kPlanThreads) prefill_plan_kernel(
     const int32_t *qo, const int32_t *seq_lens, int batch, int T, int32_t *plan, int capacity,
     int32_t *errors) {
   __shared__ int s_part[kPlanThreads / 32];
+  __shared__ int s_first[kMaxBatchDevice + 1];  // first record of every request
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int chunk = (batch + kPlanThreads - 1) / kPlanThreads;
   const int lo = min(batch, tid * chunk), hi = min(batch, lo + chunk);
@@ -54,33 +55,39 @@ __global__ void __launch_bounds__(kPlanThreads) prefill_plan_kernel(
   __syncthreads();
   int base = 0;
   for (int w = 0; w < warp; ++w) base += s_part[w];
-  if (tid == kPlanThreads - 1) plan[0] = min(base + incl, capacity);
-
   int run = base + incl - sum;
-  int over = 0;
   for (int b = lo; b < hi; ++b) {
-    const int r = records_of(qo, seq_lens, b, T);
-    if (r <= 0) continue;
-    const int q0 = qo[b], n = qo[b + 1] - q0, sl = seq_lens[b];
-    for (int k = 0; k < r; ++k) {
-      const int idx = run + k;
-      if (idx >= capacity) {
-        ++over;
-        continue;
-      }
-      const int ntok = min(kPlanTokens, n - kPlanTokens * k);
-      int32_t *rec = plan + kPlanHeaderInts + (long long)kPlanRecordInts * idx;
-      rec[0] = q0 + kPlanTokens * k;                 // first token
-      rec[1] = b;                                    // block-table row
-      rec[2] = sl - n + kPlanTokens * k + ntok;      // last position + 1
-      rec[3] = ntok;
-      rec[4] = sl;                                   // the request's seq_len
-      rec[5] = 0;
-      rec[6] = 0;
-      rec[7] = 0;
-    }
-    run += r;
+    s_first[b] = run;
+    run += max(records_of(qo, seq_lens, b, T), 0);
   }
+  if (tid == kPlanThreads - 1) {
+    s_first[batch] = base + incl;
+    plan[0] = min(base + incl, capacity);
+  }
+  __syncthreads();
+
+  // every thread writes records tid, tid + kPlanThreads, ...; the request
+  // of record idx is the last one whose first record is <= idx (requests
+  // without records share their successor's first record)
+  const int total = s_first[batch];
+  const int n_out = min(total, capacity);
+  for (int idx = tid; idx < n_out; idx += kPlanThreads) {
+    int b0 = 0, b1 = batch - 1;
+    while (b0 < b1) {
+      const int mid = (b0 + b1 + 1) >> 1;
+      if (s_first[mid] <= idx) b0 = mid;
+      else b1 = mid - 1;
+    }
+    const int b = b0, k = idx - s_first[b0];
+    const int q0 = qo[b], n = qo[b + 1] - q0, sl = seq_lens[b];
+    const int ntok = min(kPlanTokens, n - kPlanTokens * k);
+    int4 *rec = reinterpret_cast<int4 *>(plan + kPlanHeaderInts + (long long)kPlanRecordInts * idx);
+    // {first token, block-table row, last position + 1, tokens}, {the
+    // request's seq_len, 0, 0, 0}
+    rec[0] = make_int4(q0 + kPlanTokens * k, b, sl - n + kPlanTokens * k + ntok, ntok);
+    rec[1] = make_int4(sl, 0, 0, 0);
+  }
+  const int over = tid == 0 ? max(total - capacity, 0) : 0;
   if ((bad || over) && errors) atomicAdd(errors, bad + over);
 }
 

@@ -131,6 +131,8 @@ def test_prefill_sizes_and_checks(lib):
     lib.icp_prefill_plan.argtypes = [P, P, ctypes.c_int, ctypes.c_int, P, ctypes.c_int64, P, P]
     assert lib.icp_prefill_plan(a, a, 2, 64, a, 8 + 8 * 3, None, None) == INVALID  # too small
     assert lib.icp_prefill_plan(a, a, 2, 64, None, 8 + 8 * 4, None, None) == INVALID
+    odd = ctypes.c_void_p(a.value + 4)                    # the plan is read as int4
+    assert lib.icp_prefill_plan(a, a, 2, 64, odd, 8 + 8 * 4, None, None) == INVALID
     lib.icp_prefill_score.argtypes = [P, P, ctypes.c_int64, P, ctypes.c_int64, P, ctypes.c_int64,
                                       P] + [ctypes.c_int] * 5 + [P, P]
     assert lib.icp_prefill_score(a, a, 4, a, 4, a, 8 + 8 * 4, a, 10, 6, 0, 1, 128, None,
