@@ -327,6 +327,29 @@ __device__ __forceinline__ uint64_t warp_max_key(uint64_t k) {
   return ((uint64_t)mhi << 32) | mlo;
 }
 
+// Maximum of three floats in one instruction.
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+  float r;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+  return r;
+}
+
+// Maximum of v[0..N) into v[0] by a tree of three-input maxima (N - 1 / 2
+// instructions instead of N - 1; a maximum is exact in any order).
+template <int N>
+__device__ __forceinline__ void max_tree3(float *v) {
+  if constexpr (N > 1) {
+    constexpr int M = (N + 2) / 3;  // one level: N values into M
+#pragma unroll
+    for (int i = 0; i < M; ++i) {
+      if (3 * i + 2 < N) v[i] = fmax3(v[3 * i], v[3 * i + 1], v[3 * i + 2]);
+      else if (3 * i + 1 < N) v[i] = fmaxf(v[3 * i], v[3 * i + 1]);
+      else v[i] = v[3 * i];
+    }
+    max_tree3<M>(v);
+  }
+}
+
 // ------------------------------------------------------------- Top16 rule
 constexpr int kTopK = 16;
 

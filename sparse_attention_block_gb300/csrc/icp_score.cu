@@ -209,11 +209,7 @@ __device__ __forceinline__ void epilogue_tile(const ScoreArgs &a, uint32_t taddr
       for (int i = 0; i < R; ++i)
         if (pos0 + i > p_lane) vc[i] = -INFINITY;
     }
-#pragma unroll
-    for (int st = R / 2; st >= 1; st >>= 1) {
-#pragma unroll
-      for (int i = 0; i < st; ++i) vc[i] = fmaxf(vc[i], vc[i + st]);
-    }
+    max_tree3<R>(vc);
     const float val = vc[0] + 0.0f;  // + 0 folds -0 onto +0
     if (row_ok && c < a.cols) {
       if constexpr (!FUSED) {
@@ -279,11 +275,7 @@ __device__ __forceinline__ void epilogue_tile_wide(const ScoreArgs &a, uint32_t 
       for (int i = 0; i < R; ++i)
         if (i > lim) vc[i] = -INFINITY;
     }
-#pragma unroll
-    for (int st = R / 2; st >= 1; st >>= 1) {
-#pragma unroll
-      for (int i = 0; i < st; ++i) vc[i] = fmaxf(vc[i], vc[i + st]);
-    }
+    max_tree3<R>(vc);
     if (c < nunits && c < a.cols && row_ok)
       a.score_out[((long long)tok0 * 4 + row) * a.cols + c] = vc[0] + 0.0f;  // + 0 folds -0
   }
