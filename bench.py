@@ -47,10 +47,10 @@ FALLBACK_HBM_GBS = 6800.0
 # streamed), measured for the kernel source with this digest.  When the
 # kernel changes the digest no longer matches and `traffic` is reported null.
 NCU_TRAFFIC = {
-    # dram__bytes_read.sum + dram__bytes_write.sum = 278821376 + 3120896 bytes for
+    # dram__bytes_read.sum + dram__bytes_write.sum = 278821632 + 3133952 bytes for
     # 278330624 bytes of index-K (first 32 requests of the multitoken workload),
     # see profiles/icp_score_multitoken.md
-    ("multitoken", "9f3daeab0f12e5a6"): (278821376 + 3120896) / 278330624,
+    ("multitoken", "2dae2d2342efceae"): (278821632 + 3133952) / 278330624,
 }
 
 
