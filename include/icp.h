@@ -141,12 +141,17 @@ int icp_top16_select(const float *scores, int T, int K, const int32_t *num_valid
  *   Every row t < T, padding rows included, is written on every call.
  *   Limits: slot 0..2; world_size 1, 2 or 4; 0 <= rank < world_size;
  *   1 <= T <= capacity; spin_limit >= 1.  errors: int32 [>= 1], required.
+ *   enable_pdl (msa_icp_topk_select_publish, enable_pdl): launch with
+ *   programmatic dependent launch.  The kernel waits on the preceding
+ *   kernel (griddepcontrol.wait) before it reads anything, and only then
+ *   lets its own dependents launch, so it may follow a scorer launched with
+ *   or without it.  0 launches it as an ordinary kernel.
  */
 int icp_publish_rows(const float *scores, int T, int K, const int32_t *num_valid_pages,
                      const int64_t *recv_bases, int32_t *errors, int slot, int rank,
                      int world_size, int heads_per_rank, int capacity, int force_begin_blocks,
                      int force_end_blocks, int64_t spin_limit, int index_scale,
-                     int index_offset, void *stream);
+                     int index_offset, int enable_pdl, void *stream);
 
 /*
  * Owner merge of the decode chain (prepare_msa_icp_indexer, decode():
@@ -182,14 +187,14 @@ int icp_merge(int32_t *recv, const int32_t *num_valid_pages, int T, int slot, in
  *                generation generations[s][h][t] + 1, which is stored back.
  *   Nothing waits for a free row: as the page states, tagged mode needs at
  *   least two sparse layers between uses of one slot set.  Every row t < T,
- *   padding rows included, is written on every call.  Limits as
- *   icp_publish_rows (no spin_limit, no errors).
+ *   padding rows included, is written on every call.  Limits and
+ *   enable_pdl as icp_publish_rows (no spin_limit, no errors).
  */
 int icp_publish_rows_tagged(const float *scores, int T, int K, const int32_t *num_valid_pages,
                             const int64_t *recv_bases, int32_t *generations, int slot, int rank,
                             int world_size, int heads_per_rank, int capacity,
                             int force_begin_blocks, int force_end_blocks, int index_scale,
-                            int index_offset, void *stream);
+                            int index_offset, int enable_pdl, void *stream);
 
 /*
  * Owner merge of tagged rows (this library's reading; the counters of the

@@ -215,7 +215,7 @@ int icp_publish_rows(const float *scores, int T, int K, const int32_t *num_valid
                      const int64_t *recv_bases, int32_t *errors, int slot, int rank,
                      int world_size, int heads_per_rank, int capacity, int force_begin_blocks,
                      int force_end_blocks, int64_t spin_limit, int index_scale,
-                     int index_offset, void *stream) {
+                     int index_offset, int enable_pdl, void *stream) {
   if (!valid_select_common(T, K, force_begin_blocks, force_end_blocks, index_scale,
                            index_offset))
     return ICP_ERR_INVALID_ARG;
@@ -245,6 +245,7 @@ int icp_publish_rows(const float *scores, int T, int K, const int32_t *num_valid
   a.heads_per_rank = heads_per_rank;
   a.capacity = capacity;
   a.spin_limit = spin_limit;
+  a.pdl = enable_pdl ? 1 : 0;
   return to_status(icp::launch_select(a, 1, sms, static_cast<cudaStream_t>(stream)));
 }
 
@@ -284,7 +285,7 @@ int icp_publish_rows_tagged(const float *scores, int T, int K, const int32_t *nu
                             const int64_t *recv_bases, int32_t *generations, int slot, int rank,
                             int world_size, int heads_per_rank, int capacity,
                             int force_begin_blocks, int force_end_blocks, int index_scale,
-                            int index_offset, void *stream) {
+                            int index_offset, int enable_pdl, void *stream) {
   if (!valid_select_common(T, K, force_begin_blocks, force_end_blocks, index_scale,
                            index_offset))
     return ICP_ERR_INVALID_ARG;
@@ -313,6 +314,7 @@ int icp_publish_rows_tagged(const float *scores, int T, int K, const int32_t *nu
   a.world_size = world_size;
   a.heads_per_rank = heads_per_rank;
   a.capacity = capacity;
+  a.pdl = enable_pdl ? 1 : 0;
   return to_status(icp::launch_select(a, 2, sms, static_cast<cudaStream_t>(stream)));
 }
 

@@ -69,6 +69,7 @@ struct SelectArgs {
   long long spin_limit;
   int32_t *generations;  // tagged publish: [3][ws * hpr][capacity] counters
   int32_t *carrier;      // prefill carrier rows [ws][T][hpr][32]
+  int pdl;               // launched with programmatic dependent launch
 };
 
 struct MergeArgs {

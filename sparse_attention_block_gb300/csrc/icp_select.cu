@@ -457,6 +457,10 @@ __global__ void __launch_bounds__(32 * kSelWarps, 8) select_short_kernel(const S
   __shared__ unsigned long long s_cand[kSelWarps][kCandCap];
   __shared__ unsigned long long s_sel[kSelWarps][kTopK];
   __shared__ int s_nc[kSelWarps];
+  // under programmatic dependent launch: wait for the preceding kernel
+  // (the scorer) before reading its scores, then let dependents launch
+  pdl_wait();
+  pdl_launch_dependents();
 
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int rows = a.T * 4;
@@ -551,6 +555,10 @@ __global__ void __launch_bounds__(32 * kSelWarps, 8) select_warp_kernel(const Se
   __shared__ unsigned long long s_sel[kSelWarps][kTopK];
   __shared__ float s_cm[kSelWarps][kWarpRowChunks * 32];
   __shared__ int s_nc[kSelWarps];
+  // under programmatic dependent launch: wait for the preceding kernel
+  // (the scorer) before reading its scores, then let dependents launch
+  pdl_wait();
+  pdl_launch_dependents();
 
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int rows = a.T * 4;
@@ -611,6 +619,10 @@ __global__ void __launch_bounds__(32 * RW, 32 / RW) select_row_kernel(const Sele
   __shared__ float s_cm[RW][kLongRowChunks * 32];
   __shared__ int s_nc[RW];
   __shared__ int s_wn[RW];
+  // under programmatic dependent launch: wait for the preceding kernel
+  // (the scorer) before reading its scores, then let dependents launch
+  pdl_wait();
+  pdl_launch_dependents();
 
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int rows = a.T * 4;
@@ -917,55 +929,59 @@ __global__ void __launch_bounds__(128) merge_carrier_kernel(const MergeArgs a) {
 
 cudaError_t select_prepare() { return cudaSuccess; }
 
+// One select kernel launch, with the programmatic-serialization attribute
+// when a.pdl is set.
+template <typename Kernel>
+cudaError_t launch_one(Kernel kernel, int grid, int threads, const SelectArgs &a,
+                       cudaStream_t stream) {
+  if (!a.pdl) {
+    kernel<<<grid, threads, 0, stream>>>(a);
+    return cudaGetLastError();
+  }
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)grid);
+  cfg.blockDim = dim3((unsigned)threads);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, a);
+}
+
+template <int MODE>
+cudaError_t launch_select_mode(const SelectArgs &a, bool vec, int rows, int sm_count,
+                               cudaStream_t stream) {
+  if (a.K > kWarpRowMaxK) {
+    const int threads = 32 * kRowWarps;
+    return vec ? launch_one(select_row_kernel<kRowWarps, MODE, true>, rows, threads, a, stream)
+               : launch_one(select_row_kernel<kRowWarps, MODE, false>, rows, threads, a, stream);
+  }
+  const int threads = 32 * kSelWarps;
+  const int need = (rows + kSelWarps - 1) / kSelWarps;
+  if (vec && a.K <= kShortMaxK) {
+    // persistent: eight CTAs per SM, each warp a row at a time with the next
+    // row's loads in flight
+    const int g2 = need < 8 * sm_count ? need : 8 * sm_count;
+    return launch_one(select_short_kernel<MODE>, g2, threads, a, stream);
+  }
+  return vec ? launch_one(select_warp_kernel<MODE, true>, need, threads, a, stream)
+             : launch_one(select_warp_kernel<MODE, false>, need, threads, a, stream);
+}
+
 cudaError_t launch_select(const SelectArgs &a, int mode, int sm_count, cudaStream_t stream) {
   const int rows = a.T * 4;
   if (rows == 0) return cudaSuccess;
   // float4 rows when every row starts on a 16-byte boundary
   const bool vec = (a.K % 4 == 0) && ((reinterpret_cast<uintptr_t>(a.scores) & 15u) == 0);
-  if (a.K > kWarpRowMaxK) {
-    const int threads = 32 * kRowWarps;
-    if (mode == kEmitCarrier) {
-      if (vec) select_row_kernel<kRowWarps, kEmitCarrier, true><<<rows, threads, 0, stream>>>(a);
-      else select_row_kernel<kRowWarps, kEmitCarrier, false><<<rows, threads, 0, stream>>>(a);
-    } else if (mode == kEmitLegacy) {
-      if (vec) select_row_kernel<kRowWarps, kEmitLegacy, true><<<rows, threads, 0, stream>>>(a);
-      else select_row_kernel<kRowWarps, kEmitLegacy, false><<<rows, threads, 0, stream>>>(a);
-    } else if (mode == kEmitTagged) {
-      if (vec) select_row_kernel<kRowWarps, kEmitTagged, true><<<rows, threads, 0, stream>>>(a);
-      else select_row_kernel<kRowWarps, kEmitTagged, false><<<rows, threads, 0, stream>>>(a);
-    } else {
-      if (vec) select_row_kernel<kRowWarps, kEmitPlain, true><<<rows, threads, 0, stream>>>(a);
-      else select_row_kernel<kRowWarps, kEmitPlain, false><<<rows, threads, 0, stream>>>(a);
-    }
-    return cudaGetLastError();
+  switch (mode) {
+    case kEmitLegacy: return launch_select_mode<kEmitLegacy>(a, vec, rows, sm_count, stream);
+    case kEmitTagged: return launch_select_mode<kEmitTagged>(a, vec, rows, sm_count, stream);
+    case kEmitCarrier: return launch_select_mode<kEmitCarrier>(a, vec, rows, sm_count, stream);
+    default: return launch_select_mode<kEmitPlain>(a, vec, rows, sm_count, stream);
   }
-  const int threads = 32 * kSelWarps;
-  if (vec && a.K <= kShortMaxK) {
-    // persistent: eight CTAs per SM, each warp a row at a time with the next
-    // row's loads in flight
-    const int need = (rows + kSelWarps - 1) / kSelWarps;
-    const int g2 = need < 8 * sm_count ? need : 8 * sm_count;
-    if (mode == kEmitCarrier) select_short_kernel<kEmitCarrier><<<g2, threads, 0, stream>>>(a);
-    else if (mode == kEmitLegacy) select_short_kernel<kEmitLegacy><<<g2, threads, 0, stream>>>(a);
-    else if (mode == kEmitTagged) select_short_kernel<kEmitTagged><<<g2, threads, 0, stream>>>(a);
-    else select_short_kernel<kEmitPlain><<<g2, threads, 0, stream>>>(a);
-    return cudaGetLastError();
-  }
-  const int grid = (rows + kSelWarps - 1) / kSelWarps;
-  if (mode == kEmitCarrier) {
-    if (vec) select_warp_kernel<kEmitCarrier, true><<<grid, threads, 0, stream>>>(a);
-    else select_warp_kernel<kEmitCarrier, false><<<grid, threads, 0, stream>>>(a);
-  } else if (mode == kEmitLegacy) {
-    if (vec) select_warp_kernel<kEmitLegacy, true><<<grid, threads, 0, stream>>>(a);
-    else select_warp_kernel<kEmitLegacy, false><<<grid, threads, 0, stream>>>(a);
-  } else if (mode == kEmitTagged) {
-    if (vec) select_warp_kernel<kEmitTagged, true><<<grid, threads, 0, stream>>>(a);
-    else select_warp_kernel<kEmitTagged, false><<<grid, threads, 0, stream>>>(a);
-  } else {
-    if (vec) select_warp_kernel<kEmitPlain, true><<<grid, threads, 0, stream>>>(a);
-    else select_warp_kernel<kEmitPlain, false><<<grid, threads, 0, stream>>>(a);
-  }
-  return cudaGetLastError();
 }
 
 cudaError_t launch_merge_carrier(const MergeArgs &a, cudaStream_t stream) {

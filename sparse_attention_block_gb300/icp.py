@@ -42,7 +42,7 @@ lib.icp_top16_select.restype = _I32
 lib.icp_top16_select.argtypes = [_P, _I32, _I32, _P, _I32, _I32, _I32, _I32, _P, _P, _P]
 lib.icp_publish_rows.restype = _I32
 lib.icp_publish_rows.argtypes = [_P, _I32, _I32, _P, _P, _P, _I32, _I32, _I32, _I32, _I32, _I32,
-                                 _I32, _I64, _I32, _I32, _P]
+                                 _I32, _I64, _I32, _I32, _I32, _P]
 lib.icp_score_select_workspace_bytes.restype = _SZ
 lib.icp_score_select_workspace_bytes.argtypes = [_I32, _I32]
 lib.icp_score_select.restype = _I32
@@ -53,7 +53,7 @@ lib.icp_score_select_noalloc.argtypes = [_P, _P, _I64, _P, _I64, _P, _I32, _I32,
                                          _I32, _I32, _I32, _P, _I32, _I32, _P, _P, _P, _P]
 lib.icp_publish_rows_tagged.restype = _I32
 lib.icp_publish_rows_tagged.argtypes = [_P, _I32, _I32, _P, _P, _P, _I32, _I32, _I32, _I32,
-                                        _I32, _I32, _I32, _I32, _I32, _P]
+                                        _I32, _I32, _I32, _I32, _I32, _I32, _P]
 lib.icp_merge_tagged.restype = _I32
 lib.icp_merge_tagged.argtypes = [_P, _P, _P, _I32, _I32, _I32, _I32, _I32, _I32, _I32, _I64,
                                  _P, _P, _P, _P]
@@ -172,8 +172,10 @@ def icp_publish_rows(scores, num_valid_pages, recv_bases, errors, *, slot: int, 
                      world_size: int, heads_per_rank: int, capacity: int,
                      force_begin_blocks: int, force_end_blocks: int,
                      spin_limit: int = DEFAULT_SPIN_LIMIT, index_scale: int = 1,
-                     index_offset: int = 0, stream=None):
-    """Top16 select + publish into legacy receive rows (msa_icp_topk_select_publish)."""
+                     index_offset: int = 0, enable_pdl: bool = False, stream=None):
+    """Top16 select + publish into legacy receive rows (msa_icp_topk_select_publish).
+
+    enable_pdl: launch with programmatic dependent launch (see include/icp.h)."""
     sp = _dev(scores, "scores", (torch.float32,), 3)
     T, H, K = scores.shape
     if H != world_size * heads_per_rank:
@@ -185,7 +187,8 @@ def icp_publish_rows(scores, num_valid_pages, recv_bases, errors, *, slot: int, 
     ep = _dev(errors, "errors", (torch.int32,), 1)
     _check(lib.icp_publish_rows(sp, T, K, np_, rbp, ep, slot, rank, world_size, heads_per_rank,
                                 capacity, force_begin_blocks, force_end_blocks, spin_limit,
-                                index_scale, index_offset, _stream(stream)), "icp_publish_rows")
+                                index_scale, index_offset, 1 if enable_pdl else 0,
+                                _stream(stream)), "icp_publish_rows")
 
 
 def icp_merge(recv, num_valid_pages, out_scores, out_ids, errors, *, T: int, slot: int,
@@ -251,7 +254,8 @@ def icp_score_select(index_q, index_k, block_table, seq_lens, num_valid_pages, o
 def icp_publish_rows_tagged(scores, num_valid_pages, recv_bases, generations, *, slot: int,
                             rank: int, world_size: int, heads_per_rank: int, capacity: int,
                             force_begin_blocks: int, force_end_blocks: int,
-                            index_scale: int = 1, index_offset: int = 0, stream=None):
+                            index_scale: int = 1, index_offset: int = 0,
+                            enable_pdl: bool = False, stream=None):
     """Top16 select + publish into tagged receive rows (int64 generation << 32 | word)."""
     sp = _dev(scores, "scores", (torch.float32,), 3)
     T, H, K = scores.shape
@@ -267,7 +271,8 @@ def icp_publish_rows_tagged(scores, num_valid_pages, recv_bases, generations, *,
     _check(lib.icp_publish_rows_tagged(sp, T, K, np_, rbp, gp, slot, rank, world_size,
                                        heads_per_rank, capacity, force_begin_blocks,
                                        force_end_blocks, index_scale, index_offset,
-                                       _stream(stream)), "icp_publish_rows_tagged")
+                                       1 if enable_pdl else 0, _stream(stream)),
+           "icp_publish_rows_tagged")
 
 
 def icp_merge_tagged(recv, expected, num_valid_pages, out_scores, out_ids, errors, *, T: int,

@@ -85,11 +85,14 @@ def test_invalid_arguments_are_rejected_before_any_launch(lib):
     assert lib.icp_top16_select(a, 1, 100, a, 9, 8, 1, 0, a, a, None) == INVALID   # init+local > 16
     assert lib.icp_top16_select(a, 1, 100, a, 1, 2, 0, 0, a, a, None) == INVALID   # scale 0
     lib.icp_publish_rows.argtypes = [P, ctypes.c_int, ctypes.c_int, P, P, P] + \
-        [ctypes.c_int] * 7 + [ctypes.c_int64, ctypes.c_int, ctypes.c_int, P]
+        [ctypes.c_int] * 7 + [ctypes.c_int64, ctypes.c_int, ctypes.c_int, ctypes.c_int, P]
     # T > capacity, slot 3, hpr * ws != 4
-    assert lib.icp_publish_rows(a, 5, 10, a, a, a, 0, 0, 1, 4, 4, 1, 2, 100, 1, 0, None) == INVALID
-    assert lib.icp_publish_rows(a, 4, 10, a, a, a, 3, 0, 1, 4, 4, 1, 2, 100, 1, 0, None) == INVALID
-    assert lib.icp_publish_rows(a, 4, 10, a, a, a, 0, 0, 2, 1, 4, 1, 2, 100, 1, 0, None) == INVALID
+    assert lib.icp_publish_rows(a, 5, 10, a, a, a, 0, 0, 1, 4, 4, 1, 2, 100, 1, 0, 0,
+                                None) == INVALID
+    assert lib.icp_publish_rows(a, 4, 10, a, a, a, 3, 0, 1, 4, 4, 1, 2, 100, 1, 0, 0,
+                                None) == INVALID
+    assert lib.icp_publish_rows(a, 4, 10, a, a, a, 0, 0, 2, 1, 4, 1, 2, 100, 1, 0, 1,
+                                None) == INVALID
     lib.icp_status_string.restype = ctypes.c_char_p
     assert lib.icp_status_string(1) == b"invalid argument"
 

@@ -147,3 +147,43 @@ def test_merge_reports_a_source_that_never_published():
     ref_s, ref_i = oracle.select(plane.cpu().numpy(), nvp.cpu().numpy(), init_blocks=0,
                                  local_blocks=0)
     assert np.array_equal(i.cpu().numpy(), ref_i[:, :hpr])
+
+
+def test_chain_under_programmatic_dependent_launch():
+    # scorer and publish both launched with enable_pdl: the publish waits on
+    # the scorer before reading the plane, so the rows equal the oracle's
+    spec = W.DecodeSpec("pdl", batch=9, page_size=128, world_size=2, decode_query_len=2,
+                        max_decode_query_len=2, init_blocks=1, local_blocks=3,
+                        seq_range=(300, 20000), capacity=18)
+    inp = W.make_decode_inputs(spec, seed=77)
+    ws, hpr = 2, 2
+    cols = W.columns_for(spec, int(inp.seq_lens.max()))
+    bufs, bases = _recv(ws, hpr, spec.capacity, ws)
+    errors = torch.zeros(1, dtype=torch.int32, device="cuda")
+    q, _, bt, sl, nvp = to_dev(inp)
+    for step in range(3):
+        slot = step % 3
+        planes = []
+        for rank in range(ws):
+            shard = inp.shards[rank].cuda()
+            p = torch.empty((inp.T, 4, cols), device="cuda")
+            icp().icp_score(q, shard, bt, sl, p, rank=rank, world_size=ws, page_size=128,
+                            decode_query_len=2, max_decode_query_len=2, enable_pdl=True,
+                            errors=errors)
+            icp().icp_publish_rows(p, nvp, bases, errors, slot=slot, rank=rank, world_size=ws,
+                                   heads_per_rank=hpr, capacity=spec.capacity,
+                                   force_begin_blocks=1, force_end_blocks=3,
+                                   spin_limit=1 << 20, enable_pdl=True)
+            planes.append(p)
+        torch.cuda.synchronize()
+        ref = [np.zeros((3 * ws * hpr * spec.capacity, 33), np.int32) for _ in range(ws)]
+        for rank in range(ws):
+            oracle.publish(planes[rank].cpu().numpy(), inp.num_valid_pages.numpy(), ref,
+                           slot=slot, rank=rank, world_size=ws, heads_per_rank=hpr,
+                           capacity=spec.capacity, force_begin_blocks=1, force_end_blocks=3)
+        rows = slice(slot * ws * hpr * spec.capacity, (slot + 1) * ws * hpr * spec.capacity)
+        for owner in range(ws):
+            assert np.array_equal(bufs[owner].cpu().numpy()[rows], ref[owner][rows])
+        _merge_all(inp, spec, slot, bufs, errors, 1, 3)
+        torch.cuda.synchronize()
+        assert int(errors.item()) == 0
