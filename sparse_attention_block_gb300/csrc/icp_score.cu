@@ -415,11 +415,6 @@ score_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CU
       __syncwarp();
       pdl_wait();
     }
-    // a dependent launched with programmatic dependent launch (the Top16
-    // publish) may be scheduled now; it waits for this grid to complete
-    // before reading the plane, and this CTA has waited on its own
-    // predecessor above
-    if (lane == 0) pdl_launch_dependents();
     while (ok && walk.next(b, t0, t1)) {
       const ReqView rv = req_view(a, b);
       const int nunits = units_of(rv.seq_len, a.page_size, g.split);
