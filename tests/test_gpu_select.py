@@ -152,3 +152,34 @@ def test_short_rows_candidate_overflow_and_ties():
     nvp = torch.tensor([K, K, K, 100, K, 230], dtype=torch.int32)
     for init, local in [(0, 0), (2, 3)]:
         _check(plane, nvp, init, local, what=f"short ties init={init} local={local}")
+
+
+def test_many_full_length_rows():
+    # 2048 rows of 12284 columns, more rows than the long-row kernel keeps
+    # resident at once, with num_valid_pages at K and just below it
+    T, K = 512, 12284
+    plane, _ = W.make_select_plane(T=T, K=K, seed=21)
+    nvp = torch.full((T,), K, dtype=torch.int32)
+    nvp[::5] = K - 3
+    _check(plane, nvp, 4, 8, what="many full rows")
+
+
+def test_long_rows_with_empty_short_and_overlong_valid_ranges():
+    # 5200 rows of 2052 columns with num_valid_pages from none (and negative)
+    # through 16 and 17 (the all-kept boundary) to past K
+    T, K = 1300, 2052
+    plane, _ = W.make_select_plane(T=T, K=K, seed=22)
+    g = torch.Generator().manual_seed(22)
+    nvp = torch.randint(-3, K + 40, (T,), generator=g, dtype=torch.int32)
+    nvp[::7] = 0
+    nvp[1::7] = 16
+    nvp[2::7] = 17
+    for init, local in [(1, 3), (0, 0)]:
+        _check(plane, nvp, init, local, what=f"valid ranges init={init} local={local}")
+
+
+def test_long_rows_fewer_than_the_sms():
+    # a handful of long rows: fewer CTAs than SMs
+    for T in (1, 3):
+        plane, nvp = W.make_select_plane(T=T, K=8192, seed=23 + T)
+        _check(plane, nvp, 2, 2, what=f"T={T}")
