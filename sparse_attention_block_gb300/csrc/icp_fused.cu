@@ -23,6 +23,8 @@ fused_merge_kernel(const ScoreArgs a, const ReqInfo *info, int grid_a) {
   __shared__ float s_fsc[4][kTopK];
   __shared__ int s_flist[4][kTopK];   // lists holding forced entries, in list order
   __shared__ int s_ffirst[4][kTopK];  // slot of each such list's first forced entry
+  __shared__ unsigned long long s_sel[4][kTopK];  // the m largest candidates by rank
+  __shared__ int s_win[4][kTopK];                 // winner lists by rank
   // wait for the fused scorer (programmatic dependent launch)
   asm volatile("griddepcontrol.wait;" ::: "memory");
 
@@ -103,10 +105,26 @@ fused_merge_kernel(const ScoreArgs a, const ReqInfo *info, int grid_a) {
   const int m = kTopK - nf;
   __syncwarp();
   // tau = m-th largest list maximum; the lists holding keys >= tau are
-  // exactly the round winners
+  // exactly the m lists with the largest maxima (the winners).  Up to 32
+  // lists: every lane ranks its list's maximum against the others (the
+  // maxima are distinct keys); more lists: rounds of a warp maximum.
   unsigned long long prev = ~0ull, tau = 0;
   int found = 0, my_winner = -1;
-  for (int rd = 0; rd < m; ++rd) {
+  if (m > 0 && P <= 32) {
+    const unsigned long long x = lane < P ? mx[lane] : 0ull;
+    int rank = 0;
+#pragma unroll 8
+    for (int j = 0; j < 32; ++j) rank += __shfl_sync(0xFFFFFFFFu, x, j) > x ? 1 : 0;
+    const bool win = x != 0ull && rank < m;
+    found = __popc(__ballot_sync(0xFFFFFFFFu, win));
+    if (win) s_win[warp][rank] = lane;
+    const unsigned lastm = __ballot_sync(0xFFFFFFFFu, x != 0ull && rank == m - 1);
+    tau = found < m ? 1ull : __shfl_sync(0xFFFFFFFFu, x, lastm ? __ffs(lastm) - 1 : 0);
+    __syncwarp();
+    if (lane < found) my_winner = s_win[warp][lane];
+    __syncwarp();
+  }
+  for (int rd = 0; P > 32 && rd < m; ++rd) {
     unsigned long long local = 0;
     int lidx = -1;
     for (int k = lane; k < P; k += 32) {
@@ -125,7 +143,7 @@ fused_merge_kernel(const ScoreArgs a, const ReqInfo *info, int grid_a) {
     tau = w;
     ++found;
   }
-  if (found < m) tau = 1;  // fewer than m lists hold entries: take all of them
+  if (P > 32 && found < m) tau = 1;  // fewer than m lists hold entries: take all of them
   // one round of loads: forced entry `lane` (lane < nf_lists) from its list,
   // and every winner's 16 keys (lane L reads entries L, L + 32, ... of the
   // found * 16 keys)
@@ -169,18 +187,31 @@ fused_merge_kernel(const ScoreArgs a, const ReqInfo *info, int grid_a) {
     }
   }
   __syncwarp();
-  // the m largest candidates; lane nf + rd receives the rd-th
+  // the m largest candidates; lane nf + rd receives the rd-th.  Up to 64
+  // candidates: each is placed by its rank (the keys are distinct); more:
+  // rounds of a warp maximum.
+  unsigned long long mine = 0;
+  int nch = 0;
+  if (nc <= 64) {
+    for (int j = lane; j < nc; j += 32) {
+      const unsigned long long c = cand[j];
+      int rank = 0;
+      for (int i = 0; i < nc; ++i) rank += cand[i] > c ? 1 : 0;
+      if (rank < m) s_sel[warp][rank] = c;
+    }
+    nch = min(nc, max(m, 0));
+    __syncwarp();
+    if (lane >= nf && lane < nf + nch) mine = s_sel[warp][lane - nf];
+  }
   unsigned long long cl[9];
   unsigned long long lmax = 0;
 #pragma unroll
   for (int j = 0; j < 9; ++j) {
     const int k = lane + 32 * j;
-    cl[j] = (k < nc) ? cand[k] : 0ull;
+    cl[j] = (nc > 64 && k < nc) ? cand[k] : 0ull;
     lmax = cl[j] > lmax ? cl[j] : lmax;
   }
-  unsigned long long mine = 0;
-  int nch = 0;
-  for (int rd = 0; rd < m; ++rd) {
+  for (int rd = 0; nc > 64 && rd < m; ++rd) {
     const unsigned long long w = warp_max_key(lmax);
     if (w == 0) break;
     if (lane == nf + rd) mine = w;
