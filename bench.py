@@ -664,7 +664,11 @@ def run_reference(args, spec_name):
         return 0
     device = torch.device("cuda", local) if torch.cuda.is_available() else torch.device("cpu")
     bench = make_bench(spec_name, 0, device, args.batch)
-    per_step = float(os.environ.get("ICP_REF_STEP_SECONDS", "2.0"))
+    # each step a bounded sample: about two minutes of oracle work in all
+    # (ICP_REF_STEP_SECONDS overrides the per-step budget)
+    per_step = float(os.environ.get(
+        "ICP_REF_STEP_SECONDS",
+        str(min(2.0, max(0.05, 120.0 / max(1, args.steps + args.warmup / 4))))))
     cores, par = 1, None
     if spec_name not in ("select", "prefill"):
         # decode chains run over the requests on every host core
