@@ -697,28 +697,28 @@ __global__ void __launch_bounds__(32 * RW, 32 / RW) select_row_kernel(const Sele
   }
 }
 
-// Second half of a merge, once lane i < 16 holds entry i of every source in
-// ids[s] / scs[s] (id -1 = nothing): union with the maximum score per id,
-// the Top16 rule with num_valid_pages, and the output ordered by id.
+// Second half of a merge of NS sources (the world size), once lane i < 16
+// holds entry i of every source in ids[s] / scs[s] (id -1 = nothing): union
+// with the maximum score per id, the Top16 rule with num_valid_pages, and
+// the output ordered by id.
+template <int NS>
 __device__ __forceinline__ void merge_finish(const MergeArgs &a, int lane, int t, int hl, int nvp,
-                                             const int (&ids)[4], const float (&scs)[4],
+                                             const int (&ids)[NS], const float (&scs)[NS],
                                              int *s_idw, float *s_scw) {
   const int hpr = a.heads_per_rank;
-  const int ws = a.world_size;
   // keep an entry unless another source holds the same id with a higher
   // score (an exact tie goes to the lower source)
-  bool keep[4];
+  bool keep[NS];
 #pragma unroll
-  for (int s = 0; s < 4; ++s) keep[s] = lane < kTopK && ids[s] >= 0 && ids[s] < nvp;
-  if (ws > 1) {
+  for (int s = 0; s < NS; ++s) keep[s] = lane < kTopK && ids[s] >= 0 && ids[s] < nvp;
+  if constexpr (NS > 1) {
 #pragma unroll
-    for (int s2 = 0; s2 < 4; ++s2) {
-      if (s2 >= ws) break;
+    for (int s2 = 0; s2 < NS; ++s2) {
       for (int j = 0; j < kTopK; ++j) {
         const int id2 = __shfl_sync(0xFFFFFFFFu, ids[s2], j);
         const float sc2 = __shfl_sync(0xFFFFFFFFu, scs[s2], j);
 #pragma unroll
-        for (int s = 0; s < 4; ++s) {
+        for (int s = 0; s < NS; ++s) {
           if (s == s2 || !keep[s] || ids[s] != id2) continue;
           if (sc2 > scs[s] || (sc2 == scs[s] && s2 < s)) keep[s] = false;
         }
@@ -726,40 +726,42 @@ __device__ __forceinline__ void merge_finish(const MergeArgs &a, int lane, int t
     }
   }
   int total = 0, nforced = 0;
-  bool forced[4];
+  bool forced[NS];
 #pragma unroll
-  for (int s = 0; s < 4; ++s) {
+  for (int s = 0; s < NS; ++s) {
     forced[s] = keep[s] && forced_id(ids[s], nvp, a.init_blocks, a.local_blocks);
     total += __popc(__ballot_sync(0xFFFFFFFFu, keep[s]));
     nforced += __popc(__ballot_sync(0xFFFFFFFFu, forced[s]));
   }
-  bool sel[4];
+  bool sel[NS];
   if (total <= kTopK) {
 #pragma unroll
-    for (int s = 0; s < 4; ++s) sel[s] = keep[s];
+    for (int s = 0; s < NS; ++s) sel[s] = keep[s];
   } else {
     // m best free entries by (score desc, id asc)
     const int m = kTopK - min(nforced, kTopK);
-    unsigned long long key[4];
+    unsigned long long key[NS];
+    int rank[NS];
 #pragma unroll
-    for (int s = 0; s < 4; ++s) key[s] = (keep[s] && !forced[s]) ? make_key(scs[s], ids[s]) : 0ull;
-    int rank[4] = {0, 0, 0, 0};
+    for (int s = 0; s < NS; ++s) {
+      key[s] = (keep[s] && !forced[s]) ? make_key(scs[s], ids[s]) : 0ull;
+      rank[s] = 0;
+    }
 #pragma unroll
-    for (int s2 = 0; s2 < 4; ++s2) {
-      if (s2 >= ws) break;
+    for (int s2 = 0; s2 < NS; ++s2) {
       for (int j = 0; j < kTopK; ++j) {
         const unsigned long long k2 = __shfl_sync(0xFFFFFFFFu, key[s2], j);
 #pragma unroll
-        for (int s = 0; s < 4; ++s) rank[s] += (k2 > key[s]) ? 1 : 0;
+        for (int s = 0; s < NS; ++s) rank[s] += (k2 > key[s]) ? 1 : 0;
       }
     }
 #pragma unroll
-    for (int s = 0; s < 4; ++s) sel[s] = forced[s] || (key[s] != 0 && rank[s] < m);
+    for (int s = 0; s < NS; ++s) sel[s] = forced[s] || (key[s] != 0 && rank[s] < m);
   }
   // compact the selected entries (at most 16) and order them by id
   int n = 0;
 #pragma unroll
-  for (int s = 0; s < 4; ++s) {
+  for (int s = 0; s < NS; ++s) {
     const unsigned bal = __ballot_sync(0xFFFFFFFFu, sel[s]);
     if (sel[s]) {
       const int pos = n + __popc(bal & ((1u << lane) - 1u));
@@ -789,9 +791,10 @@ __device__ __forceinline__ void merge_finish(const MergeArgs &a, int lane, int t
 }
 
 // One warp per (token, owned head).  Lane i < 16 holds entry i of every
-// source row (at most 4 sources), so the union, the per-id maximum and the
-// ranking are done with shuffles; the result is compacted through shared
-// memory and ordered by id.
+// source row (NS = world size sources), so the union, the per-id maximum
+// and the ranking are done with shuffles; the result is compacted through
+// shared memory and ordered by id.
+template <int NS>
 __global__ void __launch_bounds__(128) merge_kernel(const MergeArgs a) {
   __shared__ int s_id[4][kTopK];
   __shared__ float s_sc[4][kTopK];
@@ -805,7 +808,7 @@ __global__ void __launch_bounds__(128) merge_kernel(const MergeArgs a) {
   if (item >= a.T * hpr) return;
   const int t = item / hpr, hl = item % hpr;
   const int nvp = a.nvp[t];
-  const int ws = a.world_size;
+  constexpr int ws = NS;
 
   // lane s < ws polls source s's flag (acquire); the warp barrier then
   // orders every lane's reads of the rows after those acquires, so all the
@@ -821,10 +824,10 @@ __global__ void __launch_bounds__(128) merge_kernel(const MergeArgs a) {
   __syncwarp();
   if (lane == 0 && read_mask != (1u << ws) - 1u)
     atomicAdd(a.errors, ws - __popc(read_mask));
-  int ids[4];
-  float scs[4];
+  int ids[NS];
+  float scs[NS];
 #pragma unroll
-  for (int s = 0; s < 4; ++s) {
+  for (int s = 0; s < NS; ++s) {
     ids[s] = -1;
     scs[s] = -INFINITY;
     if (((read_mask >> s) & 1u) && lane < kTopK) {
@@ -838,12 +841,13 @@ __global__ void __launch_bounds__(128) merge_kernel(const MergeArgs a) {
   __syncwarp();
   if (lane < ws && ok) st_release_gpu(row_of_lane + 32, 0);
 
-  merge_finish(a, lane, t, hl, nvp, ids, scs, s_id[warp], s_sc[warp]);
+  merge_finish<NS>(a, lane, t, hl, nvp, ids, scs, s_id[warp], s_sc[warp]);
 }
 
 // Owner merge of tagged rows: a source row has arrived when all 32 words
 // carry the owner's expected generation + 1 (the counter advances on every
 // merge).  Polls are bounded by spin_limit and the wait timeout.
+template <int NS>
 __global__ void __launch_bounds__(128) merge_tagged_kernel(const MergeArgs a) {
   __shared__ int s_id[4][kTopK];
   __shared__ float s_sc[4][kTopK];
@@ -854,15 +858,14 @@ __global__ void __launch_bounds__(128) merge_tagged_kernel(const MergeArgs a) {
   if (item >= a.T * hpr) return;
   const int t = item / hpr, hl = item % hpr;
   const int nvp = a.nvp[t];
-  const int ws = a.world_size;
+  constexpr int ws = NS;
 
-  int ids[4];
-  float scs[4];
+  int ids[NS];
+  float scs[NS];
 #pragma unroll
-  for (int s = 0; s < 4; ++s) {
+  for (int s = 0; s < NS; ++s) {
     ids[s] = -1;
     scs[s] = -INFINITY;
-    if (s >= ws) continue;
     const long long r = (((long long)a.slot * ws + s) * hpr + hl) * a.capacity + t;
     int *e = a.expected + r;  // same [slot][src][hl][t] layout as the rows
     unsigned want = 0;
@@ -894,12 +897,13 @@ __global__ void __launch_bounds__(128) merge_tagged_kernel(const MergeArgs a) {
       ids[s] = (int)idw;
     }
   }
-  merge_finish(a, lane, t, hl, nvp, ids, scs, s_id[warp], s_sc[warp]);
+  merge_finish<NS>(a, lane, t, hl, nvp, ids, scs, s_id[warp], s_sc[warp]);
 }
 
 // Owner merge of received prefill carrier rows [ws][T][hpr][32]: every
 // source row is there already (the caller's exchange has completed), so
 // there is nothing to wait for.
+template <int NS>
 __global__ void __launch_bounds__(128) merge_carrier_kernel(const MergeArgs a) {
   __shared__ int s_id[4][kTopK];
   __shared__ float s_sc[4][kTopK];
@@ -910,19 +914,19 @@ __global__ void __launch_bounds__(128) merge_carrier_kernel(const MergeArgs a) {
   if (item >= a.T * hpr) return;
   const int t = item / hpr, hl = item % hpr;
   const int nvp = a.nvp[t];
-  int ids[4];
-  float scs[4];
+  int ids[NS];
+  float scs[NS];
 #pragma unroll
-  for (int s = 0; s < 4; ++s) {
+  for (int s = 0; s < NS; ++s) {
     ids[s] = -1;
     scs[s] = -INFINITY;
-    if (s < a.world_size && lane < kTopK) {
+    if (lane < kTopK) {
       const int *row = a.received + (((long long)s * a.T + t) * hpr + hl) * 32;
       scs[s] = __int_as_float(row[lane]);
       ids[s] = row[kTopK + lane];
     }
   }
-  merge_finish(a, lane, t, hl, nvp, ids, scs, s_id[warp], s_sc[warp]);
+  merge_finish<NS>(a, lane, t, hl, nvp, ids, scs, s_id[warp], s_sc[warp]);
 }
 
 }  // namespace
@@ -984,19 +988,33 @@ cudaError_t launch_select(const SelectArgs &a, int mode, int sm_count, cudaStrea
   }
 }
 
-cudaError_t launch_merge_carrier(const MergeArgs &a, cudaStream_t stream) {
+// Merge kernels are compiled per world size (1, 2 or 4 sources).
+template <int NS>
+void launch_merge_ns(const MergeArgs &a, int kind, int grid, cudaStream_t stream) {
+  if (kind == 2) merge_carrier_kernel<NS><<<grid, 128, 0, stream>>>(a);
+  else if (kind == 1) merge_tagged_kernel<NS><<<grid, 128, 0, stream>>>(a);
+  else merge_kernel<NS><<<grid, 128, 0, stream>>>(a);
+}
+
+cudaError_t launch_merge_kind(const MergeArgs &a, int kind, cudaStream_t stream) {
   const int items = a.T * a.heads_per_rank;
   if (items == 0) return cudaSuccess;
-  merge_carrier_kernel<<<(items + 3) / 4, 128, 0, stream>>>(a);
+  const int grid = (items + 3) / 4;
+  switch (a.world_size) {
+    case 1: launch_merge_ns<1>(a, kind, grid, stream); break;
+    case 2: launch_merge_ns<2>(a, kind, grid, stream); break;
+    case 4: launch_merge_ns<4>(a, kind, grid, stream); break;
+    default: return cudaErrorInvalidValue;
+  }
   return cudaGetLastError();
 }
 
+cudaError_t launch_merge_carrier(const MergeArgs &a, cudaStream_t stream) {
+  return launch_merge_kind(a, 2, stream);
+}
+
 cudaError_t launch_merge(const MergeArgs &a, bool tagged, cudaStream_t stream) {
-  const int items = a.T * a.heads_per_rank;
-  if (items == 0) return cudaSuccess;
-  if (tagged) merge_tagged_kernel<<<(items + 3) / 4, 128, 0, stream>>>(a);
-  else merge_kernel<<<(items + 3) / 4, 128, 0, stream>>>(a);
-  return cudaGetLastError();
+  return launch_merge_kind(a, tagged ? 1 : 0, stream);
 }
 
 }  // namespace icp
