@@ -126,7 +126,8 @@ __device__ __forceinline__ void emit_row(const SelectArgs &a, int lane, int row,
 // rows: kRowWarps warps per row, each taking the top m of its share, then
 // the top m of their lists.  A warp takes the top m of its columns so:
 //   1. every lane scans its strided float4s (or elements), keeps its best key
-//      and records each float4's largest value in shared memory; the first
+//      (the vector kernels keep only its score: step 2 needs no more) and
+//      records each float4's largest value in shared memory; the first
 //      batch of loads is issued before num_valid_pages is known;
 //   2. tau = a lower bound of the m-th largest lane best (rounds of a warp
 //      max on the score half); only lanes whose best reaches tau can hold
@@ -212,7 +213,8 @@ __device__ __forceinline__ Forced forced_ids(const SelectArgs &a, const float *s
 __device__ __forceinline__ int free_lo(const SelectArgs &a) {
   const int scale = a.index_scale, off = a.index_offset;
   const int d = a.init_blocks - off;
-  return d <= 0 ? 0 : min((d + scale - 1) / scale, a.K);
+  if (d <= 0) return 0;
+  return min(scale == 1 ? d : (d + scale - 1) / scale, a.K);
 }
 
 // Free columns of a row: ids in [init, nvp - local) when nvp > 16, else none.
@@ -222,7 +224,8 @@ __device__ __forceinline__ void free_range(const SelectArgs &a, int nvp, int &c_
   c_hi = 0;
   if (nvp > kTopK) {
     const int id_hi = nvp - a.local_blocks;
-    c_hi = id_hi - off <= 0 ? 0 : (id_hi - off + scale - 1) / scale;
+    const int d = id_hi - off;
+    c_hi = d <= 0 ? 0 : (scale == 1 ? d : (d + scale - 1) / scale);
     c_hi = min(c_hi, a.K);
     c_lo = min(free_lo(a), c_hi);
   }
@@ -342,9 +345,12 @@ __device__ __forceinline__ int warp_top_m_vec(const float *src, float4 (&x)[kChu
   const float4 *r4 = reinterpret_cast<const float4 *>(src);
   const int f_lo = c_lo >> 2, f_hi = (c_hi + 3) >> 2;
   const int f_first = f_lo + first;
-  // 1. scan: best key, and every chunk's largest value into cm
-  float best = 0.0f;
-  int bc = -1;
+  // 1. scan: the lane's largest score in the range (tau only needs the
+  //    score half of the lane's best key), and every chunk's largest value
+  //    into cm; only the range's first and last float4 can hold columns
+  //    outside it, and every float4 of [f_lo, f_hi) holds one inside
+  float best = -INFINITY;
+  const bool has = c_lo < c_hi && f_first < f_hi;
   int nj = 0;
   for (int f0 = f_first; f0 < f_hi; f0 += stride * kChunk) {
     if (f0 != f_first) load_batch(r4, f0, stride, f_hi, x);
@@ -354,21 +360,20 @@ __device__ __forceinline__ int warp_top_m_vec(const float *src, float4 (&x)[kChu
       if (f >= f_hi) break;
       const float m4 = fmaxf(fmaxf(x[u].x, x[u].y), fmaxf(x[u].z, x[u].w));
       w.cm[32 * nj++] = m4;
-      if (bc < 0 || m4 > best) {
+      if (f == f_lo || f == f_hi - 1) {
         const float vv[4] = {x[u].x, x[u].y, x[u].z, x[u].w};
 #pragma unroll
         for (int k = 0; k < 4; ++k) {
           const int c = 4 * f + k;
-          if ((unsigned)(c - c_lo) < (unsigned)(c_hi - c_lo) && (bc < 0 || vv[k] > best)) {
-            best = vv[k];
-            bc = c;
-          }
+          if ((unsigned)(c - c_lo) < (unsigned)(c_hi - c_lo)) best = fmaxf(best, vv[k]);
         }
+      } else {
+        best = fmaxf(best, m4);
       }
     }
   }
   // 2. tau
-  const unsigned long long tm = bc < 0 ? 0ull : make_key(best, bc * scale + off);
+  const unsigned long long tm = has ? (unsigned long long)ord_float(best) << 32 : 0ull;
   const unsigned long long tau = tau_lower_bound(tm, m);
   if (lane == 0) *w.nc = 0;
   __syncwarp();
@@ -494,22 +499,22 @@ __global__ void __launch_bounds__(32 * kSelWarps, 8) select_short_kernel(const S
     const int m = kTopK - f.nf;
     int c_lo, c_hi;
     free_range(a, nvp, c_lo, c_hi);
-    // best key of the lane's columns 4 (lane + 32 u) + k, ascending
-    float best = 0.0f;
-    int bc = -1;
+    // the lane's largest score among its free columns 4 (lane + 32 u) + k
+    // (tau only needs the score half of the lane's best key)
+    float best = -INFINITY;
+    bool has = false;
 #pragma unroll
     for (int u = 0; u < kShortF4; ++u) {
       const float vv[4] = {cur[u].x, cur[u].y, cur[u].z, cur[u].w};
 #pragma unroll
       for (int k = 0; k < 4; ++k) {
         const int c = 4 * (lane + 32 * u) + k;
-        if ((unsigned)(c - c_lo) < (unsigned)(c_hi - c_lo) && (bc < 0 || vv[k] > best)) {
-          best = vv[k];
-          bc = c;
-        }
+        const bool in = (unsigned)(c - c_lo) < (unsigned)(c_hi - c_lo);
+        best = fmaxf(best, in ? vv[k] : -INFINITY);
+        has |= in;
       }
     }
-    const unsigned long long tm = bc < 0 ? 0ull : make_key(best, bc * scale + off);
+    const unsigned long long tm = has ? (unsigned long long)ord_float(best) << 32 : 0ull;
     const unsigned long long tau = tau_lower_bound(tm, m);
     if (lane == 0) *ws.nc = 0;
     __syncwarp();
