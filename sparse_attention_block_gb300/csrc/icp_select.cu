@@ -377,8 +377,24 @@ __device__ __forceinline__ int warp_top_m_vec(const float *src, float4 (&x)[kChu
   const unsigned long long tau = tau_lower_bound(tm, m);
   if (lane == 0) *w.nc = 0;
   __syncwarp();
-  // 3. re-read the chunks whose maximum reaches tau's score, four at a time
-  if (tm != 0ull && tm >= tau) {
+  // 3. the chunks whose maximum reaches tau's score offer their keys: from
+  //    x when the lane's chunks all came in the first batch (x still holds
+  //    them), else re-read four at a time
+  if (tm != 0ull && tm >= tau && nj <= kChunk) {
+    const float ts = (tau >> 32) == 0 ? -INFINITY : unord_float((uint32_t)(tau >> 32));
+#pragma unroll
+    for (int u = 0; u < kChunk; ++u) {
+      if (u >= nj) break;
+      if (!(w.cm[32 * u] >= ts)) continue;
+      const int f = f_first + stride * u;
+      const float vv[4] = {x[u].x, x[u].y, x[u].z, x[u].w};
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        const int c = 4 * f + k;
+        if ((unsigned)(c - c_lo) < (unsigned)(c_hi - c_lo)) offer_key(vv[k], c, ts, tau, scale, off, w);
+      }
+    }
+  } else if (tm != 0ull && tm >= tau) {
     const float ts = (tau >> 32) == 0 ? -INFINITY : unord_float((uint32_t)(tau >> 32));
     unsigned mask = 0;
     for (int j = 0; j < nj; ++j)
