@@ -637,7 +637,7 @@ def workload_config(name, bench):
         return {"workload": spec.description, "batch": spec.batch, "T": bench.T,
                 "cols": bench.cols, "page_size": spec.page_size, "world_size": 1,
                 "chunk_tokens": spec.decode_query_len, "index_k_bytes_per_step": bench.kbytes,
-                "l2": "index-K cache smaller than L2 (re-read from L2 by every 32-token record)",
+                "l2": "index-K cache smaller than L2 (re-read from L2 by every 64-token record)",
                 "step": "icp_prefill_plan -> icp_prefill_score -> icp_prefill_select -> "
                         "icp_prefill_merge, replayed as a CUDA graph"}
     if name == "select":

@@ -304,15 +304,15 @@ int icp_score_select_noalloc(const uint8_t *index_q, const uint8_t *index_k, int
 
 /*
  * int32 words of a prefill plan for a window of T tokens from `batch`
- * requests: room for ceil(T / 32) + batch records of 8 ints plus an 8-int
+ * requests: room for ceil(T / 64) + batch records of 8 ints plus an 8-int
  * header.  Returns -1 when batch or T is negative or the records would
  * exceed ICP_MAX_BATCH.  Host only.
  */
 int64_t icp_prefill_plan_words(int batch, int T);
 
 /*
- * prefill_window_plan: cuts every request's chunk into records of at most 32
- * consecutive tokens, 128 query rows each (one kernel, no host
+ * prefill_window_plan: cuts every request's chunk into records of at most 64
+ * consecutive tokens, 256 query rows each (one kernel, no host
  * synchronisation).
  *   qo_indptr int32 [batch + 1], seq_lens int32 [batch] (each request's
  *   length after the window's tokens), both device memory.

@@ -479,7 +479,7 @@ int icp_prefill_score(const uint8_t *index_q, const uint8_t *index_k, int64_t nu
   CUtensorMap tmk, tmq;
   st = encode_rows(&tmk, index_k, (uint64_t)num_pages * a.g.rows_per_page, (uint32_t)a.g.R);
   if (st != ICP_OK) return st;
-  // one box of a record's 4 * 32 query rows
+  // one box of a record's 4 * 64 query rows
   st = encode_rows(&tmq, index_q, (uint64_t)T * ICP_HEADS, (uint32_t)(4 * icp::kPlanTokens));
   if (st != ICP_OK) return st;
   return to_status(icp::launch_score(tmk, tmq, a, sms, static_cast<cudaStream_t>(stream)));

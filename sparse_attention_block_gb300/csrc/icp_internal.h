@@ -43,7 +43,7 @@ struct ScoreArgs {
   // capacity and *vcount the records in use
   const int32_t *vreq;
   const int32_t *vcount;
-  int wide;  // prefill scorer: 128 distinct query rows per request (records of <= 32 tokens)
+  int wide;  // prefill scorer: 256 distinct query rows per request (records of <= 64 tokens)
 };
 
 // Prefill plan: word 0 = records in use; records from word kPlanHeaderInts,
@@ -52,7 +52,7 @@ struct ScoreArgs {
 // seq_len, 0, 0, 0}.
 constexpr int kPlanHeaderInts = 8;
 constexpr int kPlanRecordInts = 8;
-constexpr int kPlanTokens = 32;  // tokens per record: 4 * 32 = 128 query rows, one MMA tile
+constexpr int kPlanTokens = 64;  // tokens per record: 4 * 64 = 256 query rows, two MMA row halves
 
 struct SelectArgs {
   const float *scores;

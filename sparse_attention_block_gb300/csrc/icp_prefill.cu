@@ -5,8 +5,8 @@
 // n_b = qo_indptr[b+1] - qo_indptr[b] tokens (window tokens qo_indptr[b] ..
 // qo_indptr[b+1] - 1), token j at position seq_len_b - n_b + j: the decode
 // placement with a per-request query length.  The plan cuts every chunk into
-// records of at most kPlanTokens (32) consecutive tokens, 128 query rows: one
-// MMA tile of distinct rows for the prefill scorer.  A record is a request of
+// records of at most kPlanTokens (64) consecutive tokens, 256 query rows: two
+// 128-row MMA operands of distinct rows for the prefill scorer.  A record is a request of
 // its own for the scorer: the request's block-table row, the record's tokens
 // as its queries, and seq_len = its last position + 1, so the causal mask
 // and the key stream are the decode ones.  The scorer writes each record's

@@ -47,6 +47,10 @@ constexpr int kAcc = 4;                // one accumulator per epilogue warp
 constexpr int kTileBytes = 128 * 128;  // 128 K rows x 128 fp8
 constexpr int kQRows = 32;             // query rows staged per request (4 * dql <= 32)
 constexpr int kQBytes = 4 * kQRows * 128;  // four copies -> the 128-row A operand
+// prefill: a plan record's 4 * kPlanTokens distinct query rows, one TMA box
+// that holds two 128-row A operands
+constexpr int kQBytesWide = 4 * kPlanTokens * 128;
+static_assert(4 * kPlanTokens == 256, "a record's query rows are two 128-row operands");
 constexpr int kThreads = 192;
 // prefill scorer: two sets of four epilogue warps take alternate tiles
 constexpr int kEpiSetsWide = 2;
@@ -60,19 +64,25 @@ constexpr uint32_t kTmemCols = kAcc * kAccCols;
 constexpr int kNumBars = 2 * kStages + 2 * kAcc + 4 + 1;
 
 // Shared-memory carve-up (offsets from a 1024-byte aligned base).
+// The prefill scorer's two query slots are twice as large.
 constexpr uint32_t kOffStages = 0;
-constexpr uint32_t kOffQ = kOffStages + kStages * kTileBytes;
-constexpr uint32_t kOffBars = kOffQ + 2 * kQBytes;
-constexpr uint32_t kOffMisc = kOffBars + ((kNumBars * 8 + 127) / 128) * 128;
-constexpr uint32_t kOffLists = kOffMisc + 128;  // fused only
+template <bool WIDE>
+struct Layout {
+  static constexpr uint32_t q_bytes = WIDE ? kQBytesWide : kQBytes;
+  static constexpr uint32_t off_q = kOffStages + kStages * kTileBytes;
+  static constexpr uint32_t off_bars = off_q + 2 * q_bytes;
+  static constexpr uint32_t off_misc = off_bars + ((kNumBars * 8 + 127) / 128) * 128;
+  static constexpr uint32_t off_lists = off_misc + 128;  // fused only
+};
 // fused epilogue: per warp 16 list keys x 32 lanes (u64) + 16 forced (id, score) x 32 lanes
 constexpr uint32_t kWarpListBytes = 16 * 32 * 8 + 16 * 32 * 8;
 constexpr uint32_t kListBytes = 4 * kWarpListBytes;   // 32 KB
 constexpr uint32_t kFusedExtra = kListBytes;
 
-template <bool FUSED>
+template <bool FUSED, bool WIDE>
 struct PrefixOffset {
-  static constexpr uint32_t value = FUSED ? kOffLists + kFusedExtra : kOffLists;
+  static constexpr uint32_t value =
+      FUSED ? Layout<WIDE>::off_lists + kFusedExtra : Layout<WIDE>::off_lists;
 };
 
 // Walks the CTA's tile range [g0, g1) request by request.
@@ -234,10 +244,10 @@ __device__ __forceinline__ void epilogue_tile(const ScoreArgs &a, uint32_t taddr
 }
 
 // Epilogue of one tile of the prefill scorer for one warp of the set that
-// owns it: lane l holds query row rowq + l of the record (128 distinct rows).
-// A column that reaches past the record's first token is masked with 32-bit
-// compares.  With release, the warp hands the accumulator back once the tile
-// is in registers (the pair's last tile).
+// owns the row half: lane l holds query row rowq + l of the record (up to
+// 256 distinct rows).  A column that reaches past the record's first token
+// is masked with 32-bit compares.  With release, the warp hands the
+// accumulator pair back once its part of the tile is in registers.
 template <int R>
 __device__ __forceinline__ void epilogue_tile_wide(const ScoreArgs &a, uint32_t ta, int lane,
                                                    int rowq, int tok0, int ntok, int tl,
@@ -281,14 +291,14 @@ __device__ __forceinline__ void epilogue_tile_wide(const ScoreArgs &a, uint32_t 
   }
 }
 
-// WIDE: the prefill scorer.  A request (a plan record of up to 32 tokens)
-// stages 128 distinct query rows in one box.  Its tiles go in pairs: two
-// adjacent ring stages form one 256-row B operand and one N = 256 MMA group
-// (N = 128 for a segment's odd last tile) fills one of two 256-column
-// accumulators, pairs alternating.  The epilogue warps form two sets of
-// four, set s finishing tile s of every pair; each warp takes its lane
-// quarter (8 of the tokens) and the accumulator is free again after all
-// eight warps have arrived.
+// WIDE: the prefill scorer.  A request (a plan record of up to 64 tokens)
+// stages its 256 distinct query rows in one box: two 128-row A operands.
+// Every 128-key tile feeds both (two N = 128 MMA groups, the second only
+// when the record has more than 32 tokens) into one of two accumulator
+// pairs, tiles alternating, so each key byte read serves 256 query rows.
+// The epilogue warps form two sets of four, set s finishing row half s of
+// every tile; each warp takes its lane quarter (8 of the half's 32 tokens)
+// and the accumulator pair is free again after all eight warps have arrived.
 template <bool FUSED, bool WIDE>
 __global__ void __launch_bounds__(BlockThreads<WIDE>::value, 1)
 score_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmq,
@@ -299,21 +309,22 @@ score_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CU
   uint8_t *gb = smem_raw + (sb - raw);
 
   constexpr int NT = BlockThreads<WIDE>::value;
+  using L = Layout<WIDE>;
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const ScoreGeom g = a.g;
 
-  auto bar_full = [&](int s) { return sb + kOffBars + 8u * s; };
-  auto bar_empty = [&](int s) { return sb + kOffBars + 8u * (kStages + s); };
-  auto bar_tfull = [&](int i) { return sb + kOffBars + 8u * (2 * kStages + i); };
-  auto bar_tempty = [&](int i) { return sb + kOffBars + 8u * (2 * kStages + kAcc + i); };
-  auto bar_qfull = [&](int i) { return sb + kOffBars + 8u * (2 * kStages + 2 * kAcc + i); };
-  auto bar_qempty = [&](int i) { return sb + kOffBars + 8u * (2 * kStages + 2 * kAcc + 2 + i); };
-  const uint32_t bar_done = sb + kOffBars + 8u * (2 * kStages + 2 * kAcc + 4);
+  auto bar_full = [&](int s) { return sb + L::off_bars + 8u * s; };
+  auto bar_empty = [&](int s) { return sb + L::off_bars + 8u * (kStages + s); };
+  auto bar_tfull = [&](int i) { return sb + L::off_bars + 8u * (2 * kStages + i); };
+  auto bar_tempty = [&](int i) { return sb + L::off_bars + 8u * (2 * kStages + kAcc + i); };
+  auto bar_qfull = [&](int i) { return sb + L::off_bars + 8u * (2 * kStages + 2 * kAcc + i); };
+  auto bar_qempty = [&](int i) { return sb + L::off_bars + 8u * (2 * kStages + 2 * kAcc + 2 + i); };
+  const uint32_t bar_done = sb + L::off_bars + 8u * (2 * kStages + 2 * kAcc + 4);
 
   // [0] TMEM base, [1] abort flag
-  volatile int *misc = reinterpret_cast<volatile int *>(gb + kOffMisc);
-  int *prefix = reinterpret_cast<int *>(gb + PrefixOffset<FUSED>::value);
+  volatile int *misc = reinterpret_cast<volatile int *>(gb + L::off_misc);
+  int *prefix = reinterpret_cast<int *>(gb + PrefixOffset<FUSED, WIDE>::value);
   int *partial = prefix + a.batch + 1;  // NT / 32 scratch ints
   const int nbatch = req_count(a);      // <= a.batch
 
@@ -338,7 +349,7 @@ score_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CU
     prefetch_tensormap(&tmk);
     prefetch_tensormap(&tmq);
   }
-  if (warp == 1) tmem_alloc(sb + kOffMisc, kTmemCols);
+  if (warp == 1) tmem_alloc(sb + L::off_misc, kTmemCols);
 
   // Tiles per request and their prefix sums (chunked block scan).
   {
@@ -423,12 +434,12 @@ score_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CU
       ok = __shfl_sync(0xFFFFFFFFu, ok, 0) != 0;
       if (!ok) break;
       if (lane == 0) {
-        mbar_arrive_expect_tx(bar_qfull(qslot), (uint32_t)kQBytes);
+        mbar_arrive_expect_tx(bar_qfull(qslot), L::q_bytes);
         if constexpr (WIDE) {
-          tma_load_2d(sb + kOffQ + qslot * kQBytes, &tmq, 0, rv.tok0 * 4, bar_qfull(qslot));
+          tma_load_2d(sb + L::off_q + qslot * L::q_bytes, &tmq, 0, rv.tok0 * 4, bar_qfull(qslot));
         } else {
           for (int r = 0; r < 4; ++r)
-            tma_load_2d(sb + kOffQ + qslot * kQBytes + r * kQRows * 128, &tmq, 0, rv.tok0 * 4,
+            tma_load_2d(sb + L::off_q + qslot * L::q_bytes + r * kQRows * 128, &tmq, 0, rv.tok0 * 4,
                         bar_qfull(qslot));
         }
       }
@@ -449,28 +460,17 @@ score_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CU
           pg_nxt = (grp + 32 + lane < cend) ? btrow[page_slot_of(grp + 32 + lane, g.split)] : 0;
         }
         const int ncol = min(g.cpt, cend - c0);
-        // WIDE: tiles go in pairs (t0, t0 + 1), ... into slots of two
-        // adjacent stages, one barrier per slot; j is the tile in its pair
-        const int j = WIDE ? ((tl - t0) & 1) : 0;
-        if (j == 0) {
-          if (lane == 0) ok = mbar_wait(bar_empty(stage), sphase ^ 1u, abort_flag);
-          ok = __shfl_sync(0xFFFFFFFFu, ok, 0) != 0;
-          if (!ok) break;
-        }
+        if (lane == 0) ok = mbar_wait(bar_empty(stage), sphase ^ 1u, abort_flag);
+        ok = __shfl_sync(0xFFFFFFFFu, ok, 0) != 0;
+        if (!ok) break;
         const int p0 = __shfl_sync(0xFFFFFFFFu, pg_cur, (c0 - grp) & 31);
         const int p1 = __shfl_sync(0xFFFFFFFFu, pg_cur, (c0 - grp + 1) & 31);
         const int p2 = __shfl_sync(0xFFFFFFFFu, pg_cur, (c0 - grp + 2) & 31);
         const int p3 = __shfl_sync(0xFFFFFFFFu, pg_cur, (c0 - grp + 3) & 31);
         if (lane == 0) {
           const uint32_t bar = bar_full(stage);
-          if (j == 0) {
-            uint32_t bytes = (uint32_t)(ncol * g.R * 128);
-            if (WIDE && tl + 1 < t1)
-              bytes += (uint32_t)(min(g.cpt, cend - c0 - g.cpt) * g.R * 128);
-            mbar_arrive_expect_tx(bar, bytes);
-          }
-          const uint32_t dst = WIDE ? sb + kOffStages + (stage * 2 + j) * kTileBytes
-                                    : sb + kOffStages + stage * kTileBytes;
+          mbar_arrive_expect_tx(bar, (uint32_t)(ncol * g.R * 128));
+          const uint32_t dst = sb + kOffStages + stage * kTileBytes;
           for (int k = 0; k < ncol; ++k) {
             const int c = c0 + k;
             const int pg = k == 0 ? p0 : (k == 1 ? p1 : (k == 2 ? p2 : p3));
@@ -479,18 +479,16 @@ score_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CU
           }
         }
         __syncwarp();
-        if (!WIDE || j == 1 || tl + 1 == t1) {
-          ++issued;
-          if (++stage == (WIDE ? kStages / 2 : kStages)) {
-            stage = 0;
-            sphase ^= 1u;
-          }
+        ++issued;
+        if (++stage == kStages) {
+          stage = 0;
+          sphase ^= 1u;
         }
       }
     }
     if (*abort_flag && lane == 0) {
       // let copies still in flight land before the CTA exits
-      constexpr int nst = WIDE ? kStages / 2 : kStages;
+      constexpr int nst = kStages;
       const long long first = issued > nst ? issued - nst : 0;
       for (long long n = first; n < issued; ++n)
         mbar_wait_drain(bar_full((int)(n % nst)), (uint32_t)((n / nst) & 1));
@@ -513,26 +511,28 @@ score_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CU
       while (ok && walk.next(b, t0, t1)) {
         ok = mbar_wait(bar_qfull(qslot), qslot ? qph1 : qph0, abort_flag);
         if (!ok) break;
-        const uint32_t qaddr = sb + kOffQ + qslot * kQBytes;
+        const uint32_t qaddr = sb + L::off_q + qslot * L::q_bytes;
         if constexpr (WIDE) {
-          // a pair of tiles is one 256-row B operand (N = 256; N = 128 for a
-          // segment's odd last tile) into one of two 256-column accumulators
-          for (int tl = t0; tl < t1; tl += 2) {
-            const int np = min(2, t1 - tl);
+          // every tile feeds the record's row halves (the second only past
+          // 32 tokens): N = 128 MMA groups into one of two accumulator pairs
+          const int nh = req_view(a, b).ntok > kPlanTokens / 2 ? 2 : 1;
+          for (int tl = t0; tl < t1; ++tl) {
             ok = mbar_wait(bar_full(stage), sphase, abort_flag) &&
                  mbar_wait(bar_tempty(acc), aphase ^ 1u, abort_flag);
             if (!ok) break;
             tc_fence_after();
-            const uint32_t kaddr = sb + kOffStages + stage * 2 * kTileBytes;
-            const uint32_t d = tmem_base + (uint32_t)acc * (2 * kAccCols);
-            const uint32_t id = np == 2 ? idesc_f8_f32(128, 2 * (int)kAccCols) : idesc;
+            const uint32_t kaddr = sb + kOffStages + stage * kTileBytes;
+            for (int h = 0; h < nh; ++h) {
+              const uint32_t d = tmem_base + (uint32_t)acc * (2 * kAccCols) + (uint32_t)h * kAccCols;
+              const uint32_t qh = qaddr + (uint32_t)h * (128 * 128);
 #pragma unroll
-            for (int k = 0; k < 4; ++k)
-              mma_f8(d, smem_desc_sw128(qaddr + 32 * k), smem_desc_sw128(kaddr + 32 * k), id,
-                     k > 0 ? 1u : 0u);
+              for (int k = 0; k < 4; ++k)
+                mma_f8(d, smem_desc_sw128(qh + 32 * k), smem_desc_sw128(kaddr + 32 * k), idesc,
+                       k > 0 ? 1u : 0u);
+            }
             mma_commit(bar_empty(stage));
             mma_commit(bar_tfull(acc));
-            if (++stage == kStages / 2) {
+            if (++stage == kStages) {
               stage = 0;
               sphase ^= 1u;
             }
@@ -615,13 +615,13 @@ score_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CU
     }
     uint32_t aphase = 0;
     int idx = 0;
-    int pi = 0;          // WIDE: the CTA's tile-pair counter
+    int pi = 0;          // WIDE: the CTA's tile counter
     const uint32_t taddr = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)e * kAccCols;
     unsigned long long *lk = nullptr;
     int *lfid = nullptr;
     float *lfsc = nullptr;
     if constexpr (FUSED) {
-      uint8_t *wl = gb + kOffLists + e * kWarpListBytes;
+      uint8_t *wl = gb + L::off_lists + e * kWarpListBytes;
       lk = reinterpret_cast<unsigned long long *>(wl);
       lfid = reinterpret_cast<int *>(wl + 16 * 32 * 8);
       lfsc = reinterpret_cast<float *>(wl + 16 * 32 * 8 + 16 * 32 * 4);
@@ -645,32 +645,33 @@ score_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CU
         for (int j = 0; j < kTopK; ++j) lk[j * 32 + lane] = 0ull;
       }
       if constexpr (WIDE) {
-        // every pair: set s finishes the pair's tile s, this warp's lane
-        // quarter (tokens 8 q .. 8 q + 7); pi counts the CTA's pairs as the
-        // MMA thread does, pair pi sits in accumulator pi & 1
+        // every tile: set s finishes row half s, this warp's lane quarter
+        // (tokens 32 s + 8 q .. 32 s + 8 q + 7); pi counts the CTA's tiles
+        // as the MMA thread does, tile pi sits in accumulator pair pi & 1
         const int set = (warp - 2) >> 2;
-        for (int tl = t0; ok && tl < t1; tl += 2, ++pi) {
-          const int np = min(2, t1 - tl);
+        const int nh = rv.ntok > kPlanTokens / 2 ? 2 : 1;
+        for (int tl = t0; ok && tl < t1; ++tl, ++pi) {
           const int acc = pi & 1;
           const uint32_t wph = (uint32_t)(pi >> 1) & 1u;
           if (lane == 0) ok = mbar_wait(bar_tfull(acc), wph, abort_flag);
           ok = __shfl_sync(0xFFFFFFFFu, ok, 0) != 0;
           if (!ok) break;
           tc_fence_after();
-          if (set < np) {
+          if (set < nh) {
             const uint32_t tj = tmem_base + ((uint32_t)(q * 32) << 16) +
                                 (uint32_t)acc * (2 * kAccCols) + (uint32_t)set * kAccCols;
+            const int rowq = set * 128 + q * 32;
             if (g.R == 128)
-              epilogue_tile_wide<128>(a, tj, lane, q * 32, rv.tok0, rv.ntok, tl + set, nunits,
-                                      seq_len, bar_tempty(acc), true);
+              epilogue_tile_wide<128>(a, tj, lane, rowq, rv.tok0, rv.ntok, tl, nunits, seq_len,
+                                      bar_tempty(acc), true);
             else if (g.R == 64)
-              epilogue_tile_wide<64>(a, tj, lane, q * 32, rv.tok0, rv.ntok, tl + set, nunits,
-                                     seq_len, bar_tempty(acc), true);
+              epilogue_tile_wide<64>(a, tj, lane, rowq, rv.tok0, rv.ntok, tl, nunits, seq_len,
+                                     bar_tempty(acc), true);
             else
-              epilogue_tile_wide<32>(a, tj, lane, q * 32, rv.tok0, rv.ntok, tl + set, nunits,
-                                     seq_len, bar_tempty(acc), true);
+              epilogue_tile_wide<32>(a, tj, lane, rowq, rv.tok0, rv.ntok, tl, nunits, seq_len,
+                                     bar_tempty(acc), true);
           } else {
-            // a segment's odd last tile: nothing for this set to read
+            // a record of at most 32 tokens: nothing for this set to read
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(bar_tempty(acc));
@@ -730,10 +731,11 @@ score_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CU
   if (threadIdx.x == 0 && *abort_flag && a.errors) atomicAdd(a.errors, 1);
 }
 
-template <bool FUSED>
+template <bool FUSED, bool WIDE = false>
 size_t smem_bytes_for(int batch) {
-  static_assert(PrefixOffset<FUSED>::value % 16 == 0, "prefix alignment");
-  return 1024 + PrefixOffset<FUSED>::value + sizeof(int) * (size_t)(batch + 1 + kThreadsWide / 32);
+  static_assert(PrefixOffset<FUSED, WIDE>::value % 16 == 0, "prefix alignment");
+  return 1024 + PrefixOffset<FUSED, WIDE>::value +
+         sizeof(int) * (size_t)(batch + 1 + kThreadsWide / 32);
 }
 
 }  // namespace
@@ -748,7 +750,7 @@ cudaError_t score_prepare(int device) {
                                        (int)smem_bytes_for<false>(kMaxBatchDevice));
   if (e != cudaSuccess) return e;
   e = cudaFuncSetAttribute(score_kernel<false, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           (int)smem_bytes_for<false>(kMaxBatchDevice));
+                           (int)smem_bytes_for<false, true>(kMaxBatchDevice));
   if (e != cudaSuccess) return e;
   return cudaFuncSetAttribute(score_kernel<true, false>,
                               cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -758,7 +760,7 @@ cudaError_t score_prepare(int device) {
 cudaError_t launch_score(const CUtensorMap &tmk, const CUtensorMap &tmq, const ScoreArgs &a,
                          int grid, cudaStream_t stream) {
   if (a.wide) {
-    score_kernel<false, true><<<grid, kThreadsWide, smem_bytes_for<false>(a.batch), stream>>>(
+    score_kernel<false, true><<<grid, kThreadsWide, smem_bytes_for<false, true>(a.batch), stream>>>(
         tmk, tmq, a);
     return cudaGetLastError();
   }

@@ -122,17 +122,17 @@ def test_fused_workspace_size_and_checks(lib):
 def test_prefill_sizes_and_checks(lib):
     lib.icp_prefill_plan_words.restype = ctypes.c_int64
     lib.icp_prefill_plan_words.argtypes = [ctypes.c_int, ctypes.c_int]
-    # ceil(T / 32) + batch records of 8 ints, plus an 8-int header
-    assert lib.icp_prefill_plan_words(4, 8192) == 8 + 8 * (256 + 4)
+    # ceil(T / 64) + batch records of 8 ints, plus an 8-int header
+    assert lib.icp_prefill_plan_words(4, 8192) == 8 + 8 * (128 + 4)   # 64-token records
     assert lib.icp_prefill_plan_words(3, 1) == 8 + 8 * 4
     assert lib.icp_prefill_plan_words(-1, 8) == -1
-    assert lib.icp_prefill_plan_words(1, 4096 * 32) == -1   # more than 4096 records
+    assert lib.icp_prefill_plan_words(1, 4096 * 64) == -1   # more than 4096 records
     P = ctypes.c_void_p
     buf = ctypes.create_string_buffer(1 << 16)
     a = ctypes.cast(ctypes.addressof(buf) + (-ctypes.addressof(buf) % 256), P)
     INVALID = 1
     lib.icp_prefill_plan.argtypes = [P, P, ctypes.c_int, ctypes.c_int, P, ctypes.c_int64, P, P]
-    assert lib.icp_prefill_plan(a, a, 2, 64, a, 8 + 8 * 3, None, None) == INVALID  # too small
+    assert lib.icp_prefill_plan(a, a, 2, 65, a, 8 + 8 * 3, None, None) == INVALID  # too small
     assert lib.icp_prefill_plan(a, a, 2, 64, None, 8 + 8 * 4, None, None) == INVALID
     odd = ctypes.c_void_p(a.value + 4)                    # the plan is read as int4
     assert lib.icp_prefill_plan(a, a, 2, 64, odd, 8 + 8 * 4, None, None) == INVALID

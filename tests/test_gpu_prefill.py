@@ -45,8 +45,9 @@ def _gpu_plane(q, k, bt, sl, qo, *, cols, rank, world_size, page_size, errors=No
     return out, plan
 
 
-# chunks below, at and across the 32-token records, an empty one, a whole prompt
-RAGGED = ([1000, 2500, 129, 300, 40, 9000, 5000], [1, 17, 129, 32, 0, 33, 100])
+# chunks below, at and across the 64-token records (and across their 32-token
+# row halves), an empty one, a whole prompt
+RAGGED = ([1000, 2500, 129, 300, 40, 9000, 5000], [1, 17, 129, 64, 0, 65, 100])
 
 
 @pytest.mark.parametrize("page_size,ws", [(128, 1), (128, 2), (128, 4), (256, 1), (256, 2),
@@ -72,17 +73,18 @@ def test_prefill_plane_ragged_chunks(page_size, ws):
 
 
 def test_plan_records_by_hand():
-    sl = torch.tensor([100, 40, 20], dtype=torch.int32, device="cuda")
-    qo = torch.tensor([0, 70, 70, 73], dtype=torch.int32, device="cuda")   # chunks 70, 0, 3
-    plan = torch.full((icp().icp_prefill_plan_words(3, 73),), -7, dtype=torch.int32,
+    sl = torch.tensor([200, 40, 20], dtype=torch.int32, device="cuda")
+    qo = torch.tensor([0, 150, 150, 153], dtype=torch.int32, device="cuda")  # chunks 150, 0, 3
+    plan = torch.full((icp().icp_prefill_plan_words(3, 153),), -7, dtype=torch.int32,
                       device="cuda")
-    icp().icp_prefill_plan(qo, sl, plan, T=73)
+    icp().icp_prefill_plan(qo, sl, plan, T=153)
     p = plan.cpu().numpy()
     assert p[0] == 4
     recs = p[8:8 + 4 * 8].reshape(4, 8)
-    # {first token, table row, last position + 1, tokens, request seq_len, 0, 0, 0}
-    assert recs.tolist() == [[0, 0, 62, 32, 100, 0, 0, 0], [32, 0, 94, 32, 100, 0, 0, 0],
-                             [64, 0, 100, 6, 100, 0, 0, 0], [70, 2, 20, 3, 20, 0, 0, 0]]
+    # {first token, table row, last position + 1, tokens, request seq_len, 0, 0, 0}:
+    # records of at most 64 tokens; request 0's chunk sits at positions 50..199
+    assert recs.tolist() == [[0, 0, 114, 64, 200, 0, 0, 0], [64, 0, 178, 64, 200, 0, 0, 0],
+                             [128, 0, 200, 22, 200, 0, 0, 0], [150, 2, 20, 3, 20, 0, 0, 0]]
 
 
 def test_invalid_chunk_is_counted_and_its_rows_left_alone():
