@@ -50,7 +50,7 @@ NCU_TRAFFIC = {
     # dram__bytes_read.sum + dram__bytes_write.sum = 278821632 + 3133952 bytes for
     # 278330624 bytes of index-K (first 32 requests of the multitoken workload),
     # see profiles/icp_score_multitoken.md
-    ("multitoken", "2dae2d2342efceae"): (278821632 + 3133952) / 278330624,
+    ("multitoken", "995c3fdf93926a28"): (278835712 + 3142656) / 278330624,
 }
 
 
