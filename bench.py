@@ -299,7 +299,7 @@ class DecodeBench:
                                  rank=rank, world_size=ws, heads_per_rank=self.hpr,
                                  capacity=self.cap, force_begin_blocks=spec.init_blocks,
                                  force_end_blocks=spec.local_blocks, spin_limit=1 << 22,
-                                 index_scale=scale, index_offset=offset)
+                                 index_scale=scale, index_offset=offset, enable_pdl=True)
         for owner in range(ws):
             icp.icp_merge(self.recv[owner], self.nvp, self.out_s[owner], self.out_i[owner],
                           self.errors, T=self.T, slot=slot, world_size=ws,
