@@ -460,17 +460,28 @@ score_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CU
           pg_nxt = (grp + 32 + lane < cend) ? btrow[page_slot_of(grp + 32 + lane, g.split)] : 0;
         }
         const int ncol = min(g.cpt, cend - c0);
-        if (lane == 0) ok = mbar_wait(bar_empty(stage), sphase ^ 1u, abort_flag);
-        ok = __shfl_sync(0xFFFFFFFFu, ok, 0) != 0;
-        if (!ok) break;
+        // WIDE: tiles go in pairs (t0, t0 + 1), ... into slots of two
+        // adjacent stages, one barrier per slot; j is the tile in its pair
+        const int j = WIDE ? ((tl - t0) & 1) : 0;
+        if (j == 0) {
+          if (lane == 0) ok = mbar_wait(bar_empty(stage), sphase ^ 1u, abort_flag);
+          ok = __shfl_sync(0xFFFFFFFFu, ok, 0) != 0;
+          if (!ok) break;
+        }
         const int p0 = __shfl_sync(0xFFFFFFFFu, pg_cur, (c0 - grp) & 31);
         const int p1 = __shfl_sync(0xFFFFFFFFu, pg_cur, (c0 - grp + 1) & 31);
         const int p2 = __shfl_sync(0xFFFFFFFFu, pg_cur, (c0 - grp + 2) & 31);
         const int p3 = __shfl_sync(0xFFFFFFFFu, pg_cur, (c0 - grp + 3) & 31);
         if (lane == 0) {
           const uint32_t bar = bar_full(stage);
-          mbar_arrive_expect_tx(bar, (uint32_t)(ncol * g.R * 128));
-          const uint32_t dst = sb + kOffStages + stage * kTileBytes;
+          if (j == 0) {
+            uint32_t bytes = (uint32_t)(ncol * g.R * 128);
+            if (WIDE && tl + 1 < t1)
+              bytes += (uint32_t)(min(g.cpt, cend - c0 - g.cpt) * g.R * 128);
+            mbar_arrive_expect_tx(bar, bytes);
+          }
+          const uint32_t dst = WIDE ? sb + kOffStages + (stage * 2 + j) * kTileBytes
+                                    : sb + kOffStages + stage * kTileBytes;
           for (int k = 0; k < ncol; ++k) {
             const int c = c0 + k;
             const int pg = k == 0 ? p0 : (k == 1 ? p1 : (k == 2 ? p2 : p3));
@@ -479,16 +490,18 @@ score_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CU
           }
         }
         __syncwarp();
-        ++issued;
-        if (++stage == kStages) {
-          stage = 0;
-          sphase ^= 1u;
+        if (!WIDE || j == 1 || tl + 1 == t1) {
+          ++issued;
+          if (++stage == (WIDE ? kStages / 2 : kStages)) {
+            stage = 0;
+            sphase ^= 1u;
+          }
         }
       }
     }
     if (*abort_flag && lane == 0) {
       // let copies still in flight land before the CTA exits
-      constexpr int nst = kStages;
+      constexpr int nst = WIDE ? kStages / 2 : kStages;
       const long long first = issued > nst ? issued - nst : 0;
       for (long long n = first; n < issued; ++n)
         mbar_wait_drain(bar_full((int)(n % nst)), (uint32_t)((n / nst) & 1));
@@ -513,32 +526,38 @@ score_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CU
         if (!ok) break;
         const uint32_t qaddr = sb + L::off_q + qslot * L::q_bytes;
         if constexpr (WIDE) {
-          // every tile feeds the record's row halves (the second only past
-          // 32 tokens): N = 128 MMA groups into one of two accumulator pairs
+          // a pair of tiles is one 256-row B operand; each of the record's
+          // row halves (the second only past 32 tokens) is one item: an
+          // N = 256 MMA group (N = 128 for a segment's odd last tile) into
+          // one of two 256-column accumulators, items alternating
           const int nh = req_view(a, b).ntok > kPlanTokens / 2 ? 2 : 1;
-          for (int tl = t0; tl < t1; ++tl) {
-            ok = mbar_wait(bar_full(stage), sphase, abort_flag) &&
-                 mbar_wait(bar_tempty(acc), aphase ^ 1u, abort_flag);
+          for (int tl = t0; ok && tl < t1; tl += 2) {
+            const int np = min(2, t1 - tl);
+            ok = mbar_wait(bar_full(stage), sphase, abort_flag);
             if (!ok) break;
-            tc_fence_after();
-            const uint32_t kaddr = sb + kOffStages + stage * kTileBytes;
+            const uint32_t kaddr = sb + kOffStages + stage * 2 * kTileBytes;
+            const uint32_t id = np == 2 ? idesc_f8_f32(128, 2 * (int)kAccCols) : idesc;
             for (int h = 0; h < nh; ++h) {
-              const uint32_t d = tmem_base + (uint32_t)acc * (2 * kAccCols) + (uint32_t)h * kAccCols;
+              ok = mbar_wait(bar_tempty(acc), aphase ^ 1u, abort_flag);
+              if (!ok) break;
+              tc_fence_after();
+              const uint32_t d = tmem_base + (uint32_t)acc * (2 * kAccCols);
               const uint32_t qh = qaddr + (uint32_t)h * (128 * 128);
 #pragma unroll
               for (int k = 0; k < 4; ++k)
-                mma_f8(d, smem_desc_sw128(qh + 32 * k), smem_desc_sw128(kaddr + 32 * k), idesc,
+                mma_f8(d, smem_desc_sw128(qh + 32 * k), smem_desc_sw128(kaddr + 32 * k), id,
                        k > 0 ? 1u : 0u);
+              mma_commit(bar_tfull(acc));
+              if (++acc == 2) {
+                acc = 0;
+                aphase ^= 1u;
+              }
             }
+            if (!ok) break;
             mma_commit(bar_empty(stage));
-            mma_commit(bar_tfull(acc));
-            if (++stage == kStages) {
+            if (++stage == kStages / 2) {
               stage = 0;
               sphase ^= 1u;
-            }
-            if (++acc == 2) {
-              acc = 0;
-              aphase ^= 1u;
             }
           }
         } else {
@@ -615,7 +634,7 @@ score_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CU
     }
     uint32_t aphase = 0;
     int idx = 0;
-    int pi = 0;          // WIDE: the CTA's tile counter
+    int pi = 0;          // WIDE: the CTA's (tile pair, row half) item counter
     const uint32_t taddr = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)e * kAccCols;
     unsigned long long *lk = nullptr;
     int *lfid = nullptr;
@@ -645,36 +664,40 @@ score_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CU
         for (int j = 0; j < kTopK; ++j) lk[j * 32 + lane] = 0ull;
       }
       if constexpr (WIDE) {
-        // every tile: set s finishes row half s, this warp's lane quarter
-        // (tokens 32 s + 8 q .. 32 s + 8 q + 7); pi counts the CTA's tiles
-        // as the MMA thread does, tile pi sits in accumulator pair pi & 1
+        // every (tile pair, row half) item: set s finishes the pair's tile s
+        // for the half's rows, this warp's lane quarter (tokens 32 h + 8 q
+        // .. 32 h + 8 q + 7); pi counts the CTA's items as the MMA thread
+        // does, item pi sits in accumulator pi & 1
         const int set = (warp - 2) >> 2;
         const int nh = rv.ntok > kPlanTokens / 2 ? 2 : 1;
-        for (int tl = t0; ok && tl < t1; ++tl, ++pi) {
-          const int acc = pi & 1;
-          const uint32_t wph = (uint32_t)(pi >> 1) & 1u;
-          if (lane == 0) ok = mbar_wait(bar_tfull(acc), wph, abort_flag);
-          ok = __shfl_sync(0xFFFFFFFFu, ok, 0) != 0;
-          if (!ok) break;
-          tc_fence_after();
-          if (set < nh) {
-            const uint32_t tj = tmem_base + ((uint32_t)(q * 32) << 16) +
-                                (uint32_t)acc * (2 * kAccCols) + (uint32_t)set * kAccCols;
-            const int rowq = set * 128 + q * 32;
-            if (g.R == 128)
-              epilogue_tile_wide<128>(a, tj, lane, rowq, rv.tok0, rv.ntok, tl, nunits, seq_len,
-                                      bar_tempty(acc), true);
-            else if (g.R == 64)
-              epilogue_tile_wide<64>(a, tj, lane, rowq, rv.tok0, rv.ntok, tl, nunits, seq_len,
-                                     bar_tempty(acc), true);
-            else
-              epilogue_tile_wide<32>(a, tj, lane, rowq, rv.tok0, rv.ntok, tl, nunits, seq_len,
-                                     bar_tempty(acc), true);
-          } else {
-            // a record of at most 32 tokens: nothing for this set to read
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(bar_tempty(acc));
+        for (int tl = t0; ok && tl < t1; tl += 2) {
+          const int np = min(2, t1 - tl);
+          for (int h = 0; ok && h < nh; ++h, ++pi) {
+            const int acc = pi & 1;
+            const uint32_t wph = (uint32_t)(pi >> 1) & 1u;
+            if (lane == 0) ok = mbar_wait(bar_tfull(acc), wph, abort_flag);
+            ok = __shfl_sync(0xFFFFFFFFu, ok, 0) != 0;
+            if (!ok) break;
+            tc_fence_after();
+            if (set < np) {
+              const uint32_t tj = tmem_base + ((uint32_t)(q * 32) << 16) +
+                                  (uint32_t)acc * (2 * kAccCols) + (uint32_t)set * kAccCols;
+              const int rowq = h * 128 + q * 32;
+              if (g.R == 128)
+                epilogue_tile_wide<128>(a, tj, lane, rowq, rv.tok0, rv.ntok, tl + set, nunits,
+                                        seq_len, bar_tempty(acc), true);
+              else if (g.R == 64)
+                epilogue_tile_wide<64>(a, tj, lane, rowq, rv.tok0, rv.ntok, tl + set, nunits,
+                                       seq_len, bar_tempty(acc), true);
+              else
+                epilogue_tile_wide<32>(a, tj, lane, rowq, rv.tok0, rv.ntok, tl + set, nunits,
+                                       seq_len, bar_tempty(acc), true);
+            } else {
+              // a segment's odd last tile: nothing for this set to read
+              tc_fence_before();
+              __syncwarp();
+              if (lane == 0) mbar_arrive(bar_tempty(acc));
+            }
           }
         }
       } else {
