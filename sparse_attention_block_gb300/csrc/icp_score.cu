@@ -193,8 +193,7 @@ __device__ __forceinline__ void epilogue_tile(const ScoreArgs &a, uint32_t taddr
                                               float *lfsc) {
   constexpr int CPT = 128 / R;
   float v[128];
-#pragma unroll
-  for (int k = 0; k < 4; ++k) tmem_ld32(taddr + 32u * k, v + 32 * k);
+  tmem_ld128(taddr, v);
   tmem_wait_ld();
   // the accumulator is in registers: hand it back to the MMA warp
   tc_fence_before();
@@ -262,8 +261,7 @@ __device__ __forceinline__ void epilogue_tile_wide(const ScoreArgs &a, uint32_t 
   // the whole tile in registers with one wait, then reductions with the most
   // independent work first
   float v[128];
-#pragma unroll
-  for (int k = 0; k < 4; ++k) tmem_ld32(ta + 32u * k, v + 32 * k);
+  tmem_ld128(ta, v);
   tmem_wait_ld();
   if (release) {
     tc_fence_before();
