@@ -86,12 +86,15 @@ struct PrefixOffset {
 };
 
 // Walks the CTA's tile range [g0, g1) request by request.
+// The list is in units of work: a request with tiles weighs its tiles plus
+// k leading units that hold no tile (the cost of starting a request), so a
+// CTA whose range covers many short requests gets fewer tiles.
 struct SegmentWalker {
-  const int *prefix;  // prefix[b] = tiles of requests < b, prefix[batch] = total
+  const int *prefix;  // prefix[b] = units of requests < b, prefix[batch] = total
   int batch;
-  int g, g1, b;
-  __device__ SegmentWalker(const int *p, int nb, int g0_, int g1_)
-      : prefix(p), batch(nb), g(g0_), g1(g1_), b(0) {
+  int g, g1, b, k;
+  __device__ SegmentWalker(const int *p, int nb, int g0_, int g1_, int k_)
+      : prefix(p), batch(nb), g(g0_), g1(g1_), b(0), k(k_) {
     int lo = 0, hi = nb;  // largest lo with prefix[lo] <= g0
     while (lo < hi) {
       const int mid = (lo + hi + 1) >> 1;
@@ -100,18 +103,29 @@ struct SegmentWalker {
     b = lo;
   }
   // Next segment: request rb, local tiles [t0, t1).  False when done.
+  // Requests of which the range holds only leading units are skipped.
   __device__ bool next(int &rb, int &t0, int &t1) {
-    if (g >= g1) return false;
-    while (b < batch && prefix[b + 1] <= g) ++b;
-    if (b >= batch) return false;
-    rb = b;
-    t0 = g - prefix[b];
-    t1 = min(g1, prefix[b + 1]) - prefix[b];
-    g = prefix[b] + t1;
-    ++b;
-    return true;
+    for (;;) {
+      if (g >= g1) return false;
+      while (b < batch && prefix[b + 1] <= g) ++b;
+      if (b >= batch) return false;
+      const int end = min(g1, prefix[b + 1]);
+      const int s0 = max(g, prefix[b] + k);  // first tile position in range
+      g = end;
+      ++b;
+      if (s0 < end) {
+        rb = b - 1;
+        t0 = s0 - prefix[b - 1] - k;
+        t1 = end - prefix[b - 1] - k;
+        return true;
+      }
+    }
   }
 };
+
+// Leading units per request in the prefill scorer's work list (about the
+// time a request's start costs a CTA there, in tiles); none for decode.
+constexpr int kWideRequestUnits = 4;
 
 __device__ __forceinline__ int page_slot_of(int c, int split) { return split ? (c >> 1) : c; }
 
@@ -357,7 +371,8 @@ score_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CU
     int sum = 0;
     for (int b = lo; b < hi; ++b) {
       const int u = units_of(req_seq_len(a, b), a.page_size, g.split);
-      sum += (u + g.cpt - 1) / g.cpt;
+      const int tiles = (u + g.cpt - 1) / g.cpt;
+      sum += tiles + (WIDE && tiles > 0 ? kWideRequestUnits : 0);
     }
     // exclusive scan of the per-thread sums: shuffles inside each warp, then
     // the warp totals (NT / 32 of them) in shared memory
@@ -376,7 +391,8 @@ score_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CU
     for (int b = lo; b < hi; ++b) {
       prefix[b] = run;
       const int u = units_of(req_seq_len(a, b), a.page_size, g.split);
-      run += (u + g.cpt - 1) / g.cpt;
+      const int tiles = (u + g.cpt - 1) / g.cpt;
+      run += tiles + (WIDE && tiles > 0 ? kWideRequestUnits : 0);
     }
   }
   __syncthreads();
@@ -397,7 +413,7 @@ score_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CU
     int qslot = 0;
     long long issued = 0;
     int last_qslot = -1;
-    SegmentWalker walk(prefix, nbatch, g0, g1);
+    SegmentWalker walk(prefix, nbatch, g0, g1, WIDE ? kWideRequestUnits : 0);
     int b, t0, t1;
     bool ok = true;
     if (a.pdl) {
@@ -405,7 +421,7 @@ score_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CU
       // tiles of this CTA into L2, only from pages that end at or before
       // seq_len - dql (the preceding kernel may still append the newest
       // keys); every real load below is issued after the wait.
-      SegmentWalker pw(prefix, nbatch, g0, g1);
+      SegmentWalker pw(prefix, nbatch, g0, g1, WIDE ? kWideRequestUnits : 0);
       int pb, p0, p1, budget = 2 * kStages;
       while (budget > 0 && pw.next(pb, p0, p1)) {
         const ReqView rv = req_view(a, pb);
@@ -516,7 +532,7 @@ score_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CU
       uint32_t sphase = 0, aphase = 0;
       uint32_t qph0 = 0, qph1 = 0;
       int qslot = 0;
-      SegmentWalker walk(prefix, nbatch, g0, g1);
+      SegmentWalker walk(prefix, nbatch, g0, g1, WIDE ? kWideRequestUnits : 0);
       int b, t0, t1;
       bool ok = true;
       while (ok && walk.next(b, t0, t1)) {
@@ -643,7 +659,7 @@ score_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CU
       lfid = reinterpret_cast<int *>(wl + 16 * 32 * 8);
       lfsc = reinterpret_cast<float *>(wl + 16 * 32 * 8 + 16 * 32 * 4);
     }
-    SegmentWalker walk(prefix, nbatch, g0, g1);
+    SegmentWalker walk(prefix, nbatch, g0, g1, WIDE ? kWideRequestUnits : 0);
     int b, t0, t1;
     bool ok = true;
     while (walk.next(b, t0, t1)) {
