@@ -195,10 +195,9 @@ __device__ __forceinline__ void lane_insert(LaneTop &s, unsigned long long *lk, 
 
 // Epilogue of one tile for a warp.  taddr addresses the warp's lane quarter
 // of the tile's accumulator: lane l holds query row rowq + l of the request
-// (row = token j * 4 + head; rowq = 0 with the replicated queries, 32 times
-// the quarter with 128 distinct rows), columns 0..127 hold the tile's keys
-// in order.  R keys feed one plane column, so the tile covers 128 / R
-// columns.
+// (row = token j * 4 + head; rowq = 0, the queries being replicated in every
+// quarter), columns 0..127 hold the tile's keys in order.  R keys feed one
+// plane column, so the tile covers 128 / R columns.
 template <int R, bool FUSED>
 __device__ __forceinline__ void epilogue_tile(const ScoreArgs &a, uint32_t taddr, int lane,
                                               int rowq, int tok0, int ntok, int tl, int nunits,
@@ -256,11 +255,11 @@ __device__ __forceinline__ void epilogue_tile(const ScoreArgs &a, uint32_t taddr
   }
 }
 
-// Epilogue of one tile of the prefill scorer for one warp of the set that
-// owns the row half: lane l holds query row rowq + l of the record (up to
-// 256 distinct rows).  A column that reaches past the record's first token
-// is masked with 32-bit compares.  With release, the warp hands the
-// accumulator pair back once its part of the tile is in registers.
+// Epilogue of one tile of the prefill scorer for one warp: lane l holds
+// query row rowq + l of the record (up to 256 distinct rows).  A column that
+// reaches past the record's first token is masked with 32-bit compares.
+// With release, the warp hands the accumulator back once its tile is in
+// registers.
 template <int R>
 __device__ __forceinline__ void epilogue_tile_wide(const ScoreArgs &a, uint32_t ta, int lane,
                                                    int rowq, int tok0, int ntok, int tl,
@@ -304,13 +303,16 @@ __device__ __forceinline__ void epilogue_tile_wide(const ScoreArgs &a, uint32_t 
 }
 
 // WIDE: the prefill scorer.  A request (a plan record of up to 64 tokens)
-// stages its 256 distinct query rows in one box: two 128-row A operands.
-// Every 128-key tile feeds both (two N = 128 MMA groups, the second only
-// when the record has more than 32 tokens) into one of two accumulator
-// pairs, tiles alternating, so each key byte read serves 256 query rows.
-// The epilogue warps form two sets of four, set s finishing row half s of
-// every tile; each warp takes its lane quarter (8 of the half's 32 tokens)
-// and the accumulator pair is free again after all eight warps have arrived.
+// stages its 256 distinct query rows in one box: two 128-row A operands
+// (row halves).  Its tiles go in pairs: two adjacent ring stages form one
+// 256-row B operand.  Each row half of a pair is one item: an N = 256 MMA
+// group (N = 128 for a segment's odd last tile; the second half only when
+// the record has more than 32 tokens) into one of two 256-column
+// accumulators, items alternating, so each key byte read serves 256 query
+// rows at the N = 256 MMA rate.  The epilogue warps form two sets of four,
+// set s finishing tile s of every item for the half's rows; each warp takes
+// its lane quarter (8 of the half's 32 tokens) and the accumulator is free
+// again after all eight warps have arrived.
 template <bool FUSED, bool WIDE>
 __global__ void __launch_bounds__(BlockThreads<WIDE>::value, 1)
 score_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmq,
