@@ -47,10 +47,10 @@ FALLBACK_HBM_GBS = 6800.0
 # streamed), measured for the kernel source with this digest.  When the
 # kernel changes the digest no longer matches and `traffic` is reported null.
 NCU_TRAFFIC = {
-    # dram__bytes_read.sum + dram__bytes_write.sum = 278821120 + 3031552 bytes for
+    # dram__bytes_read.sum + dram__bytes_write.sum = 278821632 + 3043072 bytes for
     # 278330624 bytes of index-K (first 32 requests of the multitoken workload),
     # see profiles/icp_score_multitoken.md
-    ("multitoken", "dc210446805a2855"): (278821120 + 3031552) / 278330624,
+    ("multitoken", "86d969e7fdbc9aae"): (278821632 + 3043072) / 278330624,
 }
 
 
