@@ -44,12 +44,16 @@ __device__ __forceinline__ bool poll_flag(const int *flag, int want, long long s
 // orders it), row ((h / hpr) * T + t) * hpr + h % hpr of the carrier.
 enum EmitMode { kEmitPlain = 0, kEmitLegacy = 1, kEmitTagged = 2, kEmitCarrier = 3 };
 
+// heads_per_rank is 4 / world_size (4, 2 or 1), so dividing by it is a
+// shift and the remainder a mask.
+__device__ __forceinline__ int hpr_shift(int hpr) { return hpr == 4 ? 2 : (hpr == 2 ? 1 : 0); }
+
 // Address of the legacy receive row (t, h) of this publish.
 __device__ __forceinline__ int *legacy_row(const SelectArgs &a, int t, int h) {
   const int hpr = a.heads_per_rank;
   const long long r =
-      (((long long)a.slot * a.world_size + a.rank) * hpr + h % hpr) * a.capacity + t;
-  return reinterpret_cast<int *>(a.recv_bases[h / hpr]) + r * kRowWords;
+      (((long long)a.slot * a.world_size + a.rank) * hpr + (h & (hpr - 1))) * a.capacity + t;
+  return reinterpret_cast<int *>(a.recv_bases[h >> hpr_shift(hpr)]) + r * kRowWords;
 }
 
 // The ready flag of that row, read with acquire when the row's work starts so
@@ -72,7 +76,8 @@ __device__ __forceinline__ void emit_row(const SelectArgs &a, int lane, int row,
     }
   } else if constexpr (MODE == kEmitCarrier) {
     const int hpr = a.heads_per_rank;
-    int *dst = a.carrier + (((long long)(h / hpr) * a.T + t) * hpr + h % hpr) * 32;
+    int *dst =
+        a.carrier + (((long long)(h >> hpr_shift(hpr)) * a.T + t) * hpr + (h & (hpr - 1))) * 32;
     if (lane < kTopK) {
       dst[lane] = __float_as_int(out_sc);
       dst[kTopK + lane] = out_id;
@@ -80,7 +85,7 @@ __device__ __forceinline__ void emit_row(const SelectArgs &a, int lane, int row,
   } else {
     const int hpr = a.heads_per_rank;
     const long long r =
-        (((long long)a.slot * a.world_size + a.rank) * hpr + h % hpr) * a.capacity + t;
+        (((long long)a.slot * a.world_size + a.rank) * hpr + (h & (hpr - 1))) * a.capacity + t;
     if constexpr (MODE == kEmitLegacy) {
       int *dst = legacy_row(a, t, h);
       int ok = 0;
@@ -114,7 +119,7 @@ __device__ __forceinline__ void emit_row(const SelectArgs &a, int lane, int row,
       const unsigned long long word =
           ((unsigned long long)g << 32) | (unsigned long long)(lane < kTopK ? sb : ib);
       unsigned long long *dst =
-          reinterpret_cast<unsigned long long *>(a.recv_bases[h / hpr]) + r * 32;
+          reinterpret_cast<unsigned long long *>(a.recv_bases[h >> hpr_shift(hpr)]) + r * 32;
       st_relaxed_gpu_u64(dst + lane, word);
     }
   }
@@ -827,7 +832,7 @@ __global__ void __launch_bounds__(128) merge_kernel(const MergeArgs a) {
   const int item = blockIdx.x * 4 + warp;
   const int hpr = a.heads_per_rank;
   if (item >= a.T * hpr) return;
-  const int t = item / hpr, hl = item % hpr;
+  const int t = item >> hpr_shift(hpr), hl = item & (hpr - 1);
   const int nvp = a.nvp[t];
   constexpr int ws = NS;
 
@@ -877,7 +882,7 @@ __global__ void __launch_bounds__(128) merge_tagged_kernel(const MergeArgs a) {
   const int item = blockIdx.x * 4 + warp;
   const int hpr = a.heads_per_rank;
   if (item >= a.T * hpr) return;
-  const int t = item / hpr, hl = item % hpr;
+  const int t = item >> hpr_shift(hpr), hl = item & (hpr - 1);
   const int nvp = a.nvp[t];
   constexpr int ws = NS;
 
@@ -933,7 +938,7 @@ __global__ void __launch_bounds__(128) merge_carrier_kernel(const MergeArgs a) {
   const int item = blockIdx.x * 4 + warp;
   const int hpr = a.heads_per_rank;
   if (item >= a.T * hpr) return;
-  const int t = item / hpr, hl = item % hpr;
+  const int t = item >> hpr_shift(hpr), hl = item & (hpr - 1);
   const int nvp = a.nvp[t];
   int ids[NS];
   float scs[NS];
