@@ -305,7 +305,7 @@ class DecodeBench:
                           self.errors, T=self.T, slot=slot, world_size=ws,
                           heads_per_rank=self.hpr, capacity=self.cap,
                           init_blocks=spec.init_blocks, local_blocks=spec.local_blocks,
-                          spin_limit=1 << 22)
+                          spin_limit=1 << 22, enable_pdl=True)
         self.slot = (slot + 1) % 3
 
     graph_period = 3   # receive slots rotate 0, 1, 2

@@ -166,11 +166,15 @@ int icp_publish_rows(const float *scores, int T, int K, const int32_t *num_valid
  *   merge and adds 1 to errors[0].
  *   out_scores float32 [T, heads_per_rank, 16], out_ids int32 [T, heads_per_rank, 16].
  *   Limits as icp_publish_rows.  errors: required.
+ *   enable_pdl: launch with programmatic dependent launch.  The kernel waits
+ *   on the preceding kernel (griddepcontrol.wait) before it reads anything,
+ *   and only then lets its own dependents launch.  0 launches it as an
+ *   ordinary kernel.
  */
 int icp_merge(int32_t *recv, const int32_t *num_valid_pages, int T, int slot, int world_size,
               int heads_per_rank, int capacity, int init_blocks, int local_blocks,
               int64_t spin_limit, int32_t *errors, float *out_scores, int32_t *out_ids,
-              void *stream);
+              int enable_pdl, void *stream);
 
 /*
  * Tagged publish (msa_icp_topk_select_publish with `generations`: tagged
@@ -206,12 +210,13 @@ int icp_publish_rows_tagged(const float *scores, int T, int K, const int32_t *nu
  *             counter advances on every merge.  Each wait is bounded by
  *             spin_limit polls and about two seconds; a source that has not
  *             arrived is left out and adds 1 to errors[0].
- *   Output and rule as icp_merge.  Rows are not modified (no flags to free).
+ *   Output, rule and enable_pdl as icp_merge.  Rows are not modified (no
+ *   flags to free).
  */
 int icp_merge_tagged(const int64_t *recv, int32_t *expected, const int32_t *num_valid_pages,
                      int T, int slot, int world_size, int heads_per_rank, int capacity,
                      int init_blocks, int local_blocks, int64_t spin_limit, int32_t *errors,
-                     float *out_scores, int32_t *out_ids, void *stream);
+                     float *out_scores, int32_t *out_ids, int enable_pdl, void *stream);
 
 /*
  * Workspace bytes icp_score_select needs for `batch` requests of

@@ -252,7 +252,7 @@ int icp_publish_rows(const float *scores, int T, int K, const int32_t *num_valid
 int icp_merge(int32_t *recv, const int32_t *num_valid_pages, int T, int slot, int world_size,
               int heads_per_rank, int capacity, int init_blocks, int local_blocks,
               int64_t spin_limit, int32_t *errors, float *out_scores, int32_t *out_ids,
-              void *stream) {
+              int enable_pdl, void *stream) {
   if (world_size != 1 && world_size != 2 && world_size != 4) return ICP_ERR_INVALID_ARG;
   if (heads_per_rank * world_size != ICP_HEADS) return ICP_ERR_INVALID_ARG;
   if (slot < 0 || slot > 2 || T < 1 || T > capacity || spin_limit < 1)
@@ -278,6 +278,7 @@ int icp_merge(int32_t *recv, const int32_t *num_valid_pages, int T, int slot, in
   a.errors = errors;
   a.out_scores = out_scores;
   a.out_ids = out_ids;
+  a.pdl = enable_pdl ? 1 : 0;
   return to_status(icp::launch_merge(a, false, static_cast<cudaStream_t>(stream)));
 }
 
@@ -321,7 +322,7 @@ int icp_publish_rows_tagged(const float *scores, int T, int K, const int32_t *nu
 int icp_merge_tagged(const int64_t *recv, int32_t *expected, const int32_t *num_valid_pages,
                      int T, int slot, int world_size, int heads_per_rank, int capacity,
                      int init_blocks, int local_blocks, int64_t spin_limit, int32_t *errors,
-                     float *out_scores, int32_t *out_ids, void *stream) {
+                     float *out_scores, int32_t *out_ids, int enable_pdl, void *stream) {
   if (world_size != 1 && world_size != 2 && world_size != 4) return ICP_ERR_INVALID_ARG;
   if (heads_per_rank * world_size != ICP_HEADS) return ICP_ERR_INVALID_ARG;
   if (slot < 0 || slot > 2 || T < 1 || T > capacity || spin_limit < 1)
@@ -350,6 +351,7 @@ int icp_merge_tagged(const int64_t *recv, int32_t *expected, const int32_t *num_
   a.errors = errors;
   a.out_scores = out_scores;
   a.out_ids = out_ids;
+  a.pdl = enable_pdl ? 1 : 0;
   return to_status(icp::launch_merge(a, true, static_cast<cudaStream_t>(stream)));
 }
 

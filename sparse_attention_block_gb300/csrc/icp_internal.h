@@ -83,6 +83,7 @@ struct MergeArgs {
   const unsigned long long *recv64;  // tagged merge: this owner's tagged rows
   int32_t *expected;                 // tagged merge: [3][ws][hpr][capacity] counters
   const int32_t *received;           // prefill merge: carrier rows [ws][T][hpr][32]
+  int pdl;                           // launched with programmatic dependent launch
 };
 
 // Launchers (return a cudaError_t from the launch).

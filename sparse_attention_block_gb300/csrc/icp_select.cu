@@ -824,8 +824,11 @@ template <int NS>
 __global__ void __launch_bounds__(128) merge_kernel(const MergeArgs a) {
   __shared__ int s_id[4][kTopK];
   __shared__ float s_sc[4][kTopK];
-  // a scorer launched next with early start may begin its set-up now: it
-  // reads nothing this kernel writes before waiting for it
+  // under programmatic dependent launch: wait for the preceding kernel (the
+  // publish) before reading anything; then a scorer launched next with early
+  // start may begin its set-up (it reads nothing this kernel writes before
+  // waiting for it)
+  if (a.pdl) pdl_wait();
   pdl_launch_dependents();
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -877,6 +880,9 @@ template <int NS>
 __global__ void __launch_bounds__(128) merge_tagged_kernel(const MergeArgs a) {
   __shared__ int s_id[4][kTopK];
   __shared__ float s_sc[4][kTopK];
+  // as merge_kernel
+  if (a.pdl) pdl_wait();
+  pdl_launch_dependents();
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int item = blockIdx.x * 4 + warp;
@@ -1015,11 +1021,30 @@ cudaError_t launch_select(const SelectArgs &a, int mode, int sm_count, cudaStrea
 }
 
 // Merge kernels are compiled per world size (1, 2 or 4 sources).
+template <typename Kernel>
+void launch_merge_one(Kernel kernel, const MergeArgs &a, int grid, cudaStream_t stream) {
+  if (!a.pdl) {
+    kernel<<<grid, 128, 0, stream>>>(a);
+    return;
+  }
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)grid);
+  cfg.blockDim = dim3(128);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  cudaLaunchKernelEx(&cfg, kernel, a);
+}
+
 template <int NS>
 void launch_merge_ns(const MergeArgs &a, int kind, int grid, cudaStream_t stream) {
-  if (kind == 2) merge_carrier_kernel<NS><<<grid, 128, 0, stream>>>(a);
-  else if (kind == 1) merge_tagged_kernel<NS><<<grid, 128, 0, stream>>>(a);
-  else merge_kernel<NS><<<grid, 128, 0, stream>>>(a);
+  if (kind == 2) launch_merge_one(merge_carrier_kernel<NS>, a, grid, stream);
+  else if (kind == 1) launch_merge_one(merge_tagged_kernel<NS>, a, grid, stream);
+  else launch_merge_one(merge_kernel<NS>, a, grid, stream);
 }
 
 cudaError_t launch_merge_kind(const MergeArgs &a, int kind, cudaStream_t stream) {

@@ -56,9 +56,10 @@ lib.icp_publish_rows_tagged.argtypes = [_P, _I32, _I32, _P, _P, _P, _I32, _I32, 
                                         _I32, _I32, _I32, _I32, _I32, _I32, _P]
 lib.icp_merge_tagged.restype = _I32
 lib.icp_merge_tagged.argtypes = [_P, _P, _P, _I32, _I32, _I32, _I32, _I32, _I32, _I32, _I64,
-                                 _P, _P, _P, _P]
+                                 _P, _P, _P, _I32, _P]
 lib.icp_merge.restype = _I32
-lib.icp_merge.argtypes = [_P, _P, _I32, _I32, _I32, _I32, _I32, _I32, _I32, _I64, _P, _P, _P, _P]
+lib.icp_merge.argtypes = [_P, _P, _I32, _I32, _I32, _I32, _I32, _I32, _I32, _I64, _P, _P, _P,
+                          _I32, _P]
 lib.icp_prefill_plan_words.restype = _I64
 lib.icp_prefill_plan_words.argtypes = [_I32, _I32]
 lib.icp_prefill_plan.restype = _I32
@@ -193,8 +194,11 @@ def icp_publish_rows(scores, num_valid_pages, recv_bases, errors, *, slot: int, 
 
 def icp_merge(recv, num_valid_pages, out_scores, out_ids, errors, *, T: int, slot: int,
               world_size: int, heads_per_rank: int, capacity: int, init_blocks: int,
-              local_blocks: int, spin_limit: int = DEFAULT_SPIN_LIMIT, stream=None):
-    """Owner merge of this owner's receive rows into out_* [T, heads_per_rank, 16]."""
+              local_blocks: int, spin_limit: int = DEFAULT_SPIN_LIMIT, enable_pdl: bool = False,
+              stream=None):
+    """Owner merge of this owner's receive rows into out_* [T, heads_per_rank, 16].
+
+    enable_pdl: launch with programmatic dependent launch (see include/icp.h)."""
     rp = _dev(recv, "recv", (torch.int32,), None)
     if recv.numel() < recv_rows(world_size, heads_per_rank, capacity) * ROW_WORDS:
         raise ValueError("recv is smaller than [3][ws][hpr][capacity][33]")
@@ -206,7 +210,8 @@ def icp_merge(recv, num_valid_pages, out_scores, out_ids, errors, *, T: int, slo
         raise ValueError("out_scores / out_ids must be [T, heads_per_rank, 16]")
     ep = _dev(errors, "errors", (torch.int32,), 1)
     _check(lib.icp_merge(rp, np_, T, slot, world_size, heads_per_rank, capacity, init_blocks,
-                         local_blocks, spin_limit, ep, osp, oip, _stream(stream)), "icp_merge")
+                         local_blocks, spin_limit, ep, osp, oip, 1 if enable_pdl else 0,
+                         _stream(stream)), "icp_merge")
 
 
 def icp_score_select_workspace_bytes(batch: int, decode_query_len: int) -> int:
@@ -278,7 +283,7 @@ def icp_publish_rows_tagged(scores, num_valid_pages, recv_bases, generations, *,
 def icp_merge_tagged(recv, expected, num_valid_pages, out_scores, out_ids, errors, *, T: int,
                      slot: int, world_size: int, heads_per_rank: int, capacity: int,
                      init_blocks: int, local_blocks: int, spin_limit: int = DEFAULT_SPIN_LIMIT,
-                     stream=None):
+                     enable_pdl: bool = False, stream=None):
     """Owner merge of tagged rows into out_* [T, heads_per_rank, 16]."""
     rp = _dev(recv, "recv", (torch.int64,), None)
     if recv.numel() < recv_rows(world_size, heads_per_rank, capacity) * 32:
@@ -295,7 +300,7 @@ def icp_merge_tagged(recv, expected, num_valid_pages, out_scores, out_ids, error
     erp = _dev(errors, "errors", (torch.int32,), 1)
     _check(lib.icp_merge_tagged(rp, ep_, np_, T, slot, world_size, heads_per_rank, capacity,
                                 init_blocks, local_blocks, spin_limit, erp, osp, oip,
-                                _stream(stream)), "icp_merge_tagged")
+                                1 if enable_pdl else 0, _stream(stream)), "icp_merge_tagged")
 
 
 NOALLOC_SCRATCH_BYTES = 8 * 1024 * 1024

@@ -187,3 +187,56 @@ def test_chain_under_programmatic_dependent_launch():
         _merge_all(inp, spec, slot, bufs, errors, 1, 3)
         torch.cuda.synchronize()
         assert int(errors.item()) == 0
+
+
+def test_whole_chain_under_programmatic_dependent_launch():
+    # scorer, publish and owner merge all launched with enable_pdl, back to
+    # back with no synchronisation in between: every kernel waits on its
+    # predecessor before reading, so the merged lists equal the oracle's
+    # merge of the oracle's rows of the same planes
+    spec = W.DecodeSpec("pdl3", batch=7, page_size=128, world_size=2, decode_query_len=2,
+                        max_decode_query_len=2, init_blocks=1, local_blocks=3,
+                        seq_range=(300, 20000), capacity=14)
+    inp = W.make_decode_inputs(spec, seed=78)
+    ws, hpr, T = 2, 2, inp.T
+    cols = W.columns_for(spec, int(inp.seq_lens.max()))
+    bufs, bases = _recv(ws, hpr, spec.capacity, ws)
+    errors = torch.zeros(1, dtype=torch.int32, device="cuda")
+    q, _, bt, sl, nvp = to_dev(inp)
+    shards = [s.cuda() for s in inp.shards]
+    for step in range(3):
+        slot = step % 3
+        planes, outs = [], []
+        for rank in range(ws):
+            p = torch.empty((T, 4, cols), device="cuda")
+            icp().icp_score(q, shards[rank], bt, sl, p, rank=rank, world_size=ws, page_size=128,
+                            decode_query_len=2, max_decode_query_len=2, enable_pdl=True,
+                            errors=errors)
+            icp().icp_publish_rows(p, nvp, bases, errors, slot=slot, rank=rank, world_size=ws,
+                                   heads_per_rank=hpr, capacity=spec.capacity,
+                                   force_begin_blocks=1, force_end_blocks=3,
+                                   spin_limit=1 << 20, enable_pdl=True)
+            planes.append(p)
+        for owner in range(ws):
+            s = torch.empty((T, hpr, 16), dtype=torch.float32, device="cuda")
+            i = torch.empty((T, hpr, 16), dtype=torch.int32, device="cuda")
+            icp().icp_merge(bufs[owner], nvp, s, i, errors, T=T, slot=slot, world_size=ws,
+                            heads_per_rank=hpr, capacity=spec.capacity, init_blocks=1,
+                            local_blocks=3, spin_limit=1 << 20, enable_pdl=True)
+            outs.append((s, i))
+        torch.cuda.synchronize()
+        assert int(errors.item()) == 0
+        ref = [np.zeros((3 * ws * hpr * spec.capacity, 33), np.int32) for _ in range(ws)]
+        for rank in range(ws):
+            oracle.publish(planes[rank].cpu().numpy(), inp.num_valid_pages.numpy(), ref,
+                           slot=slot, rank=rank, world_size=ws, heads_per_rank=hpr,
+                           capacity=spec.capacity, force_begin_blocks=1, force_end_blocks=3)
+        for owner in range(ws):
+            ms, mi, missing = oracle.merge(ref[owner], inp.num_valid_pages.numpy(), T=T,
+                                           slot=slot, owner=owner, world_size=ws,
+                                           heads_per_rank=hpr, capacity=spec.capacity,
+                                           init_blocks=1, local_blocks=3)
+            assert missing == 0
+            s, i = outs[owner]
+            np.testing.assert_array_equal(i.cpu().numpy(), mi)
+            np.testing.assert_array_equal(s.cpu().numpy().view(np.int32), ms.view(np.int32))
