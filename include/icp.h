@@ -7,7 +7,8 @@
  *   msa_icp_topk_select_publish         -> icp_top16_select (select only) and
  *                                          icp_publish_rows (select + legacy receive rows)
  *   prepare_msa_icp_indexer, decode()   -> icp_merge (owner merge of the chain
- *                                          "score plane -> select and publish -> owner merge")
+ *                                          whose steps are score plane, Top16 select and
+ *                                          publish, owner merge)
  *                                          and icp_score_select (fused scorer + select)
  *
  * Conventions for every entry point:
@@ -53,8 +54,8 @@ const char *icp_status_string(int status);
 /*
  * Plane width for the longest request (msa_icp_decode_index_score_sharded,
  * parameter score_out, which defers to msa_icp_decode_score_columns()):
- * the number of columns of a request of max_seq_len tokens, rounded up to a
- * multiple of four.  A column is a global B128 block at page_size 128, a
+ * the number of columns of a request of max_seq_len tokens, padded to the
+ * next multiple of 4.  A column is a global B128 block at page_size 128, a
  * local page at page_size 256 with world_size 2 or 4, and a B128 block at
  * page_size 256 with world_size 1.  Returns the width, or -1 when the
  * arguments are invalid or the width would exceed ICP_MAX_COLS.  Host only.
@@ -86,13 +87,13 @@ int icp_score_columns(int max_seq_len, int page_size, int world_size);
  *   world_size; 1 <= decode_query_len <= max_decode_query_len,
  *   4 * max_decode_query_len <= 32; 0 <= batch <= ICP_MAX_BATCH.
  *   enable_pdl (parameter enable_pdl of the same page): non-zero launches with
- *   programmatic dependent launch.  The kernel then reads seq_lens and
- *   block_table and prefetches into L2 the index_k pages that end at or
- *   before seq_len - decode_query_len before it waits on the preceding
- *   kernel; it writes nothing and loads nothing else before that wait.  The
- *   kernel launched just before must not write seq_lens, block_table or
- *   those pages, and must either be launched without programmatic dependent
- *   launch or wait on its own predecessor before it triggers its dependents.
+ *   programmatic dependent launch.  Ahead of its griddepcontrol.wait the
+ *   kernel only reads seq_lens and block_table and warms L2 with the index_k
+ *   pages lying wholly below position seq_len - decode_query_len; no other
+ *   load and no store precedes the wait.  The caller guarantees that the
+ *   kernel queued just ahead leaves seq_lens, block_table and those pages
+ *   alone, and that it is either an ordinary launch or one that waits for its
+ *   own predecessor before it signals its dependents.
  *   0 removes the requirement.
  *   errors: optional int32 [>= 1] counter for timed-out internal waits.
  */
@@ -154,8 +155,8 @@ int icp_publish_rows(const float *scores, int T, int K, const int32_t *num_valid
                      int index_offset, int enable_pdl, void *stream);
 
 /*
- * Owner merge of the decode chain (prepare_msa_icp_indexer, decode():
- * "score plane -> Top16 select and publish -> owner merge"; the merge rule is
+ * Owner merge of the decode chain (prepare_msa_icp_indexer, decode(): the
+ * score plane, then the Top16 select and publish, then this merge; the rule is
  * this library's reading: union of the world_size published lists, maximum
  * score per id, then the icp_top16_select rule with num_valid_pages[t]).
  *   recv   this owner's receive storage, int32 [3][world_size][heads_per_rank][capacity][33].
@@ -189,8 +190,8 @@ int icp_merge(int32_t *recv, const int32_t *num_valid_pages, int T, int slot, in
  *                publish counters of this rank, zeroed once by the caller and
  *                never between steps: row (t, h) of slot s is published with
  *                generation generations[s][h][t] + 1, which is stored back.
- *   Nothing waits for a free row: as the page states, tagged mode needs at
- *   least two sparse layers between uses of one slot set.  Every row t < T,
+ *   Nothing waits for a free row: instead the page has the caller leave two
+ *   or more sparse layers between two uses of the same slot set.  Every row t < T,
  *   padding rows included, is written on every call.  Limits and
  *   enable_pdl as icp_publish_rows (no spin_limit, no errors).
  */

@@ -9,19 +9,19 @@
  * Sources (FlashInfer "msa_ops" API documentation pages):
  *   [SCORE]   flashinfer.msa_ops.msa_icp_decode_index_score_sharded
  *             - description: which score_out columns are written, the P128 /
- *               P256 column meaning, "other columns are not written";
- *             - parameter index_q: token j of a request sits at position
+ *               P256 column meaning; columns past those are left as they were;
+ *             - parameter index_q: the position of a request's token j is
  *               seq_len - decode_query_len + j;
  *             - parameter index_k: the [pages, page_size / world_size, 128] shard.
  *   [SELECT]  flashinfer.msa_ops.msa_icp_topk_select_publish
  *             - description: row (t, h) goes to peer h // heads_per_rank at row
  *               ((slot * world_size + rank) * heads_per_rank + h % heads_per_rank)
  *               * capacity + t; legacy rows are 33 int32 words (16 raw scores,
- *               16 ascending global ids, ready flag); every row is written on
- *               every call, padding rows included;
+ *               16 ascending global ids, ready flag); each call writes all the
+ *               rows, padded ones too;
  *             - parameter num_valid_pages: global B128 block counts per token;
- *             - parameter errors: a publish that waits spin_limit polls for a
- *               free row adds one.
+ *             - parameter errors: a publish that finds no free row within
+ *               spin_limit polls increments it.
  *   [PLAN]    flashinfer.msa_ops.prepare_msa_icp_indexer
  *             - init_blocks / local_blocks: forced begin / end blocks (sum <= 16);
  *             - decode(): score plane -> Top16 select and publish -> owner merge.
@@ -78,7 +78,7 @@ double icp_orc_e4m3(uint8_t code)
 }
 
 /* Number of columns of a request that hold keys, and the number written
- * (rounded up to a multiple of four) [SCORE description]. */
+ * (padded to the next multiple of 4) [SCORE description]. */
 static int unit_tokens(int page_size, int world_size)
 {
     /* P128: a column is a global B128 block.  P256 sharded: a column is a
@@ -688,8 +688,8 @@ int icp_orc_merge_carrier(const int32_t *received, const int32_t *num_valid_page
  *     [3, ws, hpr, capacity], zeroed once); a merge of slot `slot` takes a
  *     source row as arrived when all 32 words carry expected + 1, and the
  *     counter advances on every merge, arrived or not;
- *   - nothing waits for a free row: the pages require at least two sparse
- *     layers between uses of a slot set instead.
+ *   - nothing waits for a free row: the pages instead ask for two or more
+ *     sparse layers between two uses of one slot set.
  */
 int icp_orc_publish_tagged(const float *scores, int T, int K, const int32_t *num_valid_pages,
                            int64_t *const *recv, int32_t *generations, int slot, int rank,

@@ -420,9 +420,9 @@ score_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CU
     bool ok = true;
     if (a.pdl) {
       // Early start: while the preceding kernel finishes, pull the first
-      // tiles of this CTA into L2, only from pages that end at or before
-      // seq_len - dql (the preceding kernel may still append the newest
-      // keys); every real load below is issued after the wait.
+      // tiles of this CTA into L2, only from pages lying wholly below
+      // position seq_len - dql (the newest keys may still be appended by the
+      // preceding kernel); every real load below is issued after the wait.
       SegmentWalker pw(prefix, nbatch, g0, g1, WIDE ? kWideRequestUnits : 0);
       int pb, p0, p1, budget = 2 * kStages;
       while (budget > 0 && pw.next(pb, p0, p1)) {

@@ -230,7 +230,7 @@ def make_select_plane(*, T: int = SELECT_T, K: int = SELECT_K, dup: float = SELE
 
 def columns_for(spec: DecodeSpec, max_seq_len: int) -> int:
     """Plane width for a workload: one column per unit (B128 block, or local
-    page for P256 sharded), rounded up to a multiple of four."""
+    page for P256 sharded), padded to the next multiple of 4."""
     unit = 128 if (spec.page_size == 128 or spec.world_size == 1) else spec.page_size
     n = (max_seq_len + unit - 1) // unit
     return max(4, (n + 3) // 4 * 4)

@@ -90,3 +90,15 @@ def test_traffic_table_keys_and_ratios():
     for (workload, digest), ratio in bench.NCU_TRAFFIC.items():
         assert len(digest) == 16
         assert 1.0 <= ratio < 1.1, (workload, ratio)
+
+
+def test_code_digest_ignores_comments_but_not_code():
+    base = {"icp_score.cu": "int a; // x\n/* y */ int b;\n", "icp_fused.cuh": "f();\n",
+            "icp_device.cuh": ""}
+    d = bench.kernel_digest(lambda f: base[f])
+    reworded = dict(base)
+    reworded["icp_score.cu"] = "int a; // other words\n\n int b; /* a\n longer note */\n"
+    assert bench.kernel_digest(lambda f: reworded[f]) == d
+    changed = dict(base)
+    changed["icp_score.cu"] = "int a; // x\n/* y */ int c;\n"
+    assert bench.kernel_digest(lambda f: changed[f]) != d
