@@ -284,8 +284,8 @@ int icp_score_select_noalloc(const uint8_t *index_q, const uint8_t *index_k, int
                              int32_t *out_ids, int32_t *errors, void *stream);
 
 /*
- * Prefill window (prepare_msa_icp_indexer: prefill_window_plan once per
- * query window and step, prefill_local per query chunk, the caller's one
+ * Prefill window (prepare_msa_icp_indexer: one prefill_window_plan for each
+ * window of queries in a step, prefill_local per query chunk, the caller's one
  * exchange per layer, then prefill_merge(received, num_valid_pages,
  * output)).  The pages that define these calls are missing; the reading
  * taken:

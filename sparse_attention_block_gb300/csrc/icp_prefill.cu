@@ -1,5 +1,5 @@
 // icp_prefill.cu - the prefill window plan (prepare_msa_icp_indexer:
-// prefill_window_plan, once per query window and step).
+// prefill_window_plan, built one time for each window of queries in a step).
 //
 // A window holds, for every request b, a chunk of its newest
 // n_b = qo_indptr[b+1] - qo_indptr[b] tokens (window tokens qo_indptr[b] ..

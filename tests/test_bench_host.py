@@ -2,8 +2,8 @@
 
 - The algorithmic byte counts of a decode step and of a prefill window,
   worked out by hand from their definitions on small cases: index-K rows
-  needed, queries, plane columns written (a request's columns rounded up to
-  a multiple of 4), block table entries, the select's plane read and
+  needed, queries, plane columns written (a request's columns padded to the
+  next multiple of 4), block table entries, the select's plane read and
   published rows, the merge's reads and writes.
 - The clock record: its summary of NVML samples, and which records reject a
   timing (thermal or hardware slowdown, or clocks held low with no reason).
