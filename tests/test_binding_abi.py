@@ -1,0 +1,63 @@
+"""The ctypes binding declares every entry point exactly as include/icp.h
+does: same parameter count, and for each position a pointer, a 32-bit int,
+an int64_t or a size_t where the header has one, and the same return type.
+A binding that drifts from the header would pass truncated or shifted
+arguments to the library, so this is checked on the CPU."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "icp.h")
+
+
+def _ctype(decl: str):
+    decl = decl.strip()
+    if "*" in decl:
+        return ctypes.c_void_p
+    base = decl.rsplit(None, 1)[0] if " " in decl else decl
+    base = base.replace("const", "").strip()
+    return {"int": ctypes.c_int, "int32_t": ctypes.c_int32, "int64_t": ctypes.c_int64,
+            "size_t": ctypes.c_size_t}[base]
+
+
+def _prototypes():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    out = {}
+    for ret, name, params in re.findall(
+            r"^\s*((?:const\s+)?\w+\s*\*?)\s*(icp_\w+)\s*\(([^)]*)\)\s*;", text, flags=re.M | re.S):
+        out[name] = (ret.strip(), [p for p in params.split(",") if p.strip()])
+    return out
+
+
+@pytest.fixture(scope="module")
+def binding():
+    from sparse_attention_block_gb300 import build
+    build.build()
+    from sparse_attention_block_gb300 import icp
+    return icp
+
+
+def test_header_parses_into_every_entry_point():
+    protos = _prototypes()
+    assert len(protos) == 16, sorted(protos)
+    assert "icp_score" in protos and len(protos["icp_score"][1]) == 17
+
+
+def test_binding_matches_the_header(binding):
+    for name, (ret, params) in _prototypes().items():
+        fn = getattr(binding.lib, name)
+        assert fn.argtypes is not None, f"{name}: no argtypes"
+        want = [_ctype(p) for p in params]
+        got = list(fn.argtypes)
+        assert len(got) == len(want), f"{name}: {len(got)} arguments, header has {len(want)}"
+        for i, (g, w) in enumerate(zip(got, want)):
+            assert ctypes.sizeof(g) == ctypes.sizeof(w) and (g is ctypes.c_void_p) == \
+                (w is ctypes.c_void_p), f"{name} argument {i}: {g} vs {w} ({params[i].strip()})"
+        if ret == "const char *" or ret == "const char*":
+            assert fn.restype is ctypes.c_char_p, name
+        else:
+            assert ctypes.sizeof(fn.restype) == ctypes.sizeof(_ctype(ret + " r")), name
