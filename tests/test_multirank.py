@@ -35,7 +35,7 @@ def _worker(rank, world, port, out):
 
 def test_max_over_ranks_with_gloo():
     port = _free_port()
-    out = mp.Manager().dict()
+    out = mp.get_context("spawn").Manager().dict()
     mp.spawn(_worker, args=(2, port, out), nprocs=2, join=True)
     assert out[0] == 11.0 and out[1] == 11.0
 
@@ -102,6 +102,6 @@ def _prefill_exchange_worker(rank, world, port, out):
 
 def test_prefill_carrier_exchange_with_gloo():
     port = _free_port()
-    out = mp.Manager().dict()
+    out = mp.get_context("spawn").Manager().dict()
     mp.spawn(_prefill_exchange_worker, args=(2, port, out), nprocs=2, join=True)
     assert out[0] and out[1]
