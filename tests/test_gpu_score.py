@@ -84,6 +84,33 @@ def test_block_table_with_row_stride_and_zero_length_requests():
     assert_plane_matches(gp, ex, ab, "strided table")
 
 
+@pytest.mark.parametrize("page_size", [128, 256])
+def test_block_table_entries_outside_the_pool_read_as_zero_keys(page_size):
+    # entries past the pool and below 0 inside each request's pages: the
+    # tensor map fills those rows with zeros, so the plane must equal the
+    # oracle's plane with the entries pointing at an all-zero page
+    spec, inp = _case(page_size, 1, 2, [700, 300], seed=5)
+    num_pages = inp.index_k.shape[0]
+    bt = inp.block_table.clone()
+    bt[0, 1] = num_pages + 7
+    bt[0, 2] = num_pages
+    bt[1, 0] = -2
+    kz = torch.cat([inp.index_k, torch.zeros((1,) + tuple(inp.index_k.shape[1:]),
+                                             dtype=torch.uint8)])
+    bz = bt.clone()
+    bz[0, 1] = bz[0, 2] = bz[1, 0] = num_pages
+    q, k, _, sl, _ = to_dev(inp)
+    errors = torch.zeros(1, dtype=torch.int32, device="cuda")
+    cols = W.columns_for(spec, 700)
+    gp = gpu_score(q, k, bt.cuda(), sl, cols=cols, rank=0, world_size=1, page_size=page_size,
+                   dql=2, errors=errors)
+    torch.cuda.synchronize()
+    assert int(errors.item()) == 0
+    ex, ab = oracle_plane(inp.index_q, kz, bz, inp.seq_lens, cols=cols, rank=0, world_size=1,
+                          page_size=page_size, dql=2)
+    assert_plane_matches(gp, ex, ab, f"pages outside the pool, P{page_size}")
+
+
 def test_extreme_fp8_values_stay_within_tolerance():
     # max-magnitude and subnormal codes; sums of 128 products of 448 * 448
     spec = W.DecodeSpec("x", batch=2, page_size=128, world_size=1, decode_query_len=2,
