@@ -110,6 +110,21 @@ def _dev(t: torch.Tensor, name: str, dtypes, ndim=None, contiguous=True):
 _FP8 = (torch.uint8, torch.float8_e4m3fn)
 
 
+def _on_current_device(*tensors):
+    """The library launches on the current CUDA device: every tensor must live
+    there (a tensor of another device would be read through a foreign
+    pointer)."""
+    cur = torch.cuda.current_device()
+    for t in tensors:
+        if t is not None and t.get_device() != cur:
+            raise ValueError(f"a tensor is on {t.device}, the current device is cuda:{cur}")
+
+
+def _rows_at_least(t, n: int, name: str):
+    if t.shape[0] < n:
+        raise ValueError(f"{name} has {t.shape[0]} rows, the call reads {n}")
+
+
 def icp_score_columns(max_seq_len: int, page_size: int, world_size: int) -> int:
     cols = lib.icp_score_columns(int(max_seq_len), int(page_size), int(world_size))
     if cols < 0:
@@ -139,6 +154,8 @@ def icp_score(index_q, index_k, block_table, seq_lens, score_out, *, rank: int, 
     if score_out.shape[0] != T or score_out.shape[1] != HEADS:
         raise ValueError(f"score_out must be [{T}, 4, cols]")
     ep = 0 if errors is None else _dev(errors, "errors", (torch.int32,), 1)
+    _rows_at_least(block_table, B, "block_table")
+    _on_current_device(index_q, index_k, block_table, seq_lens, score_out, errors)
     _check(lib.icp_score(qp, kp, index_k.shape[0], btp, block_table.stride(0), slp, sop, B,
                          score_out.shape[2], rank, world_size, page_size, decode_query_len,
                          max_decode_query_len, 1 if enable_pdl else 0, ep, _stream(stream)),
@@ -160,6 +177,7 @@ def icp_top16_select(scores, num_valid_pages, out_scores, out_ids, *, init_block
     oip = _dev(out_ids, "out_ids", (torch.int32,), 3)
     if tuple(out_scores.shape) != (T, HEADS, TOPK) or tuple(out_ids.shape) != (T, HEADS, TOPK):
         raise ValueError("out_scores / out_ids must be [T, 4, 16]")
+    _on_current_device(scores, num_valid_pages, out_scores, out_ids)
     _check(lib.icp_top16_select(sp, T, K, np_, init_blocks, local_blocks, index_scale,
                                 index_offset, osp, oip, _stream(stream)), "icp_top16_select")
 
@@ -186,6 +204,9 @@ def icp_publish_rows(scores, num_valid_pages, recv_bases, errors, *, slot: int, 
     if recv_bases.shape[0] != world_size:
         raise ValueError("recv_bases must be [world_size]")
     ep = _dev(errors, "errors", (torch.int32,), 1)
+    _rows_at_least(num_valid_pages, T, "num_valid_pages")
+    _rows_at_least(errors, 1, "errors")
+    _on_current_device(scores, num_valid_pages, recv_bases, errors)
     _check(lib.icp_publish_rows(sp, T, K, np_, rbp, ep, slot, rank, world_size, heads_per_rank,
                                 capacity, force_begin_blocks, force_end_blocks, spin_limit,
                                 index_scale, index_offset, 1 if enable_pdl else 0,
@@ -209,6 +230,9 @@ def icp_merge(recv, num_valid_pages, out_scores, out_ids, errors, *, T: int, slo
             tuple(out_ids.shape) != (T, heads_per_rank, TOPK):
         raise ValueError("out_scores / out_ids must be [T, heads_per_rank, 16]")
     ep = _dev(errors, "errors", (torch.int32,), 1)
+    _rows_at_least(num_valid_pages, T, "num_valid_pages")
+    _rows_at_least(errors, 1, "errors")
+    _on_current_device(recv, num_valid_pages, out_scores, out_ids, errors)
     _check(lib.icp_merge(rp, np_, T, slot, world_size, heads_per_rank, capacity, init_blocks,
                          local_blocks, spin_limit, ep, osp, oip, 1 if enable_pdl else 0,
                          _stream(stream)), "icp_merge")
@@ -249,6 +273,10 @@ def icp_score_select(index_q, index_k, block_table, seq_lens, num_valid_pages, o
         raise ValueError("out_scores / out_ids must be [T, 4, 16]")
     wp = _dev(workspace, "workspace", (torch.uint8,), 1)
     ep = 0 if errors is None else _dev(errors, "errors", (torch.int32,), 1)
+    _rows_at_least(block_table, B, "block_table")
+    _rows_at_least(num_valid_pages, T, "num_valid_pages")
+    _on_current_device(index_q, index_k, block_table, seq_lens, num_valid_pages, out_scores,
+                       out_ids, workspace, errors)
     _check(lib.icp_score_select(qp, kp, index_k.shape[0], btp, block_table.stride(0), slp, B,
                                 cols, rank, world_size, page_size, decode_query_len,
                                 max_decode_query_len, np_, init_blocks, local_blocks, wp,
@@ -273,6 +301,8 @@ def icp_publish_rows_tagged(scores, num_valid_pages, recv_bases, generations, *,
     gp = _dev(generations, "generations", (torch.int32,), 3)
     if tuple(generations.shape) != (3, world_size * heads_per_rank, capacity):
         raise ValueError("generations must be [3, world_size * heads_per_rank, capacity]")
+    _rows_at_least(num_valid_pages, T, "num_valid_pages")
+    _on_current_device(scores, num_valid_pages, recv_bases, generations)
     _check(lib.icp_publish_rows_tagged(sp, T, K, np_, rbp, gp, slot, rank, world_size,
                                        heads_per_rank, capacity, force_begin_blocks,
                                        force_end_blocks, index_scale, index_offset,
@@ -298,6 +328,9 @@ def icp_merge_tagged(recv, expected, num_valid_pages, out_scores, out_ids, error
             tuple(out_ids.shape) != (T, heads_per_rank, TOPK):
         raise ValueError("out_scores / out_ids must be [T, heads_per_rank, 16]")
     erp = _dev(errors, "errors", (torch.int32,), 1)
+    _rows_at_least(num_valid_pages, T, "num_valid_pages")
+    _rows_at_least(errors, 1, "errors")
+    _on_current_device(recv, expected, num_valid_pages, out_scores, out_ids, errors)
     _check(lib.icp_merge_tagged(rp, ep_, np_, T, slot, world_size, heads_per_rank, capacity,
                                 init_blocks, local_blocks, spin_limit, erp, osp, oip,
                                 1 if enable_pdl else 0, _stream(stream)), "icp_merge_tagged")
@@ -332,6 +365,10 @@ def icp_score_select_noalloc(index_q, index_k, block_table, seq_lens, num_valid_
     if tuple(out_scores.shape) != (T, HEADS, TOPK) or tuple(out_ids.shape) != (T, HEADS, TOPK):
         raise ValueError("out_scores / out_ids must be [T, 4, 16]")
     ep = 0 if errors is None else _dev(errors, "errors", (torch.int32,), 1)
+    _rows_at_least(block_table, B, "block_table")
+    _rows_at_least(num_valid_pages, T, "num_valid_pages")
+    _on_current_device(index_q, index_k, block_table, seq_lens, num_valid_pages, out_scores,
+                       out_ids, errors)
     _check(lib.icp_score_select_noalloc(qp, kp, index_k.shape[0], btp, block_table.stride(0),
                                         slp, B, cols, rank, world_size, page_size,
                                         decode_query_len, max_decode_query_len, np_,
@@ -352,7 +389,7 @@ def icp_prefill_plan_words(batch: int, T: int) -> int:
 
 
 def icp_prefill_plan(qo_indptr, seq_lens, plan, *, T: int, errors=None, stream=None):
-    """prefill_window_plan: records of up to 8 tokens of every request's chunk into plan."""
+    """prefill_window_plan: every request's chunk as records of up to 64 tokens, into plan."""
     B = seq_lens.shape[0]
     qp = _dev(qo_indptr, "qo_indptr", (torch.int32,), 1)
     if qo_indptr.shape[0] != B + 1:
@@ -360,6 +397,7 @@ def icp_prefill_plan(qo_indptr, seq_lens, plan, *, T: int, errors=None, stream=N
     slp = _dev(seq_lens, "seq_lens", (torch.int32,), 1)
     pp = _dev(plan, "plan", (torch.int32,), 1)
     ep = 0 if errors is None else _dev(errors, "errors", (torch.int32,), 1)
+    _on_current_device(qo_indptr, seq_lens, plan, errors)
     _check(lib.icp_prefill_plan(qp, slp, B, int(T), pp, plan.numel(), ep, _stream(stream)),
            "icp_prefill_plan")
 
@@ -382,6 +420,7 @@ def icp_prefill_score(index_q, index_k, block_table, plan, score_out, *, rank: i
     if score_out.shape[0] != T or score_out.shape[1] != HEADS:
         raise ValueError(f"score_out must be [{T}, 4, cols]")
     ep = 0 if errors is None else _dev(errors, "errors", (torch.int32,), 1)
+    _on_current_device(index_q, index_k, block_table, plan, score_out, errors)
     _check(lib.icp_prefill_score(qp, kp, index_k.shape[0], btp, block_table.stride(0), pp,
                                  plan.numel(), sop, T, score_out.shape[2], rank, world_size,
                                  page_size, ep, _stream(stream)), "icp_prefill_score")
@@ -399,6 +438,8 @@ def icp_prefill_select(scores, num_valid_pages, carrier, *, world_size: int,
     cp = _dev(carrier, "carrier", (torch.int32,), 4)
     if tuple(carrier.shape) != (world_size, T, heads_per_rank, CARRIER_WORDS):
         raise ValueError("carrier must be [world_size, T, heads_per_rank, 32]")
+    _rows_at_least(num_valid_pages, T, "num_valid_pages")
+    _on_current_device(scores, num_valid_pages, carrier)
     _check(lib.icp_prefill_select(sp, T, K, np_, world_size, heads_per_rank, init_blocks,
                                   local_blocks, index_scale, index_offset, cp, _stream(stream)),
            "icp_prefill_select")
@@ -416,5 +457,7 @@ def icp_prefill_merge(received, num_valid_pages, out_scores, out_ids, *, world_s
     oip = _dev(out_ids, "out_ids", (torch.int32,), 3)
     if tuple(out_scores.shape) != (T, hpr, TOPK) or tuple(out_ids.shape) != (T, hpr, TOPK):
         raise ValueError("out_scores / out_ids must be [T, heads_per_rank, 16]")
+    _rows_at_least(num_valid_pages, T, "num_valid_pages")
+    _on_current_device(received, num_valid_pages, out_scores, out_ids)
     _check(lib.icp_prefill_merge(rp, np_, T, world_size, heads_per_rank, init_blocks,
                                  local_blocks, osp, oip, _stream(stream)), "icp_prefill_merge")
