@@ -149,3 +149,18 @@ def test_prefill_sizes_and_checks(lib):
     lib.icp_prefill_merge.argtypes = [P, P] + [ctypes.c_int] * 5 + [P, P, P]
     assert lib.icp_prefill_merge(a, a, 4, 3, 1, 1, 2, a, a, None) == INVALID
     assert lib.icp_prefill_merge(a, a, 4, 4, 1, 9, 8, a, a, None) == INVALID
+
+
+def test_binding_fails_loudly_without_the_library(tmp_path):
+    # a copy of the binding beside no _lib/libicp.so must refuse to import
+    import shutil
+    import subprocess
+    import sys
+    pkg = tmp_path / "pkg"
+    pkg.mkdir()
+    (pkg / "__init__.py").write_text("")
+    shutil.copy(os.path.join(ROOT, "sparse_attention_block_gb300", "icp.py"), pkg / "icp.py")
+    r = subprocess.run([sys.executable, "-c", "import pkg.icp"], cwd=tmp_path,
+                       capture_output=True, text=True, timeout=300)
+    assert r.returncode != 0
+    assert "ImportError" in r.stderr and "libicp.so is missing" in r.stderr
