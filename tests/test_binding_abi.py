@@ -61,3 +61,26 @@ def test_binding_matches_the_header(binding):
             assert fn.restype is ctypes.c_char_p, name
         else:
             assert ctypes.sizeof(fn.restype) == ctypes.sizeof(_ctype(ret + " r")), name
+
+
+class _FakeTensor:
+    """Just what the binding's device and row checks look at."""
+
+    def __init__(self, device_index, rows):
+        self._index = device_index
+        self.device = f"cuda:{device_index}"
+        self.shape = (rows,)
+
+    def get_device(self):
+        return self._index
+
+
+def test_device_and_row_checks(binding, monkeypatch):
+    import torch
+    monkeypatch.setattr(torch.cuda, "current_device", lambda: 1)
+    binding._on_current_device(_FakeTensor(1, 4), None, _FakeTensor(1, 2))
+    with pytest.raises(ValueError, match="current device is cuda:1"):
+        binding._on_current_device(_FakeTensor(1, 4), _FakeTensor(0, 4))
+    binding._rows_at_least(_FakeTensor(1, 5), 5, "num_valid_pages")
+    with pytest.raises(ValueError, match="the call reads 6"):
+        binding._rows_at_least(_FakeTensor(1, 5), 6, "num_valid_pages")
