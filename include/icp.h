@@ -23,7 +23,9 @@
  *     is not an sm_103 GPU, ICP_ERR_CUDA when a CUDA call or launch fails.
  *   - Device-side waits are bounded; a wait that runs out adds 1 to errors[0]
  *     (when `errors` is not NULL) and the kernel returns without trapping.
- *     The caller reads errors[0] after its own synchronization.
+ *     The caller reads errors[0] after its own synchronization; a non-zero
+ *     count maps to ICP_ERR_TIMEOUT, a status no entry point returns itself
+ *     (none of them waits for the device).
  */
 #ifndef ICP_H
 #define ICP_H
@@ -39,6 +41,7 @@ extern "C" {
 #define ICP_ERR_INVALID_ARG 1
 #define ICP_ERR_CUDA 2
 #define ICP_ERR_UNSUPPORTED 3
+#define ICP_ERR_TIMEOUT 4  /* for callers: errors[0] > 0 after their own sync */
 
 #define ICP_HEADS 4        /* index heads (prepare_msa_icp_indexer: num_index_heads must be 4) */
 #define ICP_DIM 128        /* fp8 values per index query / key row */

@@ -132,6 +132,7 @@ const char *icp_status_string(int status) {
     case ICP_ERR_INVALID_ARG: return "invalid argument";
     case ICP_ERR_CUDA: return "CUDA error";
     case ICP_ERR_UNSUPPORTED: return "unsupported device (needs sm_103)";
+    case ICP_ERR_TIMEOUT: return "a bounded device wait timed out (errors > 0)";
     default: return "unknown status";
   }
 }

@@ -27,7 +27,7 @@ HEADS, DIM, TOPK, ROW_WORDS = 4, 128, 16, 33
 MAX_COLS, MAX_K, MAX_BATCH = 8192, 12287, 4096
 DEFAULT_SPIN_LIMIT = 67108864
 
-OK, ERR_INVALID_ARG, ERR_CUDA, ERR_UNSUPPORTED = 0, 1, 2, 3
+OK, ERR_INVALID_ARG, ERR_CUDA, ERR_UNSUPPORTED, ERR_TIMEOUT = 0, 1, 2, 3, 4
 
 _P, _I32, _I64, _SZ = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_size_t
 
@@ -83,6 +83,15 @@ class IcpError(RuntimeError):
 def _check(status: int, where: str):
     if status != OK:
         raise IcpError(status, where)
+
+
+def icp_check_errors(errors, where: str = "icp"):
+    """Reads the `errors` counter (a device-to-host copy, so it waits for the
+    work queued before it) and raises IcpError(ERR_TIMEOUT) when a bounded
+    device wait ran out.  Not for the hot path: call it where the caller
+    synchronizes anyway."""
+    if int(errors.sum().item()) > 0:
+        raise IcpError(ERR_TIMEOUT, where)
 
 
 def _stream(stream):

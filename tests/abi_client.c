@@ -31,6 +31,8 @@ int main(void) {
   CHECK(strcmp(icp_status_string(ICP_OK), "ok") == 0);
   CHECK(icp_status_string(ICP_ERR_INVALID_ARG) != NULL);
   CHECK(icp_status_string(12345) != NULL);
+  CHECK(strstr(icp_status_string(ICP_ERR_TIMEOUT), "timed out") != NULL);
+  CHECK(ICP_ERR_TIMEOUT != ICP_ERR_CUDA && ICP_ERR_TIMEOUT != ICP_ERR_UNSUPPORTED);
 
   /* plane width: B128 blocks (or local pages), padded to a multiple of 4 */
   CHECK(icp_score_columns(1000, 128, 1) == 8);

@@ -84,3 +84,12 @@ def test_device_and_row_checks(binding, monkeypatch):
     binding._rows_at_least(_FakeTensor(1, 5), 5, "num_valid_pages")
     with pytest.raises(ValueError, match="the call reads 6"):
         binding._rows_at_least(_FakeTensor(1, 5), 6, "num_valid_pages")
+
+
+def test_error_counter_maps_to_the_timeout_status(binding):
+    import torch
+    binding.icp_check_errors(torch.zeros(1, dtype=torch.int32))
+    with pytest.raises(binding.IcpError) as e:
+        binding.icp_check_errors(torch.tensor([2], dtype=torch.int32), "icp_merge")
+    assert e.value.status == binding.ERR_TIMEOUT
+    assert "icp_merge" in str(e.value) and "timed out" in str(e.value)
