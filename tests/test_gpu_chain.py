@@ -7,7 +7,7 @@ import torch
 import oracle
 from sparse_attention_block_gb300 import workloads as W
 
-from gpu_util import assert_select_equal, gpu_score, gpu_select, icp, to_dev
+from gpu_util import gpu_score, gpu_select, icp, to_dev
 
 pytestmark = pytest.mark.gpu
 

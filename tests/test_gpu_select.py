@@ -1,6 +1,5 @@
 """icp_top16_select (CUDA) against the oracle's select run on the same plane:
 ids and score bits must be identical."""
-import numpy as np
 import pytest
 import torch
 
