@@ -76,7 +76,10 @@ int icp_score_columns(int max_seq_len, int page_size, int world_size);
  *                of every page.
  *   block_table  int32 [batch, >= ceil(seq_len / page_size)], unit last stride,
  *                row stride block_table_stride (elements); entries must lie in
- *                [0, num_pages) (an entry outside reads as zero keys).
+ *                [0, num_pages).  An entry outside is read as a page of zero
+ *                keys, and every request whose pages hold such an entry adds 1
+ *                to errors[0] (once per request and call, when errors is not
+ *                NULL).
  *   seq_lens     int32 [batch].
  *   score_out    float32 [batch * decode_query_len, 4, cols], contiguous.  For
  *                each request only columns c < round_up(n, 4) are written, n
@@ -98,7 +101,9 @@ int icp_score_columns(int max_seq_len, int page_size, int world_size);
  *   alone, and that it is either an ordinary launch or one that waits for its
  *   own predecessor before it signals its dependents.
  *   0 removes the requirement.
- *   errors: optional int32 [>= 1] counter for timed-out internal waits.
+ *   errors: optional int32 [>= 1] counter of timed-out internal waits,
+ *           requests with block-table entries outside the pool, and requests
+ *           wider than the plane.
  */
 int icp_score(const uint8_t *index_q, const uint8_t *index_k, int64_t num_pages,
               const int32_t *block_table, int64_t block_table_stride, const int32_t *seq_lens,
@@ -267,12 +272,17 @@ int icp_score_select(const uint8_t *index_q, const uint8_t *index_k, int64_t num
  * by every GPU that loads this library until the process exits.  Nothing is
  * allocated or freed by the call.
  *   - Limit: accepted when icp_score_select_workspace_bytes(batch,
- *     decode_query_len) <= ICP_NOALLOC_SCRATCH_BYTES (for example up to 128
- *     requests of 4 tokens, or 8 requests of 8 tokens); a larger batch returns
- *     ICP_ERR_INVALID_ARG and launches nothing.
+ *     decode_query_len) <= ICP_NOALLOC_SCRATCH_BYTES, which allows at most
+ *     1654, 748, 446, 294, 203, 143, 100 or 67 requests at decode_query_len
+ *     1 to 8; a larger batch returns ICP_ERR_INVALID_ARG and launches
+ *     nothing.
  *   - The first call on each device looks up the array's device address
  *     (cudaGetSymbolAddress, with that device current); make that first call
- *     before any stream capture begins.
+ *     before any stream capture begins.  The address is kept for the life of
+ *     the process and belongs to the device's primary context, the one the
+ *     CUDA runtime uses: after cudaDeviceReset, or from another context on
+ *     that device, it is stale, so such a caller must not use this entry
+ *     point.
  *   - All calls on a device share the array and it keeps what the last call
  *     left; no part of it needs clearing, but calls that overlap on the GPU
  *     race on it, so the caller must not run two at once.

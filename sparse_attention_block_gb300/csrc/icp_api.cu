@@ -166,6 +166,7 @@ int icp_score(const uint8_t *index_q, const uint8_t *index_k, int64_t num_pages,
   memset(&a, 0, sizeof(a));
   a.block_table = block_table;
   a.bt_stride = block_table_stride;
+  a.num_pages = (int)num_pages;
   a.seq_lens = seq_lens;
   a.score_out = score_out;
   a.errors = errors;
@@ -388,6 +389,7 @@ int icp_score_select(const uint8_t *index_q, const uint8_t *index_k, int64_t num
   memset(&a, 0, sizeof(a));
   a.block_table = block_table;
   a.bt_stride = block_table_stride;
+  a.num_pages = (int)num_pages;
   a.seq_lens = seq_lens;
   a.errors = errors;
   a.batch = batch;
@@ -466,6 +468,7 @@ int icp_prefill_score(const uint8_t *index_q, const uint8_t *index_k, int64_t nu
   memset(&a, 0, sizeof(a));
   a.block_table = block_table;
   a.bt_stride = block_table_stride;
+  a.num_pages = (int)num_pages;
   a.score_out = score_out;
   a.errors = errors;
   a.batch = capacity;

@@ -29,6 +29,7 @@ struct ScoreArgs {
   float *score_out;  // plane (icp_score only)
   int32_t *errors;
   int batch, cols, rank, world_size, page_size, dql;
+  int num_pages;  // pages of the index-K shard: valid block-table entries are below it
   ScoreGeom g;
   int pdl;  // launched with programmatic dependent launch (early start)
   // fused scorer + select only

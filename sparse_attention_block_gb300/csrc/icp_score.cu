@@ -35,6 +35,8 @@
 // Products of two e4m3 values are exact in fp32; the MMA sums 128 of them in
 // fp32.  The per-key arithmetic does not depend on where the key sits in the
 // tile, so sharded and unsharded layouts give identical key scores.
+#include <climits>
+
 #include "icp_device.cuh"
 #include "icp_fused.cuh"
 #include "icp_internal.h"
@@ -159,6 +161,28 @@ __device__ __forceinline__ ReqView req_view(const ScoreArgs &a, int b) {
   return ReqView{sl, b * a.dql, b, a.dql, sl};
 }
 __device__ __forceinline__ int row_off_of(int c, int split) { return split ? (c & 1) * 128 : 0; }
+
+// Counts a request whose block table holds an entry outside [0, num_pages)
+// once per call: fb is the first such column a producer warp met in its
+// segment of request (or plan record) b.  The warp that met the request's
+// first bad page counts it: no earlier page of the row may be bad, and for a
+// plan record the preceding record of the same request (which covers a
+// prefix of the same columns) must not reach that column.
+__device__ __noinline__ void count_bad_entry(const ScoreArgs &a, int b, const ReqView &rv,
+                                             const int32_t *btrow, int fb, int lane) {
+  if (fb == INT_MAX || !a.errors) return;
+  const ScoreGeom &g = a.g;
+  const int slot = page_slot_of(fb, g.split);
+  bool earlier = false;
+  for (int i = lane; i < slot && !earlier; i += 32)
+    earlier = (unsigned)btrow[i] >= (unsigned)a.num_pages;
+  earlier = __any_sync(0xFFFFFFFFu, earlier);
+  if (!earlier && a.vreq && b > 0) {
+    const ReqView pv = req_view(a, b - 1);
+    earlier = pv.bt_row == rv.bt_row && fb < units_of(pv.seq_len, a.page_size, g.split);
+  }
+  if (!earlier && lane == 0) atomicAdd(a.errors, 1);
+}
 
 // Per-lane running Top16 of one query row over the columns a warp has seen.
 struct LaneTop {
@@ -423,19 +447,24 @@ score_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CU
       // tiles of this CTA into L2, only from pages lying wholly below
       // position seq_len - dql (the newest keys may still be appended by the
       // preceding kernel); every real load below is issued after the wait.
+      // The first 2 * kStages tiles' columns are spread over the lanes, so
+      // their block-table reads are in flight together.
       SegmentWalker pw(prefix, nbatch, g0, g1, WIDE ? kWideRequestUnits : 0);
-      int pb, p0, p1, budget = 2 * kStages;
+      int pb, p0, p1, budget = 2 * kStages * g.cpt;  // columns
       while (budget > 0 && pw.next(pb, p0, p1)) {
         const ReqView rv = req_view(a, pb);
         const int nunits = units_of(rv.seq_len, a.page_size, g.split);
         const int32_t *btrow = a.block_table + (long long)rv.bt_row * a.bt_stride;
         const long long safe_end = (long long)rv.seq_len - rv.ntok;
-        for (int tl = p0; tl < p1 && budget > 0; ++tl, --budget) {
-          const int c = tl * g.cpt + lane;
-          if (lane < g.cpt && c < nunits) {
-            const int slot = page_slot_of(c, g.split);
-            if ((long long)(slot + 1) * a.page_size <= safe_end)
-              tma_prefetch_l2_2d(&tmk, 0, btrow[slot] * g.rows_per_page + row_off_of(c, g.split));
+        const int c0 = p0 * g.cpt;
+        const int c1 = min(min(p1 * g.cpt, nunits), c0 + budget);
+        budget -= max(c1 - c0, 1);
+        for (int c = c0 + lane; c < c1; c += 32) {
+          const int slot = page_slot_of(c, g.split);
+          if ((long long)(slot + 1) * a.page_size <= safe_end) {
+            const int pg = btrow[slot];
+            if ((unsigned)pg < (unsigned)a.num_pages)
+              tma_prefetch_l2_2d(&tmk, 0, pg * g.rows_per_page + row_off_of(c, g.split));
           }
         }
       }
@@ -465,14 +494,28 @@ score_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CU
       const int cbeg = t0 * g.cpt;
       const int cend = min(t1 * g.cpt, nunits);
       const int32_t *btrow = a.block_table + (long long)rv.bt_row * a.bt_stride;
+      // A table entry outside [0, num_pages) is replaced by num_pages, whose
+      // rows lie past the end of the tensor map: the box reads as zeros.  The
+      // lane notes the first such column it met (an entry is vetted when it
+      // is first used, so the load stays in flight until then; at P256 with
+      // world_size 1 a page feeds two columns and only the even one counts).
+      int first_bad = INT_MAX;
+      auto vet = [&](int pg, int c) {
+        if ((unsigned)pg >= (unsigned)a.num_pages) {
+          if (c < cend && !(g.split && (c & 1))) first_bad = min(first_bad, c);
+          return a.num_pages;
+        }
+        return pg;
+      };
       int grp = cbeg;
       int pg_cur = (cbeg + lane < cend) ? btrow[page_slot_of(cbeg + lane, g.split)] : 0;
       int pg_nxt = (cbeg + 32 + lane < cend) ? btrow[page_slot_of(cbeg + 32 + lane, g.split)] : 0;
+      pg_cur = vet(pg_cur, cbeg + lane);
       for (int tl = t0; tl < t1; ++tl) {
         const int c0 = tl * g.cpt;
         if (c0 >= grp + 32) {
           grp += 32;
-          pg_cur = pg_nxt;
+          pg_cur = vet(pg_nxt, grp + lane);
           pg_nxt = (grp + 32 + lane < cend) ? btrow[page_slot_of(grp + 32 + lane, g.split)] : 0;
         }
         const int ncol = min(g.cpt, cend - c0);
@@ -514,6 +557,7 @@ score_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CU
           }
         }
       }
+      if (ok) count_bad_entry(a, b, rv, btrow, __reduce_min_sync(0xFFFFFFFFu, first_bad), lane);
     }
     if (*abort_flag && lane == 0) {
       // let copies still in flight land before the CTA exits

@@ -84,31 +84,111 @@ def test_block_table_with_row_stride_and_zero_length_requests():
     assert_plane_matches(gp, ex, ab, "strided table")
 
 
-@pytest.mark.parametrize("page_size", [128, 256])
-def test_block_table_entries_outside_the_pool_read_as_zero_keys(page_size):
-    # entries past the pool and below 0 inside each request's pages: the
-    # tensor map fills those rows with zeros, so the plane must equal the
-    # oracle's plane with the entries pointing at an all-zero page
-    spec, inp = _case(page_size, 1, 2, [700, 300], seed=5)
+def _bad_table_case(page_size):
+    """Requests whose block tables hold entries outside the pool: request 0
+    two of them, request 1 one, request 3 two far apart (so that different
+    CTAs read them); request 2 none.  Returns the case, the bad table, the
+    oracle's reading of it (the entries point at an extra all-zero page) and
+    the number of requests holding a bad entry."""
+    seq_lens = [700, 300, 500, 20000]
+    spec, inp = _case(page_size, 1, 2, seq_lens, seed=5)
     num_pages = inp.index_k.shape[0]
     bt = inp.block_table.clone()
-    bt[0, 1] = num_pages + 7
-    bt[0, 2] = num_pages
-    bt[1, 0] = -2
+    far = (100, 140) if page_size == 128 else (40, 70)
+    bad = [(0, 1, num_pages + 7), (0, 2, num_pages), (1, 0, -2), (3, far[0], -1),
+           (3, far[1], 1 << 30)]
+    for b, j, v in bad:
+        bt[b, j] = v
     kz = torch.cat([inp.index_k, torch.zeros((1,) + tuple(inp.index_k.shape[1:]),
                                              dtype=torch.uint8)])
     bz = bt.clone()
-    bz[0, 1] = bz[0, 2] = bz[1, 0] = num_pages
+    for b, j, _ in bad:
+        bz[b, j] = num_pages
+    return spec, inp, bt, kz, bz, len({b for b, _, _ in bad})
+
+
+@pytest.mark.parametrize("page_size", [128, 256])
+@pytest.mark.parametrize("pdl", [False, True])
+def test_block_table_entries_outside_the_pool_are_counted_and_read_as_zero_keys(page_size, pdl):
+    # the tensor map fills those rows with zeros, so the plane must equal the
+    # oracle's plane with the entries pointing at an all-zero page; errors
+    # counts each request that holds such an entry once
+    from gpu_util import icp, sentinel_plane
+    spec, inp, bt, kz, bz, nbad = _bad_table_case(page_size)
     q, k, _, sl, _ = to_dev(inp)
     errors = torch.zeros(1, dtype=torch.int32, device="cuda")
-    cols = W.columns_for(spec, 700)
-    gp = gpu_score(q, k, bt.cuda(), sl, cols=cols, rank=0, world_size=1, page_size=page_size,
-                   dql=2, errors=errors)
+    cols = W.columns_for(spec, int(inp.seq_lens.max()))
+    gp = sentinel_plane(inp.T, cols)
+    icp().icp_score(q, k, bt.cuda(), sl, gp, rank=0, world_size=1, page_size=page_size,
+                    decode_query_len=2, max_decode_query_len=2, enable_pdl=pdl, errors=errors)
     torch.cuda.synchronize()
-    assert int(errors.item()) == 0
+    assert int(errors.item()) == nbad
     ex, ab = oracle_plane(inp.index_q, kz, bz, inp.seq_lens, cols=cols, rank=0, world_size=1,
                           page_size=page_size, dql=2)
     assert_plane_matches(gp, ex, ab, f"pages outside the pool, P{page_size}")
+
+
+@pytest.mark.parametrize("page_size", [128, 256])
+def test_fused_path_counts_block_table_entries_outside_the_pool(page_size):
+    from gpu_util import gpu_select, icp
+    spec, inp, bt, _, _, nbad = _bad_table_case(page_size)
+    q, k, _, sl, nvp = to_dev(inp)
+    btd = bt.cuda()
+    cols = W.columns_for(spec, int(inp.seq_lens.max()))
+    T = inp.T
+    errors = torch.zeros(1, dtype=torch.int32, device="cuda")
+    work = torch.empty((icp().icp_score_select_workspace_bytes(4, 2),), dtype=torch.uint8,
+                       device="cuda")
+    fs = torch.empty((T, 4, 16), device="cuda")
+    fi = torch.empty((T, 4, 16), dtype=torch.int32, device="cuda")
+    icp().icp_score_select(q, k, btd, sl, nvp, fs, fi, work, cols=cols, rank=0, world_size=1,
+                           page_size=page_size, decode_query_len=2, max_decode_query_len=2,
+                           init_blocks=1, local_blocks=2, errors=errors)
+    torch.cuda.synchronize()
+    assert int(errors.item()) == nbad
+    gp = gpu_score(q, k, btd, sl, cols=cols, rank=0, world_size=1, page_size=page_size, dql=2)
+    s, i = gpu_select(gp, nvp, init=1, local=2)
+    torch.cuda.synchronize()
+    assert torch.equal(fi, i) and torch.equal(fs.view(torch.int32), s.view(torch.int32))
+
+
+def test_prefill_window_counts_a_request_with_bad_entries_once():
+    # request 0's 150-token chunk is three plan records that all read its
+    # early pages; request 1's bad page is reached only by its later records
+    from gpu_util import icp, sentinel_plane
+    seq_lens, chunks = [3000, 9000], [150, 130]
+    spec = W.DecodeSpec("w", batch=2, page_size=128, world_size=1, decode_query_len=1,
+                        max_decode_query_len=1, init_blocks=1, local_blocks=3,
+                        seq_lens=tuple(seq_lens))
+    inp = W.make_decode_inputs(spec, seed=8)
+    num_pages = inp.index_k.shape[0]
+    bt = inp.block_table.clone()
+    bt[0, 3] = -4
+    bt[0, 20] = num_pages
+    last = (9000 - 130 + 64) // 128 + 1            # past the first record's last column
+    bt[1, last] = num_pages + 1
+    T = sum(chunks)
+    g = torch.Generator().manual_seed(8)
+    q = (0.5 * torch.randn((T, 4, 128), generator=g) + 1.5 * inp.u).to(
+        torch.float8_e4m3fn).view(torch.uint8)
+    qo = torch.tensor([0, chunks[0], T], dtype=torch.int32, device="cuda")
+    cols = W.columns_for(spec, max(seq_lens))
+    plan = torch.empty((icp().icp_prefill_plan_words(2, T),), dtype=torch.int32, device="cuda")
+    errors = torch.zeros(1, dtype=torch.int32, device="cuda")
+    icp().icp_prefill_plan(qo, inp.seq_lens.cuda(), plan, T=T, errors=errors)
+    gp = sentinel_plane(T, cols)
+    icp().icp_prefill_score(q.cuda(), inp.index_k.cuda(), bt.cuda(), plan, gp, rank=0,
+                            world_size=1, page_size=128, errors=errors)
+    torch.cuda.synchronize()
+    assert int(errors.item()) == 2
+    import oracle
+    kz = torch.cat([inp.index_k, torch.zeros((1, 128, 128), dtype=torch.uint8)])
+    bz = bt.clone()
+    bz[0, 3] = bz[0, 20] = bz[1, last] = num_pages
+    ex, ab = oracle.score_chunks(q.numpy(), kz.numpy(), bz.numpy(), inp.seq_lens.numpy(),
+                                 qo.cpu().numpy(), cols=cols, rank=0, world_size=1,
+                                 page_size=128)
+    assert_plane_matches(gp, ex, ab, "prefill window with pages outside the pool")
 
 
 def test_extreme_fp8_values_stay_within_tolerance():
