@@ -1,4 +1,4 @@
-"""Times the oracle's decode chain over several host cores (test infrastructure).
+"""Runs the oracle over several host cores (test infrastructure).
 
 The CPU baseline runs the oracle as it is, request by request:
 - the score plane of the request (``score``), one per shard;
@@ -7,8 +7,10 @@ The CPU baseline runs the oracle as it is, request by request:
 
 This module computes nothing of its own. ``decode_request`` is that chain
 for one request. ``ParallelChain`` runs it over the requests of a batch in
-worker processes started with ``spawn``. The batch's arrays (the index-K
-shards above all) sit in shared memory, so no worker copies them.
+worker processes started with ``spawn``. ``PlanePool`` gives the tests the
+oracle's exact score plane of a whole full-size batch the same way, one
+request (or one slice of a prefill chunk) per task.  The batch's arrays (the
+index-K shards above all) sit in shared memory, so no worker copies them.
 """
 from __future__ import annotations
 
@@ -19,7 +21,7 @@ from multiprocessing import shared_memory
 
 import numpy as np
 
-from . import merge, publish, score
+from . import merge, publish, score, score_chunks
 
 
 def decode_request(q, shards, bt, sl, nvp, b, *, cols, world_size, page_size, decode_query_len,
@@ -102,6 +104,110 @@ class ParallelChain:
         t0 = time.perf_counter()
         self._pool.map(_run, parts, chunksize=1)
         return time.perf_counter() - t0
+
+    def close(self):
+        self._pool.close()
+        self._pool.join()
+        for shm in self._shms:
+            shm.close()
+            shm.unlink()
+
+    def __enter__(self):
+        return self
+
+    def __exit__(self, *exc):
+        self.close()
+
+
+# ---------------------------------------------------------------- planes
+def _plane_task(task):
+    """One request's rows of the exact plane (oracle.score on its own
+    block-table row), or one slice of a prefill chunk (oracle.score_chunks
+    on the tokens j0 .. j1 - 1 of request b's chunk of n tokens, which sit at
+    positions seq_len - n + j0 .. seq_len - n + j1 - 1: a window of its own
+    whose request length ends at the last of them)."""
+    a = _W["arrays"]
+    k = a[f"shard{task['k']}"]
+    b = task["b"]
+    if task["kind"] == "decode":
+        dql = task["dql"]
+        plane, absplane = score(a["q"][b * dql:(b + 1) * dql], k, a["bt"][b:b + 1],
+                                a["sl"][b:b + 1], cols=task["cols"], rank=task["rank"],
+                                world_size=task["world_size"], page_size=task["page_size"],
+                                decode_query_len=dql, fill=np.nan)
+        return task, plane, absplane
+    j0, j1, n, q0 = task["j0"], task["j1"], task["n"], task["q0"]
+    L = int(a["sl"][b])
+    plane, absplane = score_chunks(a["q"][q0 + j0:q0 + j1], k, a["bt"][b:b + 1],
+                                   np.array([L - n + j1], np.int32),
+                                   np.array([0, j1 - j0], np.int32), cols=task["cols"], rank=0,
+                                   world_size=1, page_size=task["page_size"], fill=np.nan)
+    return task, plane, absplane
+
+
+class PlanePool:
+    """The oracle's exact score planes of a batch, computed by spawned worker
+    processes over the batch held in shared memory.
+
+    q: uint8 [T, 4, 128]; ks: list of index-K arrays (the shards of a sharded
+    cache, or the whole cache); bt: int32 [B, W]; sl: int32 [B].
+    """
+
+    def __init__(self, q, ks, bt, sl, workers=None):
+        self.workers = workers or os.cpu_count() or 1
+        self._shms = []
+        desc = {"arrays": {}, "params": {}, "nshards": len(ks)}
+        named = {"q": q, "bt": bt, "sl": sl, "nvp": np.zeros(1, np.int32)}
+        named.update({f"shard{r}": kk for r, kk in enumerate(ks)})
+        for name, arr in named.items():
+            arr = np.ascontiguousarray(arr)
+            shm = shared_memory.SharedMemory(create=True, size=max(arr.nbytes, 1))
+            np.ndarray(arr.shape, dtype=arr.dtype, buffer=shm.buf)[...] = arr
+            self._shms.append(shm)
+            desc["arrays"][name] = (shm.name, arr.shape, arr.dtype.str)
+        self.sl = np.asarray(sl)
+        self.T_rows = np.asarray(q).shape[0]
+        ctx = mp.get_context("spawn")
+        self._pool = ctx.Pool(self.workers, initializer=_attach, initargs=(desc,))
+
+    def decode_plane(self, *, k, cols, rank, world_size, page_size, decode_query_len,
+                     requests=None):
+        """Exact plane float64 [B * dql, 4, cols] (NaN where not written) and
+        its |q.k| scale plane, as oracle.score over the whole batch would
+        give them, computed request by request (a request's rows depend only
+        on its own block-table row and seq_len)."""
+        dql = decode_query_len
+        B = len(self.sl)
+        reqs = range(B) if requests is None else requests
+        # longest requests first, so that the pool ends together
+        order = sorted(reqs, key=lambda b: -int(self.sl[b]))
+        tasks = [dict(kind="decode", k=k, b=b, cols=cols, rank=rank, world_size=world_size,
+                      page_size=page_size, dql=dql) for b in order]
+        plane = np.full((B * dql, 4, cols), np.nan)
+        absplane = np.full((B * dql, 4, cols), np.nan)
+        for task, p, ab in self._pool.imap_unordered(_plane_task, tasks, chunksize=1):
+            b = task["b"]
+            plane[b * dql:(b + 1) * dql] = p
+            absplane[b * dql:(b + 1) * dql] = ab
+        return plane, absplane
+
+    def window_slices(self, qo_indptr, *, cols, page_size, piece=128, k=0):
+        """Exact rows of a prefill window (oracle.score_chunks), in slices of
+        at most `piece` tokens of each request's chunk.  Yields
+        (b, j0, j1, plane [j1 - j0, 4, cols], absplane): the slice's tokens
+        are window rows qo[b] + j0 .. qo[b] + j1 - 1, and the slice is scored
+        as a window whose request length ends at its last token, so only the
+        columns that length reaches are written (NaN elsewhere)."""
+        qo = np.asarray(qo_indptr)
+        tasks = []
+        for b in range(len(self.sl)):
+            n = int(qo[b + 1] - qo[b])
+            for j0 in range(0, n, piece):
+                tasks.append(dict(kind="window", k=k, b=b, j0=j0, j1=min(n, j0 + piece), n=n,
+                                  q0=int(qo[b]), cols=cols, page_size=page_size))
+        tasks.sort(key=lambda t: -(int(self.sl[t["b"]]) - t["n"] + t["j1"]))
+        for task, p, ab in self._pool.imap_unordered(_plane_task, tasks, chunksize=1):
+            yield task["b"], task["j0"], task["j1"], p, ab
 
     def close(self):
         self._pool.close()

@@ -203,3 +203,62 @@ def test_window_of_uniform_chunks_equals_the_decode_scorer():
                     max_decode_query_len=8)
     torch.cuda.synchronize()
     assert torch.equal(gp.view(torch.int32), dp.view(torch.int32))
+
+
+def test_benched_prefill_window_full_size():
+    # the window bench.py --workload prefill times: B=4 requests, chunks of
+    # 2048 tokens (T = 8192, 128 plan records), drawn on the GPU with seed 0
+    from gpu_util import exact_selection_agrees
+    from oracle.parallel import PlanePool
+    spec = W.PREFILL
+    inp = W.make_decode_inputs(spec, seed=0, device="cuda")
+    q, k, bt, sl, nvp = (inp.index_q, inp.index_k, inp.block_table, inp.seq_lens,
+                         inp.num_valid_pages)
+    B, n = sl.shape[0], spec.decode_query_len
+    T = B * n
+    qo = torch.arange(0, (B + 1) * n, n, dtype=torch.int32, device="cuda")
+    cols = W.columns_for(spec, int(sl.max()))
+    errors = torch.zeros(1, dtype=torch.int32, device="cuda")
+    gp, plan = _gpu_plane(q, k, bt, sl, qo, cols=cols, rank=0, world_size=1, page_size=128,
+                          errors=errors)
+    car = torch.zeros((1, T, 4, 32), dtype=torch.int32, device="cuda")
+    icp().icp_prefill_select(gp, nvp, car, world_size=1, heads_per_rank=4,
+                             init_blocks=spec.init_blocks, local_blocks=spec.local_blocks)
+    out_s = torch.empty((T, 4, 16), device="cuda")
+    out_i = torch.empty((T, 4, 16), dtype=torch.int32, device="cuda")
+    icp().icp_prefill_merge(car, nvp, out_s, out_i, world_size=1, heads_per_rank=4,
+                            init_blocks=spec.init_blocks, local_blocks=spec.local_blocks)
+    torch.cuda.synchronize()
+    assert int(errors.item()) == 0
+    assert int(plan[0].item()) == T // 64                  # 128 records of 64 tokens
+    g = gp.cpu().numpy()
+    hn = nvp.cpu().numpy()
+    # carrier rows and merged lists: every row, bit-exact on the GPU's plane
+    ref = oracle.carrier(g, hn, world_size=1, heads_per_rank=4, init_blocks=spec.init_blocks,
+                         local_blocks=spec.local_blocks)
+    np.testing.assert_array_equal(car.cpu().numpy(), ref)
+    ms, mi = oracle.merge_carrier(ref, hn, world_size=1, heads_per_rank=4,
+                                  init_blocks=spec.init_blocks, local_blocks=spec.local_blocks)
+    np.testing.assert_array_equal(out_i.cpu().numpy(), mi)
+    np.testing.assert_array_equal(out_s.cpu().numpy().view(np.int32), ms.view(np.int32))
+    # every token's plane row against the exact window, computed over the
+    # host cores in slices of 128 tokens; a slice is scored as a window whose
+    # request ends at its last token, so the request's columns past its
+    # reach hold no visible key and are -inf (the whole-window reading)
+    hq, hk, hbt, hsl, hqo = (t.cpu().numpy() for t in (q, k, bt, sl, qo))
+    ex = np.full((T, 4, cols), np.nan)
+    ab = np.full((T, 4, cols), np.nan)
+    with PlanePool(hq, [hk], hbt, hsl) as pool:
+        for b, j0, j1, p, a in pool.window_slices(hqo, cols=cols, page_size=128, piece=128):
+            rows = slice(int(hqo[b]) + j0, int(hqo[b]) + j1)
+            wreq = W.columns_for(spec, int(hsl[b]))
+            reach = np.isnan(p) & (np.arange(cols) < wreq)[None, None, :]
+            p[reach] = -np.inf
+            a[reach] = 0.0
+            ex[rows], ab[rows] = p, a
+    assert not np.isnan(ex[:, :, 0]).any()
+    assert_plane_matches(g, ex, ab, "prefill window, every token")
+    checked, skipped = exact_selection_agrees(ex, ab, out_i.cpu().numpy(), hn, spec.init_blocks,
+                                              spec.local_blocks)
+    print(f"prefill window: exact selection checked on {checked} of {checked + skipped} rows")
+    assert checked >= 0.97 * (checked + skipped)

@@ -42,3 +42,53 @@ def test_worker_pool_runs_the_chain_over_the_requests():
     with ParallelChain(*arrays, params, workers=2) as pc:
         assert pc.workers == 2
         assert pc.time(range(len(arrays[3]))) > 0.0
+
+
+def test_plane_pool_equals_the_oracle_over_the_whole_batch():
+    from oracle.parallel import PlanePool
+    spec = W.DecodeSpec("p", batch=5, page_size=256, world_size=1, decode_query_len=3,
+                        max_decode_query_len=3, init_blocks=1, local_blocks=2,
+                        seq_lens=(1, 300, 129, 700, 2500))
+    inp = W.make_decode_inputs(spec, seed=3)
+    q, k, bt, sl = (inp.index_q.numpy(), inp.index_k.numpy(), inp.block_table.numpy(),
+                    inp.seq_lens.numpy())
+    cols = W.columns_for(spec, 2500) + 4
+    whole, whole_abs = oracle.score(q, k, bt, sl, cols=cols, rank=0, world_size=1,
+                                    page_size=256, decode_query_len=3, fill=np.nan)
+    with PlanePool(q, [k], bt, sl, workers=2) as pool:
+        plane, absplane = pool.decode_plane(k=0, cols=cols, rank=0, world_size=1,
+                                            page_size=256, decode_query_len=3)
+    np.testing.assert_array_equal(plane, whole)
+    np.testing.assert_array_equal(absplane, whole_abs)
+
+
+def test_window_slices_equal_the_whole_window():
+    # a slice of a chunk, scored as a window whose request ends at its last
+    # token, gives the whole window's rows on the columns it writes; the
+    # whole window's remaining columns of the request are -inf (no key at or
+    # before those tokens' positions)
+    from oracle.parallel import PlanePool
+    seq_lens, chunks = [300, 1000, 2600], [40, 200, 150]
+    spec = W.DecodeSpec("w", batch=3, page_size=128, world_size=1, decode_query_len=1,
+                        max_decode_query_len=1, init_blocks=1, local_blocks=3,
+                        seq_lens=tuple(seq_lens))
+    inp = W.make_decode_inputs(spec, seed=6)
+    qo = np.concatenate([[0], np.cumsum(chunks)]).astype(np.int32)
+    T = int(qo[-1])
+    rng = np.random.default_rng(6)
+    q = rng.integers(0, 0x7F, size=(T, 4, 128), dtype=np.uint8)   # finite e4m3 codes
+    k, bt, sl = inp.index_k.numpy(), inp.block_table.numpy(), inp.seq_lens.numpy()
+    cols = W.columns_for(spec, max(seq_lens))
+    whole, whole_abs = oracle.score_chunks(q, k, bt, sl, qo, cols=cols, rank=0, world_size=1,
+                                           page_size=128)
+    seen = np.zeros(T, bool)
+    with PlanePool(q, [k], bt, sl, workers=2) as pool:
+        for b, j0, j1, p, ab in pool.window_slices(qo, cols=cols, page_size=128, piece=64):
+            rows = slice(qo[b] + j0, qo[b] + j1)
+            w = ~np.isnan(p)
+            np.testing.assert_array_equal(p[w], whole[rows][w])
+            np.testing.assert_array_equal(ab[w], whole_abs[rows][w])
+            rest = np.isnan(p) & ~np.isnan(whole[rows])
+            assert np.all(np.isneginf(whole[rows][rest]))
+            seen[rows] = True
+    assert seen.all()
