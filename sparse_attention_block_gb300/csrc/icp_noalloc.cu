@@ -35,7 +35,11 @@ constexpr int kMaxDevices = 64;
 std::mutex g_scratch_mutex;
 void *g_scratch_ptr[kMaxDevices] = {};
 
-// Device address of this device's scratch array; resolved on first use.
+// Device address of this device's scratch array; resolved on first use and
+// kept for the life of the process.  It is the address in the device's
+// primary context (the CUDA runtime's); after cudaDeviceReset, or under
+// another context on the same device, it would be stale, which the header
+// tells callers.
 int scratch_for_current_device(void **out) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return ICP_ERR_CUDA;

@@ -93,3 +93,35 @@ def test_error_counter_maps_to_the_timeout_status(binding):
         binding.icp_check_errors(torch.tensor([2], dtype=torch.int32), "icp_merge")
     assert e.value.status == binding.ERR_TIMEOUT
     assert "icp_merge" in str(e.value) and "timed out" in str(e.value)
+
+
+def test_binding_constants_equal_the_header_defines(binding):
+    # the binding keeps its own copies of the header's sizes and limits
+    text = open(HEADER).read()
+    defines = {m.group(1): m.group(2) for m in
+               re.finditer(r"^#define\s+(ICP_\w+)\s+(.+?)\s*(?:/\*.*)?$", text, flags=re.M)}
+
+    def value(name):
+        return int(eval(re.sub(r"(\d+)u\b", r"\1", defines[name])))
+
+    assert binding.NOALLOC_SCRATCH_BYTES == value("ICP_NOALLOC_SCRATCH_BYTES")
+    assert (binding.HEADS, binding.DIM, binding.TOPK, binding.ROW_WORDS) == tuple(
+        value(n) for n in ("ICP_HEADS", "ICP_DIM", "ICP_TOPK", "ICP_ROW_WORDS"))
+    assert (binding.MAX_COLS, binding.MAX_K, binding.MAX_BATCH) == tuple(
+        value(n) for n in ("ICP_MAX_COLS", "ICP_MAX_K", "ICP_MAX_BATCH"))
+    assert (binding.OK, binding.ERR_INVALID_ARG, binding.ERR_CUDA, binding.ERR_UNSUPPORTED,
+            binding.ERR_TIMEOUT) == tuple(value(n) for n in (
+                "ICP_OK", "ICP_ERR_INVALID_ARG", "ICP_ERR_CUDA", "ICP_ERR_UNSUPPORTED",
+                "ICP_ERR_TIMEOUT"))
+
+
+def test_noalloc_batch_limits_in_the_header_hold(binding):
+    # the header lists the largest batch the fixed scratch takes per query length
+    text = open(HEADER).read()
+    m = re.search(r"allows at most\s+([\d, ]+?)\s*or\s*(\d+)\s+requests", text.replace("*", " "))
+    stated = [int(x) for x in m.group(1).replace(",", " ").split()] + [int(m.group(2))]
+    assert len(stated) == 8
+    lim = binding.NOALLOC_SCRATCH_BYTES
+    for dql, B in enumerate(stated, start=1):
+        assert 0 < binding.icp_score_select_workspace_bytes(B, dql) <= lim
+        assert binding.icp_score_select_workspace_bytes(B + 1, dql) > lim
