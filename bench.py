@@ -297,6 +297,8 @@ class DecodeBench:
             algorithmic_bytes(spec, self.seq_list, self.cols)
         self.launches_per_step = 3 * ws
         self.kernel_launches_per_step = ws
+        # the scorers start early under programmatic dependent launch
+        self.score_pdl = True
 
     @property
     def fused_bytes(self):
@@ -324,8 +326,8 @@ class DecodeBench:
             icp.icp_score(self.q, self.shards[rank], self.bt, self.sl, self.planes[rank],
                           rank=rank, world_size=ws, page_size=spec.page_size,
                           decode_query_len=spec.decode_query_len,
-                          max_decode_query_len=spec.max_decode_query_len, enable_pdl=True,
-                          errors=self.errors)
+                          max_decode_query_len=spec.max_decode_query_len,
+                          enable_pdl=self.score_pdl, errors=self.errors)
             if ev is not None and rank == ws - 1:
                 ev[1].record()
         for rank in range(ws):
@@ -352,8 +354,8 @@ class DecodeBench:
             icp.icp_score(self.q, self.shards[rank], self.bt, self.sl, self.planes[rank],
                           rank=rank, world_size=ws, page_size=spec.page_size,
                           decode_query_len=spec.decode_query_len,
-                          max_decode_query_len=spec.max_decode_query_len, enable_pdl=True,
-                          errors=self.errors)
+                          max_decode_query_len=spec.max_decode_query_len,
+                          enable_pdl=self.score_pdl, errors=self.errors)
 
     def fused_step(self):
         """The fused scorer + Top16 select (no score plane), one launch per shard."""
@@ -475,7 +477,7 @@ class SelectBench:
 class PrefillBench:
     """One prefill window: plan, scorer over the plan's records, Top16 into
     carrier rows, and the merge of the (single-rank) carrier."""
-    graph_period = 1
+    graph_period = 3   # windows per graph replay (the same window each time)
 
     def __init__(self, spec, seed, device):
         from sparse_attention_block_gb300 import icp
@@ -549,11 +551,57 @@ def prefill_bytes(seq_lens, n, cols):
 
 
 # ------------------------------------------------------------ CPU baselines
+def _np(x):
+    """A host numpy array of a tensor (or an array already on the host)."""
+    import numpy as np
+    return x.cpu().numpy() if hasattr(x, "cpu") else np.asarray(x)
+
+
+class OracleBatch:
+    """One workload's batch for the oracle arm, as host arrays.
+
+    It is drawn by the same seeded recipe as the CUDA arm's batch, on the GPU
+    when there is one (so that both arms time the same batch), and the plane
+    width comes from the oracle's own column count.  Nothing on this path
+    loads the CUDA library."""
+
+    def __init__(self, name, seed, device, batch=0):
+        import dataclasses
+
+        import oracle
+        from sparse_attention_block_gb300 import workloads as W
+        if name == "select":
+            plane, nvp = W.make_select_plane(seed=seed, device=device)
+            self.plane, self.nvp = _np(plane), _np(nvp)
+            self.T, self.K = self.plane.shape[0], self.plane.shape[2]
+            self.init, self.local = W.SELECT_INIT, W.SELECT_LOCAL
+            self.rows = self.T * 4
+            return
+        spec = W.PREFILL if name == "prefill" else W.DECODE_SPECS[name]
+        if batch and name != "prefill":
+            spec = dataclasses.replace(spec, batch=batch, seq_lens=spec.seq_lens[:batch],
+                                       description=spec.description +
+                                       f" (first {batch} requests)")
+        inp = W.make_decode_inputs(spec, seed=seed, device=device, make_shards=True)
+        self.spec = spec
+        self.q, self.bt, self.sl, self.nvp = (_np(inp.index_q), _np(inp.block_table),
+                                              _np(inp.seq_lens), _np(inp.num_valid_pages))
+        self.shards = ([_np(s) for s in inp.shards] if spec.world_size > 1
+                       else [_np(inp.index_k)])
+        self.k = self.shards[0]
+        del inp
+        self.seq_list = [int(x) for x in self.sl]
+        self.T = len(self.seq_list) * spec.decode_query_len
+        self.cols = oracle.columns_written(max(self.seq_list), spec.page_size, spec.world_size)
+        self.kbytes = sum(L * 128 for L in self.seq_list)
+        self.rows = self.T * 4
+
+
 def _oracle_arrays(bench):
     """The batch as numpy arrays, and the chain's parameters."""
     spec = bench.spec
-    arrays = (bench.q.cpu().numpy(), [s.cpu().numpy() for s in bench.shards],
-              bench.bt.cpu().numpy(), bench.sl.cpu().numpy(), bench.nvp.cpu().numpy())
+    arrays = (_np(bench.q), [_np(s) for s in bench.shards], _np(bench.bt), _np(bench.sl),
+              _np(bench.nvp))
     params = dict(cols=bench.cols, world_size=spec.world_size, page_size=spec.page_size,
                   decode_query_len=spec.decode_query_len, init_blocks=spec.init_blocks,
                   local_blocks=spec.local_blocks)
@@ -613,10 +661,9 @@ class OracleParallel:
 
 
 def oracle_select_sample(bench, budget_s):
-    import numpy as np
     import oracle
-    plane = bench.plane.cpu().numpy()
-    nvp = bench.nvp.cpu().numpy()
+    plane = _np(bench.plane)
+    nvp = _np(bench.nvp)
     spent, rows, t = 0.0, 0, 0
     while t < bench.T and (spent < budget_s or rows == 0):
         t0 = time.perf_counter()
@@ -636,11 +683,11 @@ def oracle_prefill_sample(bench, budget_s):
     import oracle
     spec = bench.spec
     n = spec.decode_query_len
-    L = int(bench.sl[0].item())
-    q = bench.q[:n].cpu().numpy()
-    k = bench.k.cpu().numpy()
-    bt = bench.bt[:1].cpu().numpy()
-    nvp = bench.nvp[:n].cpu().numpy()
+    L = int(bench.sl[0])
+    q = _np(bench.q[:n])
+    k = _np(bench.k)
+    bt = _np(bench.bt[:1])
+    nvp = _np(bench.nvp[:n])
     spent, nbytes, rows, m = 0.0, 0, 0, 0
     step = 16
     while m < n and (spent < budget_s or rows == 0):
@@ -691,6 +738,15 @@ def workload_config(name, bench):
 
 
 # ---------------------------------------------------------------- main arms
+ORACLE_STEPS = {
+    "decode": "the oracle's chain per request (plain C, fp64): exact score plane of every "
+              "shard -> Top16 select + publish into receive rows -> owner merge",
+    "select": "the oracle's brute-force Top16 select per row (plain C)",
+    "prefill": "the oracle's prefill chain (plain C, fp64): exact window plane -> carrier rows "
+               "-> carrier merge",
+}
+
+
 def run_reference(args, spec_name):
     """The oracle (plain C) timed per step on a bounded sample: decode chains
     over the requests on every host core, select and prefill on one thread."""
@@ -698,7 +754,7 @@ def run_reference(args, spec_name):
     if rank != 0:
         return 0
     device = torch.device("cuda", local) if torch.cuda.is_available() else torch.device("cpu")
-    bench = make_bench(spec_name, 0, device, args.batch)
+    bench = OracleBatch(spec_name, 0, device, args.batch)
     # each step a bounded sample: about two minutes of oracle work in all
     # (ICP_REF_STEP_SECONDS overrides the per-step budget)
     per_step = float(os.environ.get(
@@ -729,7 +785,8 @@ def run_reference(args, spec_name):
         "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": round(tot_s / args.steps * 1e3, 3), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": workload_config(spec_name, bench),
+        "config": dict(workload_config(spec_name, bench), step=ORACLE_STEPS[
+            spec_name if spec_name in ORACLE_STEPS else "decode"]),
         "rows_per_s": round(tot_r / tot_s, 2),
         "cpu_baseline": {"value": round(value, 4), "unit": UNIT, "cores": cores, "kind": "oracle",
                          "sample": f"first {reqs} request(s) / row(s) of the workload per step, "
@@ -766,6 +823,170 @@ def make_bench(name, seed, device, batch=0):
     return DecodeBench(spec, seed, device)
 
 
+def capture(bench):
+    """CUDA graphs of the step and of the dominant kernel alone.  The library
+    only enqueues, so its calls capture.  One graph holds a whole period of
+    steps (the receive slots 0, 1, 2, or the rotated inputs) back to back,
+    so that every launch inside it follows its predecessor as in a serving
+    loop: launched with programmatic dependent launch, a scorer starts its
+    set-up while the previous step's merge runs.  Shorter graphs cover the
+    remainder of a step count that is not a multiple of the period."""
+    period = bench.graph_period
+
+    def graph_of(fn, n):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            for _ in range(n):
+                fn()
+        return g
+
+    steps = [graph_of(bench.step, period)] + [graph_of(bench.step, r) for r in range(1, period)]
+    kernels = [graph_of(bench.kernel_only, period)] + [graph_of(bench.kernel_only, r)
+                                                        for r in range(1, period)]
+    return steps, kernels
+
+
+def replay(graphs, n):
+    """Replays n steps' worth: whole periods, then the remainder graph."""
+    period = len(graphs)
+    for _ in range(n // period):
+        graphs[0].replay()
+    if n % period:
+        graphs[n % period].replay()
+
+
+def timed_graphs(bench, steps, warmup, local, dist=None):
+    """Step and dominant-kernel times (ms) of graph replays, CUDA events on
+    the launching stream, clocks sampled through the timed region.  A timing
+    whose clock record shows a slowdown (or a leftover clock lock) is taken
+    once more, every rank following the same decision."""
+    for _ in range(max(warmup, 3)):
+        bench.step()
+    torch.cuda.synchronize()
+    graphs, kgraphs = capture(bench)
+    stream = torch.cuda.current_stream()
+    device = torch.device("cuda", local)
+    replay(graphs, max(warmup, 3))
+    replay(kgraphs, max(warmup, 3))
+    torch.cuda.synchronize()
+
+    def region():
+        start, end, ka, kb = (torch.cuda.Event(enable_timing=True) for _ in range(4))
+        sampler = ClockSampler(local)
+        barrier(dist)
+        torch.cuda.synchronize()
+        sampler.start()
+        start.record(stream)
+        replay(graphs, steps)
+        end.record(stream)
+        # the dominant kernel's launch duration, same stream, same inputs
+        ka.record(stream)
+        replay(kgraphs, steps)
+        kb.record(stream)
+        torch.cuda.synchronize()
+        sampler.stop()
+        barrier(dist)
+        return start.elapsed_time(end) / steps, ka.elapsed_time(kb) / steps, sampler.summary()
+
+    step_ms, kernel_ms, clocks = region()
+    if max_over_ranks(dist, float(ClockSampler.rejected(clocks)), device) > 0:
+        first = clocks["reasons"]
+        step_ms, kernel_ms, clocks = region()
+        clocks = dict(clocks, remeasured=True, first_run_reasons=first)
+    return step_ms, kernel_ms, clocks
+
+
+def timed_fused(bench, steps, warmup):
+    """ms per step of the fused scorer + select, replayed like the step."""
+    for _ in range(max(warmup, 3)):
+        bench.fused_step()
+    torch.cuda.synchronize()
+    period = bench.graph_period
+    graphs = []
+    for n in [period] + list(range(1, period)):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            for _ in range(n):
+                bench.fused_step()
+        graphs.append(g)
+    replay(graphs, 3)
+    torch.cuda.synchronize()
+    stream = torch.cuda.current_stream()
+    fa, fb = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    fa.record(stream)
+    replay(graphs, steps)
+    fb.record(stream)
+    torch.cuda.synchronize()
+    return fa.elapsed_time(fb) / steps
+
+
+def timed_step_without_scorer_pdl(bench, steps, warmup, local):
+    """The decode step with the scorers launched as ordinary kernels (no
+    early start), timed like the step itself: ms per step."""
+    bench.score_pdl = False
+    try:
+        step_ms, _, _ = timed_graphs(bench, steps, warmup, local)
+    finally:
+        bench.score_pdl = True
+    return step_ms
+
+
+def roofline_of(name, bench, kernel_ms, peak, peak_kind, digest, traffic=None):
+    kernel_name = "icp_top16_select" if name == "select" else (
+        "icp_prefill_score" if name == "prefill" else "icp_score")
+    kernel_bytes = bench.score_bytes
+    achieved = kernel_bytes / (kernel_ms / 1e3) / 1e9
+    if name == "prefill":
+        # many query rows against the same keys: a dense fp8 contraction
+        tpeak, tkind = measured_tensor_peak_fp8()
+        t_achieved = bench.flops / (kernel_ms / 1e3) / 1e12
+        return {"bound": "tensor", "kernel": kernel_name, "achieved": round(t_achieved, 1),
+                "peak": tpeak, "unit": "TFLOP/s", "frac": round(t_achieved / tpeak, 4),
+                "peak_source": tkind, "traffic": None,
+                "algorithmic_flops_per_launch": bench.flops,
+                "hbm_achieved_gbs": round(achieved, 1), "kernel_digest": digest}
+    per = bench.kernel_launches_per_step
+    return {"bound": "hbm", "kernel": kernel_name, "achieved": round(achieved, 1),
+            "peak": peak, "unit": "GB/s", "frac": round(achieved / peak, 4),
+            "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)"
+            if peak_kind == "measured" else "fallback 6.8 TB/s",
+            "traffic": traffic, "algorithmic_bytes_per_launch": kernel_bytes // per,
+            "launches_timed_together": per, "algorithmic_bytes_timed": kernel_bytes,
+            "kernel_digest": digest}
+
+
+# The other workloads, each reported as a short record in the default line.
+RECORD_WORKLOADS = ("longctx", "batched", "sharded", "select", "prefill")
+
+
+def workload_record(name, steps, warmup, local, peak, peak_kind, digest):
+    """Device-timed record of one more workload: its dominant kernel, its
+    step, the roofline of the kernel, the fused step where there is one, the
+    decode step without the scorer's early start, and the clocks."""
+    bench = make_bench(name, 0, torch.device("cuda", local))
+    try:
+        step_ms, kernel_ms, clocks = timed_graphs(bench, steps, warmup, local)
+        rec = {"config": workload_config(name, bench),
+               "kernel_ms": round(kernel_ms, 5), "step_ms": round(step_ms, 5),
+               "step_GB/s": round(bench.step_bytes / (step_ms / 1e3) / 1e9, 1),
+               "rows_per_s": round(bench.rows / (step_ms / 1e3), 1),
+               "roofline": roofline_of(name, bench, kernel_ms, peak, peak_kind, digest),
+               "clocks": clocks}
+        if isinstance(bench, DecodeBench):
+            f_ms = timed_fused(bench, steps, warmup)
+            rec["fused_step_ms"] = round(f_ms, 5)
+            rec["fused_GB/s"] = round(bench.fused_bytes / (f_ms / 1e3) / 1e9, 1)
+            rec["step_ms_scorer_without_pdl"] = round(
+                timed_step_without_scorer_pdl(bench, steps, warmup, local), 5)
+        errors = int(bench.errors.item()) if hasattr(bench, "errors") else 0
+        if errors:
+            raise SystemExit(f"{name}: {errors} device errors during the benchmark")
+        return rec
+    finally:
+        del bench
+        torch.cuda.empty_cache()
+
+
 def run_ours(args, spec_name):
     ws, rank, local = dist_env()
     if not torch.cuda.is_available():
@@ -775,91 +996,23 @@ def run_ours(args, spec_name):
     dist = init_dist(ws, "nccl")
     bench = make_bench(spec_name, rank, device, args.batch)
 
-    for _ in range(max(args.warmup, 3)):
-        bench.step()
-    torch.cuda.synchronize()
-    # The timed work replays CUDA graphs of the step (the library enqueues
-    # only, so it captures), one graph per receive slot / rotated input.
-    period = bench.graph_period
-    graphs = []
-    for _ in range(period):
-        g = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(g):
-            bench.step()
-        graphs.append(g)
-    kgraph = torch.cuda.CUDAGraph()       # the dominant kernel alone
-    with torch.cuda.graph(kgraph):
-        bench.kernel_only()
-    stream = torch.cuda.current_stream()
-    for i in range(max(args.warmup, 3)):
-        graphs[i % period].replay()
-        kgraph.replay()
-    torch.cuda.synchronize()
-
-    def timed_region():
-        start = torch.cuda.Event(enable_timing=True)
-        end = torch.cuda.Event(enable_timing=True)
-        ka = torch.cuda.Event(enable_timing=True)
-        kb = torch.cuda.Event(enable_timing=True)
-        sampler = ClockSampler(local)
-        barrier(dist)
-        torch.cuda.synchronize()
-        sampler.start()
-        start.record(stream)
-        for i in range(args.steps):
-            graphs[i % period].replay()
-        end.record(stream)
-        # the dominant kernel's launch duration, same stream, same inputs
-        ka.record(stream)
-        for i in range(args.steps):
-            kgraph.replay()
-        kb.record(stream)
-        torch.cuda.synchronize()
-        sampler.stop()
-        barrier(dist)
-        return start.elapsed_time(end), ka.elapsed_time(kb) / args.steps, sampler.summary()
-
-    elapsed_ms, kernel_ms, clocks = timed_region()
-    # a timing taken under a slowdown (or a leftover clock lock) is taken
-    # again once; every rank follows the same decision
-    if max_over_ranks(dist, float(ClockSampler.rejected(clocks)), device) > 0:
-        first = clocks["reasons"]
-        elapsed_ms, kernel_ms, clocks = timed_region()
-        clocks = dict(clocks, remeasured=True, first_run_reasons=first)
-    elapsed_ms = max_over_ranks(dist, elapsed_ms, device)
+    ms_per_step, kernel_ms, clocks = timed_graphs(bench, args.steps, args.warmup, local, dist)
+    ms_per_step = max_over_ranks(dist, ms_per_step, device)
     errors = int(bench.errors.item()) if hasattr(bench, "errors") else 0
     if errors:
-        raise SystemExit(f"{errors} bounded waits timed out during the benchmark")
+        raise SystemExit(f"{errors} device errors during the benchmark")
 
-    ms_per_step = elapsed_ms / args.steps
     n = ws
     value = n * bench.step_bytes / (ms_per_step / 1e3) / 1e9
     rows_per_s = n * bench.rows / (ms_per_step / 1e3)
     peak, peak_kind = measured_peaks()
-    kernel_name = "icp_top16_select" if spec_name == "select" else "icp_score"
-    kernel_bytes = bench.score_bytes
-    achieved = kernel_bytes / (kernel_ms / 1e3) / 1e9
     digest = kernel_digest()
     traffic = None
     tr = NCU_TRAFFIC.get((spec_name, digest))
     if tr is not None:
         traffic = int(tr * bench.kbytes) if bench.kbytes else int(tr)
-
-    roofline = {"bound": "hbm", "kernel": kernel_name, "achieved": round(achieved, 1),
-                "peak": peak, "unit": "GB/s", "frac": round(achieved / peak, 4),
-                "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)"
-                if peak_kind == "measured" else "fallback 6.8 TB/s",
-                "traffic": traffic, "algorithmic_bytes_per_launch": kernel_bytes,
-                "kernel_digest": digest}
-    if spec_name == "prefill":
-        # many query rows against the same keys: a dense fp8 contraction
-        tpeak, tkind = measured_tensor_peak_fp8()
-        t_achieved = bench.flops / (kernel_ms / 1e3) / 1e12
-        roofline = {"bound": "tensor", "kernel": kernel_name, "achieved": round(t_achieved, 1),
-                    "peak": tpeak, "unit": "TFLOP/s", "frac": round(t_achieved / tpeak, 4),
-                    "peak_source": tkind, "traffic": None,
-                    "algorithmic_flops_per_launch": bench.flops,
-                    "hbm_achieved_gbs": round(achieved, 1), "kernel_digest": digest}
+    roofline = roofline_of(spec_name, bench, kernel_ms, peak, peak_kind, digest, traffic)
+    kernel_name = roofline["kernel"]
     line = {
         "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": n,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 5),
@@ -873,23 +1026,8 @@ def run_ours(args, spec_name):
         "gpu_launches": bench.launches_per_step * args.steps,
         "kernel_timing_launches": bench.kernel_launches_per_step * args.steps,
     }
-    if spec_name not in ("select", "prefill"):
-        for _ in range(max(args.warmup, 3)):
-            bench.fused_step()
-        torch.cuda.synchronize()
-        fgraph = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(fgraph):
-            bench.fused_step()
-        for _ in range(3):
-            fgraph.replay()
-        torch.cuda.synchronize()
-        fa, fb = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        fa.record(stream)
-        for _ in range(args.steps):
-            fgraph.replay()
-        fb.record(stream)
-        torch.cuda.synchronize()
-        f_ms = fa.elapsed_time(fb) / args.steps
+    if isinstance(bench, DecodeBench):
+        f_ms = timed_fused(bench, args.steps, args.warmup)
         f_bytes = bench.fused_bytes
         line["fused_score_select"] = {
             "ms_per_step": round(f_ms, 5),
@@ -899,6 +1037,8 @@ def run_ours(args, spec_name):
             "launches_per_step": bench.ws,
             "note": "icp_score_select: scorer bytes without the plane write, plus Top16 "
                     "output; no score plane"}
+        line["step_ms_scorer_without_pdl"] = round(
+            timed_step_without_scorer_pdl(bench, args.steps, args.warmup, local), 5)
         e2e_s, bi, bo = bench.e2e(args.steps, max(args.warmup, 3))
         e2e_s = max_over_ranks(dist, e2e_s, device)
         line["e2e"] = {"value": round(n * bench.step_bytes / e2e_s / 1e9, 2), "unit": UNIT,
@@ -936,6 +1076,13 @@ def run_ours(args, spec_name):
                           f"process per core over the requests",
                 "rows_per_s": round(pr / pw, 2), "seconds": round(pw, 2),
                 "single_thread": single}
+    if ws == 1 and spec_name == "multitoken" and not args.batch and not args.no_workloads:
+        # every other workload as a short device-timed record (no CPU baseline)
+        del bench
+        torch.cuda.empty_cache()
+        line["workloads"] = {
+            w: workload_record(w, args.steps, args.warmup, local, peak, peak_kind, digest)
+            for w in RECORD_WORKLOADS}
     if rank == 0:
         print(json.dumps(line), flush=True)
     if dist is not None:
@@ -953,6 +1100,8 @@ def main(argv=None):
                     choices=["tiny", "batched", "multitoken", "sharded", "longctx", "select",
                              "prefill"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-workloads", action="store_true",
+                    help="leave out the records of the other workloads")
     ap.add_argument("--batch", type=int, default=0,
                     help="use only the first B requests (smaller profiling cases)")
     args = ap.parse_args(argv)

@@ -10,6 +10,7 @@
 - The ncu traffic table is keyed by a source digest and holds ratios of DRAM
   bytes to index-K bytes that cannot fall below 1 (every row is read once).
 """
+import json
 from types import SimpleNamespace
 
 import bench
@@ -102,3 +103,24 @@ def test_code_digest_ignores_comments_but_not_code():
     changed = dict(base)
     changed["icp_score.cu"] = "int a; // x\n/* y */ int c;\n"
     assert bench.kernel_digest(lambda f: changed[f]) != d
+
+
+def test_reference_arm_runs_the_oracle_without_the_cuda_library(tmp_path):
+    # the oracle arm draws and sizes its batch itself: the product's binding
+    # (and with it libicp.so) must stay unloaded
+    import os
+    import subprocess
+    import sys
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    code = ("import json, sys, bench\n"
+            "bench.main(['--impl', 'reference', '--workload', 'tiny', '--steps', '1',"
+            " '--warmup', '0'])\n"
+            "assert 'sparse_attention_block_gb300.icp' not in sys.modules\n"
+            "assert 'libicp' not in open('/proc/self/maps').read()\n")
+    env = dict(os.environ, ICP_REF_STEP_SECONDS="0.05", CUDA_VISIBLE_DEVICES="")
+    r = subprocess.run([sys.executable, "-c", code], cwd=root, env=env, capture_output=True,
+                       text=True, timeout=300)
+    assert r.returncode == 0, r.stderr[-2000:]
+    line = json.loads([ln for ln in r.stdout.splitlines() if ln.startswith("{")][-1])
+    assert line["impl"] == "reference" and line["cpu_baseline"]["kind"] == "oracle"
+    assert line["config"]["cols"] == 20 and "oracle" in line["config"]["step"]
