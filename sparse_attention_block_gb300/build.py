@@ -5,7 +5,13 @@ into ``sparse_attention_block_gb300/_lib/libicp.so`` with the CUDA runtime
 linked statically (the library needs no libcuda at load time; it reaches the
 driver through the runtime's entry-point query).
 
-    python -m sparse_attention_block_gb300.build [--force]
+``timeline=True`` builds ``_lib/libicp_timeline.so`` instead: the same
+library compiled with ICP_TIMELINE, whose scorer records globaltimer stamps
+of its phases per CTA and which also exports icp_timeline_read
+(include/icp_timeline.h).  It is a measurement build, loaded only by
+``sparse_attention_block_gb300.timeline``.
+
+    python -m sparse_attention_block_gb300.build [--force] [--timeline]
 """
 from __future__ import annotations
 
@@ -21,6 +27,7 @@ CSRC = os.path.join(HERE, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 OUT_DIR = os.path.join(HERE, "_lib")
 LIB_PATH = os.path.join(OUT_DIR, "libicp.so")
+TIMELINE_LIB_PATH = os.path.join(OUT_DIR, "libicp_timeline.so")
 OBJ_DIR = os.path.join(ROOT, "_build", "icp")
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
@@ -47,23 +54,26 @@ def _inputs():
     return deps
 
 
-def up_to_date() -> bool:
-    if not os.path.exists(LIB_PATH):
+def up_to_date(lib_path: str = LIB_PATH) -> bool:
+    if not os.path.exists(lib_path):
         return False
-    t = os.path.getmtime(LIB_PATH)
+    t = os.path.getmtime(lib_path)
     return all(os.path.getmtime(d) <= t for d in _inputs())
 
 
-def build(force: bool = False, verbose: bool = False) -> str:
-    if not force and up_to_date():
-        return LIB_PATH
+def build(force: bool = False, verbose: bool = False, timeline: bool = False) -> str:
+    lib_path = TIMELINE_LIB_PATH if timeline else LIB_PATH
+    obj_dir = OBJ_DIR + ("_timeline" if timeline else "")
+    extra = ["-DICP_TIMELINE"] if timeline else []
+    if not force and up_to_date(lib_path):
+        return lib_path
     nvcc = _nvcc()
-    os.makedirs(OBJ_DIR, exist_ok=True)
+    os.makedirs(obj_dir, exist_ok=True)
     os.makedirs(OUT_DIR, exist_ok=True)
 
     def compile_one(src):
-        obj = os.path.join(OBJ_DIR, os.path.basename(src)[:-3] + ".o")
-        cmd = [nvcc, *ARCH, *NVCC_FLAGS, "-c", src, "-o", obj]
+        obj = os.path.join(obj_dir, os.path.basename(src)[:-3] + ".o")
+        cmd = [nvcc, *ARCH, *NVCC_FLAGS, *extra, "-c", src, "-o", obj]
         r = subprocess.run(cmd, capture_output=True, text=True)
         if r.returncode != 0:
             raise RuntimeError(f"nvcc failed on {src}:\n{r.stdout}\n{r.stderr}")
@@ -74,18 +84,18 @@ def build(force: bool = False, verbose: bool = False) -> str:
     with cf.ThreadPoolExecutor(max_workers=min(8, os.cpu_count() or 1)) as ex:
         objs = list(ex.map(compile_one, sources()))
     # export the C ABI only; the static CUDA runtime stays private to the library
-    vmap = os.path.join(OBJ_DIR, "icp.map")
+    vmap = os.path.join(obj_dir, "icp.map")
     with open(vmap, "w") as f:
         f.write("{ global: icp_*; local: *; };\n")
-    tmp = LIB_PATH + f".tmp{os.getpid()}"
+    tmp = lib_path + f".tmp{os.getpid()}"
     cmd = [nvcc, *ARCH, "-shared", "-cudart", "static", "-Xlinker", "--version-script=" + vmap,
            "-o", tmp, *objs]
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError(f"link failed:\n{r.stdout}\n{r.stderr}")
-    os.replace(tmp, LIB_PATH)
-    return LIB_PATH
+    os.replace(tmp, lib_path)
+    return lib_path
 
 
 if __name__ == "__main__":
-    print(build(force="--force" in sys.argv, verbose=True))
+    print(build(force="--force" in sys.argv, verbose=True, timeline="--timeline" in sys.argv))

@@ -42,6 +42,18 @@
 #include "icp_internal.h"
 
 namespace icp {
+
+#ifdef ICP_TIMELINE
+// Timeline build only: globaltimer stamps of each CTA's phases (slot
+// meanings in include/icp_timeline.h), read back by icp_timeline_read.
+constexpr int kTimelineCtas = 1024;
+constexpr int kTimelineSlots = 24;
+__device__ unsigned long long g_timeline[kTimelineCtas * kTimelineSlots];
+#define ICP_STAMP(slot) (g_timeline[blockIdx.x * kTimelineSlots + (slot)] = globaltimer_ns())
+#else
+#define ICP_STAMP(slot) ((void)0)
+#endif
+
 namespace {
 
 constexpr int kStages = 8;
@@ -367,6 +379,7 @@ score_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CU
   const int nbatch = req_count(a);      // <= a.batch
 
   if (threadIdx.x == 0) {
+    ICP_STAMP(0);
     for (int s = 0; s < kStages; ++s) {
       mbar_init(bar_full(s), 1);
       mbar_init(bar_empty(s), 1);
@@ -400,6 +413,9 @@ score_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CU
       const int tiles = (u + g.cpt - 1) / g.cpt;
       sum += tiles + (WIDE && tiles > 0 ? kWideRequestUnits : 0);
     }
+#ifdef ICP_TIMELINE
+    if (threadIdx.x == 0 && sum >= 0) ICP_STAMP(15);
+#endif
     // exclusive scan of the per-thread sums: shuffles inside each warp, then
     // the warp totals (NT / 32 of them) in shared memory
     int incl = sum;
@@ -424,6 +440,7 @@ score_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CU
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = (uint32_t)misc[0];
+  if (threadIdx.x == 0) ICP_STAMP(1);
 
   const long long total = prefix[nbatch];
   const int g0 = (int)(total * blockIdx.x / gridDim.x);
@@ -442,6 +459,9 @@ score_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CU
     SegmentWalker walk(prefix, nbatch, g0, g1, WIDE ? kWideRequestUnits : 0);
     int b, t0, t1;
     bool ok = true;
+#ifdef ICP_TIMELINE
+    if (lane == 0 && walk.b >= 0) ICP_STAMP(18);
+#endif
     if (a.pdl) {
       // Early start: while the preceding kernel finishes, pull the first
       // tiles of this CTA into L2, only from pages lying wholly below
@@ -470,14 +490,21 @@ score_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CU
       }
       __syncwarp();
       pdl_wait();
+      if (lane == 0) ICP_STAMP(12);
     }
     while (ok && walk.next(b, t0, t1)) {
       const ReqView rv = req_view(a, b);
       const int nunits = units_of(rv.seq_len, a.page_size, g.split);
       const uint32_t qph = qslot ? qph1 : qph0;
+#ifdef ICP_TIMELINE
+      if (lane == 0 && issued == 0 && nunits >= 0) ICP_STAMP(16);
+#endif
       if (lane == 0) ok = mbar_wait(bar_qempty(qslot), qph ^ 1u, abort_flag);
       ok = __shfl_sync(0xFFFFFFFFu, ok, 0) != 0;
       if (!ok) break;
+#ifdef ICP_TIMELINE
+      if (lane == 0 && issued == 0) ICP_STAMP(17);
+#endif
       if (lane == 0) {
         mbar_arrive_expect_tx(bar_qfull(qslot), L::q_bytes);
         if constexpr (WIDE) {
@@ -491,6 +518,9 @@ score_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CU
       last_qslot = qslot;
       if (qslot) qph1 ^= 1u; else qph0 ^= 1u;
       qslot ^= 1;
+#ifdef ICP_TIMELINE
+      if (lane == 0 && issued == 0) ICP_STAMP(13);
+#endif
       const int cbeg = t0 * g.cpt;
       const int cend = min(t1 * g.cpt, nunits);
       const int32_t *btrow = a.block_table + (long long)rv.bt_row * a.bt_stride;
@@ -511,6 +541,9 @@ score_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CU
       int pg_cur = (cbeg + lane < cend) ? btrow[page_slot_of(cbeg + lane, g.split)] : 0;
       int pg_nxt = (cbeg + 32 + lane < cend) ? btrow[page_slot_of(cbeg + 32 + lane, g.split)] : 0;
       pg_cur = vet(pg_cur, cbeg + lane);
+#ifdef ICP_TIMELINE
+      if (lane == 0 && issued == 0 && pg_cur >= 0) ICP_STAMP(14);
+#endif
       for (int tl = t0; tl < t1; ++tl) {
         const int c0 = tl * g.cpt;
         if (c0 >= grp + 32) {
@@ -547,6 +580,10 @@ score_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CU
             const int y = pg * g.rows_per_page + row_off_of(c, g.split);
             tma_load_2d_hint(dst + k * g.R * 128, &tmk, 0, y, bar, pol);
           }
+#ifdef ICP_TIMELINE
+          if (issued == 0) ICP_STAMP(2);
+          ICP_STAMP(3);
+#endif
         }
         __syncwarp();
         if (!WIDE || j == 1 || tl + 1 == t1) {
@@ -574,6 +611,9 @@ score_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CU
     // reconvergence of the warp.
     if (lane == 0) {
       const uint32_t idesc = idesc_f8_f32(128, (int)kAccCols);
+#ifdef ICP_TIMELINE
+      long long mma_tiles = 0;
+#endif
       int stage = 0, acc = 0;
       uint32_t sphase = 0, aphase = 0;
       uint32_t qph0 = 0, qph1 = 0;
@@ -634,6 +674,10 @@ score_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CU
                      k > 0 ? 1u : 0u);
             mma_commit(bar_empty(stage));
             mma_commit(bar_tfull(acc));
+#ifdef ICP_TIMELINE
+            if (mma_tiles++ == 0) ICP_STAMP(4);
+            ICP_STAMP(5);
+#endif
             if (++stage == kStages) {
               stage = 0;
               sphase ^= 1u;
@@ -780,6 +824,12 @@ score_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CU
             epilogue_tile<32, FUSED>(a, taddr, lane, 0, rv.tok0, rv.ntok, tl, nunits, seq_len,
                                      bar_tempty(e), lt, lk, lfid, lfsc);
           aphase ^= 1u;
+#ifdef ICP_TIMELINE
+          if (lane == 0) {
+            if (aphase == 1u && idx == seg_tiles && tl - t0 < 4) ICP_STAMP(6 + e);
+            ICP_STAMP(10);
+          }
+#endif
         }
       }
       if constexpr (FUSED) {
@@ -812,6 +862,7 @@ score_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CU
     tmem_dealloc(tmem_base, kTmemCols);
   }
   if (threadIdx.x == 0 && *abort_flag && a.errors) atomicAdd(a.errors, 1);
+  if (threadIdx.x == 0) ICP_STAMP(11);
 }
 
 template <bool FUSED, bool WIDE = false>
@@ -876,3 +927,18 @@ cudaError_t launch_score_select(const CUtensorMap &tmk, const CUtensorMap &tmq, 
 }
 
 }  // namespace icp
+
+#ifdef ICP_TIMELINE
+extern "C" int icp_timeline_read(unsigned long long *dst, int ctas, int clear) {
+  if (!dst || ctas < 0 || ctas > icp::kTimelineCtas) return 1;
+  const size_t n = (size_t)ctas * icp::kTimelineSlots * sizeof(unsigned long long);
+  if (cudaMemcpyFromSymbol(dst, icp::g_timeline, n) != cudaSuccess) return 2;
+  if (clear) {
+    void *p = nullptr;
+    if (cudaGetSymbolAddress(&p, icp::g_timeline) != cudaSuccess ||
+        cudaMemset(p, 0, sizeof(icp::g_timeline)) != cudaSuccess || cudaDeviceSynchronize())
+      return 2;
+  }
+  return 0;
+}
+#endif

@@ -15,7 +15,8 @@ import os
 import torch
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
-LIB_PATH = os.path.join(_HERE, "_lib", "libicp.so")
+# ICP_LIBRARY names another build of the same library (the timeline build)
+LIB_PATH = os.environ.get("ICP_LIBRARY") or os.path.join(_HERE, "_lib", "libicp.so")
 
 if not os.path.exists(LIB_PATH):
     raise ImportError(
