@@ -962,6 +962,33 @@ def roofline_of(name, bench, kernel_ms, peak, peak_kind, digest, traffic=None):
 RECORD_WORKLOADS = ("longctx", "batched", "sharded", "select", "prefill")
 
 
+def one_shot_read_ms(nbytes, steps, copies=6):
+    """A library reference for reading nbytes once: torch.sum over a float32
+    buffer of that size, six fresh buffers taken in turn (so no read hits
+    L2), replayed from one graph like the select: ms per sum."""
+    n = nbytes // 4
+    bufs = [torch.randn(n, device="cuda") for _ in range(copies)]
+    out = torch.empty((), device="cuda")
+    for b in bufs:
+        torch.sum(b, dim=0, out=out)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        for b in bufs:
+            torch.sum(b, dim=0, out=out)
+    g.replay()
+    torch.cuda.synchronize()
+    reps = max(1, steps // copies)
+    stream = torch.cuda.current_stream()
+    ea, eb = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    ea.record(stream)
+    for _ in range(reps):
+        g.replay()
+    eb.record(stream)
+    torch.cuda.synchronize()
+    return ea.elapsed_time(eb) / (reps * copies)
+
+
 def workload_record(name, steps, warmup, local, peak, peak_kind, digest):
     """Device-timed record of one more workload: its dominant kernel, its
     step, the roofline of the kernel, the fused step where there is one, the
@@ -981,6 +1008,14 @@ def workload_record(name, steps, warmup, local, peak, peak_kind, digest):
             rec["fused_GB/s"] = round(bench.fused_bytes / (f_ms / 1e3) / 1e9, 1)
             rec["step_ms_scorer_with_pdl"] = round(
                 timed_step_with_scorer_pdl(bench, steps, warmup, local), 5)
+        if name == "select":
+            # what reading the same valid bytes once costs a library kernel
+            r_ms = one_shot_read_ms(bench.score_bytes, steps)
+            rec["one_shot_read"] = {
+                "what": "torch.sum over a float32 buffer of the select's algorithmic bytes, "
+                        "6 rotated buffers, one graph", "ms": round(r_ms, 5),
+                "GB/s": round(bench.score_bytes / (r_ms / 1e3) / 1e9, 1),
+                "select_ms_over_read_ms": round(kernel_ms / r_ms, 3)}
         errors = int(bench.errors.item()) if hasattr(bench, "errors") else 0
         if errors:
             raise SystemExit(f"{name}: {errors} device errors during the benchmark")
@@ -1029,6 +1064,13 @@ def run_ours(args, spec_name):
         "gpu_launches": bench.launches_per_step * args.steps,
         "kernel_timing_launches": bench.kernel_launches_per_step * args.steps,
     }
+    if spec_name == "select":
+        r_ms = one_shot_read_ms(bench.score_bytes, args.steps)
+        line["one_shot_read"] = {
+            "what": "torch.sum over a float32 buffer of the select's algorithmic bytes, "
+                    "6 rotated buffers, one graph", "ms": round(r_ms, 5),
+            "GB/s": round(bench.score_bytes / (r_ms / 1e3) / 1e9, 1),
+            "select_ms_over_read_ms": round(kernel_ms / r_ms, 3)}
     if isinstance(bench, DecodeBench):
         f_ms = timed_fused(bench, args.steps, args.warmup)
         f_bytes = bench.fused_bytes
