@@ -23,6 +23,13 @@
  *   16  the producer read its first request's length
  *   17  the first request's query slot was free
  *   18  the producer found its first tile in the prefix sums
+ * Slots 19-23 hold per-CTA sums instead: the ns the producer waited for a
+ * free ring stage (19); for the prefill scorer, the ns its MMA thread waited
+ * for key tiles (20) and for an accumulator (21), and the ns its first
+ * epilogue warp waited for a finished item (22); the number of request
+ * segments (plan records) the CTA handled (23).  For the prefill scorer,
+ * slot 4 / 5 are its first / last tile pair's MMAs committed and 6 / 10 its
+ * first / last item finished by the first epilogue warp.
  * Slots a launch does not reach keep their previous contents.
  */
 #ifndef ICP_TIMELINE_H

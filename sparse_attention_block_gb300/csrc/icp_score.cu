@@ -50,8 +50,16 @@ constexpr int kTimelineCtas = 1024;
 constexpr int kTimelineSlots = 24;
 __device__ unsigned long long g_timeline[kTimelineCtas * kTimelineSlots];
 #define ICP_STAMP(slot) (g_timeline[blockIdx.x * kTimelineSlots + (slot)] = globaltimer_ns())
+// adds the ns spent in `wait` to a per-CTA sum (a slot that holds a total)
+#define ICP_TIMED(slot, wait)                                              \
+  do {                                                                     \
+    const unsigned long long icp_t0_ = globaltimer_ns();                   \
+    wait;                                                                  \
+    g_timeline[blockIdx.x * kTimelineSlots + (slot)] += globaltimer_ns() - icp_t0_; \
+  } while (0)
 #else
 #define ICP_STAMP(slot) ((void)0)
+#define ICP_TIMED(slot, wait) wait
 #endif
 
 namespace {
@@ -493,6 +501,9 @@ score_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CU
       if (lane == 0) ICP_STAMP(12);
     }
     while (ok && walk.next(b, t0, t1)) {
+#ifdef ICP_TIMELINE
+      if (lane == 0) g_timeline[blockIdx.x * kTimelineSlots + 23] += 1;  // segments
+#endif
       const ReqView rv = req_view(a, b);
       const int nunits = units_of(rv.seq_len, a.page_size, g.split);
       const uint32_t qph = qslot ? qph1 : qph0;
@@ -556,7 +567,7 @@ score_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CU
         // adjacent stages, one barrier per slot; j is the tile in its pair
         const int j = WIDE ? ((tl - t0) & 1) : 0;
         if (j == 0) {
-          if (lane == 0) ok = mbar_wait(bar_empty(stage), sphase ^ 1u, abort_flag);
+          if (lane == 0) ICP_TIMED(19, ok = mbar_wait(bar_empty(stage), sphase ^ 1u, abort_flag));
           ok = __shfl_sync(0xFFFFFFFFu, ok, 0) != 0;
           if (!ok) break;
         }
@@ -633,12 +644,12 @@ score_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CU
           const int nh = req_view(a, b).ntok > kPlanTokens / 2 ? 2 : 1;
           for (int tl = t0; ok && tl < t1; tl += 2) {
             const int np = min(2, t1 - tl);
-            ok = mbar_wait(bar_full(stage), sphase, abort_flag);
+            ICP_TIMED(20, ok = mbar_wait(bar_full(stage), sphase, abort_flag));
             if (!ok) break;
             const uint32_t kaddr = sb + kOffStages + stage * 2 * kTileBytes;
             const uint32_t id = np == 2 ? idesc_f8_f32(128, 2 * (int)kAccCols) : idesc;
             for (int h = 0; h < nh; ++h) {
-              ok = mbar_wait(bar_tempty(acc), aphase ^ 1u, abort_flag);
+              ICP_TIMED(21, ok = mbar_wait(bar_tempty(acc), aphase ^ 1u, abort_flag));
               if (!ok) break;
               tc_fence_after();
               const uint32_t d = tmem_base + (uint32_t)acc * (2 * kAccCols);
@@ -655,6 +666,10 @@ score_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CU
             }
             if (!ok) break;
             mma_commit(bar_empty(stage));
+#ifdef ICP_TIMELINE
+            if (mma_tiles++ == 0) ICP_STAMP(4);
+            ICP_STAMP(5);
+#endif
             if (++stage == kStages / 2) {
               stage = 0;
               sphase ^= 1u;
@@ -779,7 +794,10 @@ score_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CU
           for (int h = 0; ok && h < nh; ++h, ++pi) {
             const int acc = pi & 1;
             const uint32_t wph = (uint32_t)(pi >> 1) & 1u;
-            if (lane == 0) ok = mbar_wait(bar_tfull(acc), wph, abort_flag);
+            if (lane == 0) {
+              if (warp == 2) ICP_TIMED(22, ok = mbar_wait(bar_tfull(acc), wph, abort_flag));
+              else ok = mbar_wait(bar_tfull(acc), wph, abort_flag);
+            }
             ok = __shfl_sync(0xFFFFFFFFu, ok, 0) != 0;
             if (!ok) break;
             tc_fence_after();
@@ -802,6 +820,12 @@ score_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CU
               __syncwarp();
               if (lane == 0) mbar_arrive(bar_tempty(acc));
             }
+#ifdef ICP_TIMELINE
+            if (warp == 2 && lane == 0) {
+              if (pi == 0) ICP_STAMP(6);
+              ICP_STAMP(10);
+            }
+#endif
           }
         }
       } else {
