@@ -43,6 +43,24 @@ def test_only_the_c_abi_is_exported():
     assert syms and all(s.startswith("icp_") for s in syms), syms
 
 
+def test_timeline_build_exports_its_reader_and_the_library_does_not():
+    # the measurement build (ICP_TIMELINE) adds icp_timeline_read, declared in
+    # include/icp_timeline.h; the ordinary library has no such symbol
+    from sparse_attention_block_gb300 import build
+    ordinary = os.popen(f"nm -D --defined-only {build.build()}").read()
+    assert "icp_timeline_read" not in ordinary
+    path = build.build(timeline=True)
+    assert path != build.LIB_PATH
+    tl = ctypes.CDLL(path)
+    f = tl.icp_timeline_read
+    f.restype = ctypes.c_int
+    f.argtypes = [ctypes.c_void_p, ctypes.c_int, ctypes.c_int]
+    buf = (ctypes.c_ulonglong * 24)()
+    assert f(None, 1, 0) == 1 and f(buf, -1, 0) == 1 and f(buf, 1025, 0) == 1
+    for n in declared_functions():
+        assert hasattr(tl, n), n
+
+
 def test_score_columns_host_helper(lib):
     f = lib.icp_score_columns
     assert f(1000, 128, 1) == 8
