@@ -16,7 +16,10 @@
 //              all requests' pages (each page read once per call) into an
 //              8-stage shared-memory ring, and each request's 32 query rows
 //              (4 * dql used) once, stored four times so that every TMEM lane
-//              quarter receives all of them.
+//              quarter receives all of them.  When a tile is two or four page
+//              slices (world size 2 or 4), warp 6, a second producer, issues
+//              every other tile: one warp alone cannot issue that many boxes
+//              fast enough.
 //   warp 1     MMA issuer: per tile, 4 x tcgen05.mma kind::f8f6f4 with
 //              A = the replicated queries (M = 128), B = the 128 keys of the
 //              tile (N = 128), K = 32, into one of 4 fp32 TMEM accumulators.
@@ -77,9 +80,11 @@ constexpr int kThreads = 192;
 // prefill scorer: two sets of four epilogue warps take alternate tiles
 constexpr int kEpiSetsWide = 2;
 constexpr int kThreadsWide = 64 + 128 * kEpiSetsWide;
-template <bool WIDE>
+// NPROD 2: a second producer warp (warp 6) takes every other tile; used when
+// a tile is two or four page slices (one TMA box each)
+template <bool WIDE, int NPROD = 1>
 struct BlockThreads {
-  static constexpr int value = WIDE ? kThreadsWide : kThreads;
+  static constexpr int value = WIDE ? kThreadsWide : kThreads + 32 * (NPROD - 1);
 };
 constexpr uint32_t kAccCols = 128;     // N = 128 keys per accumulator
 constexpr uint32_t kTmemCols = kAcc * kAccCols;
@@ -357,8 +362,8 @@ __device__ __forceinline__ void epilogue_tile_wide(const ScoreArgs &a, uint32_t 
 // set s finishing tile s of every item for the half's rows; each warp takes
 // its lane quarter (8 of the half's 32 tokens) and the accumulator is free
 // again after all eight warps have arrived.
-template <bool FUSED, bool WIDE>
-__global__ void __launch_bounds__(BlockThreads<WIDE>::value, 1)
+template <bool FUSED, bool WIDE, int NPROD = 1>
+__global__ void __launch_bounds__(BlockThreads<WIDE, NPROD>::value, 1)
 score_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmq,
              const ScoreArgs a) {
   extern __shared__ uint8_t smem_raw[];
@@ -366,7 +371,9 @@ score_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CU
   const uint32_t sb = (raw + 1023u) & ~1023u;
   uint8_t *gb = smem_raw + (sb - raw);
 
-  constexpr int NT = BlockThreads<WIDE>::value;
+  constexpr int NT = BlockThreads<WIDE, NPROD>::value;
+  constexpr int kEpiThreads = WIDE ? 128 * kEpiSetsWide : 128;
+  static_assert(NPROD == 1 || (!WIDE && !FUSED), "a second producer only for the plane scorer");
   using L = Layout<WIDE>;
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -455,8 +462,12 @@ score_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CU
   const int g1 = (int)(total * (blockIdx.x + 1) / gridDim.x);
   volatile int *abort_flag = misc + 1;
 
-  if (warp == 0) {
+  if (warp == 0 || (NPROD == 2 && warp == 6)) {
     // ------------------------------------------------------------ producer
+    // With two producers, producer pp issues the tiles whose place in the
+    // CTA's tile sequence has parity pp; both walk every tile to keep the
+    // ring's stage and phase, and producer 0 alone loads the queries.
+    const int pp = NPROD == 2 && warp == 6 ? 1 : 0;
     const uint64_t pol = policy_evict_first();
     int stage = 0;
     uint32_t sphase = 0;
@@ -470,7 +481,7 @@ score_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CU
 #ifdef ICP_TIMELINE
     if (lane == 0 && walk.b >= 0) ICP_STAMP(18);
 #endif
-    if (a.pdl) {
+    if (a.pdl && pp == 0) {
       // Early start: while the preceding kernel finishes, pull the first
       // tiles of this CTA into L2, only from pages lying wholly below
       // position seq_len - dql (the newest keys may still be appended by the
@@ -499,6 +510,8 @@ score_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CU
       __syncwarp();
       pdl_wait();
       if (lane == 0) ICP_STAMP(12);
+    } else if (a.pdl) {
+      pdl_wait();
     }
     while (ok && walk.next(b, t0, t1)) {
 #ifdef ICP_TIMELINE
@@ -510,13 +523,13 @@ score_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CU
 #ifdef ICP_TIMELINE
       if (lane == 0 && issued == 0 && nunits >= 0) ICP_STAMP(16);
 #endif
-      if (lane == 0) ok = mbar_wait(bar_qempty(qslot), qph ^ 1u, abort_flag);
+      if (pp == 0 && lane == 0) ok = mbar_wait(bar_qempty(qslot), qph ^ 1u, abort_flag);
       ok = __shfl_sync(0xFFFFFFFFu, ok, 0) != 0;
       if (!ok) break;
 #ifdef ICP_TIMELINE
       if (lane == 0 && issued == 0) ICP_STAMP(17);
 #endif
-      if (lane == 0) {
+      if (pp == 0 && lane == 0) {
         mbar_arrive_expect_tx(bar_qfull(qslot), L::q_bytes);
         if constexpr (WIDE) {
           tma_load_2d(sb + L::off_q + qslot * L::q_bytes, &tmq, 0, rv.tok0 * 4, bar_qfull(qslot));
@@ -563,6 +576,15 @@ score_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CU
           pg_nxt = (grp + 32 + lane < cend) ? btrow[page_slot_of(grp + 32 + lane, g.split)] : 0;
         }
         const int ncol = min(g.cpt, cend - c0);
+        if (NPROD == 2 && (int)(issued & 1) != pp) {
+          // the other producer's tile: only the ring position advances
+          ++issued;
+          if (++stage == kStages) {
+            stage = 0;
+            sphase ^= 1u;
+          }
+          continue;
+        }
         // WIDE: tiles go in pairs (t0, t0 + 1), ... into slots of two
         // adjacent stages, one barrier per slot; j is the tile in its pair
         const int j = WIDE ? ((tl - t0) & 1) : 0;
@@ -605,15 +627,17 @@ score_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CU
           }
         }
       }
-      if (ok) count_bad_entry(a, b, rv, btrow, __reduce_min_sync(0xFFFFFFFFu, first_bad), lane);
+      if (ok && pp == 0)
+        count_bad_entry(a, b, rv, btrow, __reduce_min_sync(0xFFFFFFFFu, first_bad), lane);
     }
     if (*abort_flag && lane == 0) {
       // let copies still in flight land before the CTA exits
       constexpr int nst = WIDE ? kStages / 2 : kStages;
       const long long first = issued > nst ? issued - nst : 0;
       for (long long n = first; n < issued; ++n)
-        mbar_wait_drain(bar_full((int)(n % nst)), (uint32_t)((n / nst) & 1));
-      if (last_qslot >= 0)
+        if (NPROD == 1 || (int)(n & 1) == pp)
+          mbar_wait_drain(bar_full((int)(n % nst)), (uint32_t)((n / nst) & 1));
+      if (pp == 0 && last_qslot >= 0)
         mbar_wait_drain(bar_qfull(last_qslot), (last_qslot ? qph1 : qph0) ^ 1u);
     }
   } else if (warp == 1) {
@@ -731,7 +755,7 @@ score_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CU
         // columns [units, round_up(the request's units, 4)) of the rows this
         // CTA owns: padding, or blocks past every one of the rows' tokens
         const int npad = min(wcols, a.cols) - min(u, a.cols);
-        for (int k = et; k < npad * rows; k += NT - 64) {
+        for (int k = et; k < npad * rows; k += kEpiThreads) {
           const int r = k / npad, c = u + k % npad;
           a.score_out[((long long)rv.tok0 * 4 + r) * a.cols + c] = -INFINITY;
         }
@@ -910,6 +934,10 @@ cudaError_t score_prepare(int device) {
   e = cudaFuncSetAttribute(score_kernel<false, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            (int)smem_bytes_for<false, true>(kMaxBatchDevice));
   if (e != cudaSuccess) return e;
+  e = cudaFuncSetAttribute(score_kernel<false, false, 2>,
+                           cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           (int)smem_bytes_for<false>(kMaxBatchDevice));
+  if (e != cudaSuccess) return e;
   return cudaFuncSetAttribute(score_kernel<true, false>,
                               cudaFuncAttributeMaxDynamicSharedMemorySize,
                               (int)smem_bytes_for<true>(kMaxBatchDevice));
@@ -922,14 +950,21 @@ cudaError_t launch_score(const CUtensorMap &tmk, const CUtensorMap &tmq, const S
         tmk, tmq, a);
     return cudaGetLastError();
   }
+  // a tile of two or four page slices is as many TMA boxes: two producer
+  // warps issue them
+  const bool two = a.g.cpt >= 2;
   if (!a.pdl) {
-    score_kernel<false, false><<<grid, kThreads, smem_bytes_for<false>(a.batch), stream>>>(
-        tmk, tmq, a);
+    if (two)
+      score_kernel<false, false, 2><<<grid, BlockThreads<false, 2>::value,
+                                      smem_bytes_for<false>(a.batch), stream>>>(tmk, tmq, a);
+    else
+      score_kernel<false, false><<<grid, kThreads, smem_bytes_for<false>(a.batch), stream>>>(
+          tmk, tmq, a);
     return cudaGetLastError();
   }
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)grid);
-  cfg.blockDim = dim3(kThreads);
+  cfg.blockDim = dim3(two ? BlockThreads<false, 2>::value : kThreads);
   cfg.dynamicSmemBytes = smem_bytes_for<false>(a.batch);
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];
@@ -937,11 +972,13 @@ cudaError_t launch_score(const CUtensorMap &tmk, const CUtensorMap &tmq, const S
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, score_kernel<false, false>, tmk, tmq, a);
+  return two ? cudaLaunchKernelEx(&cfg, score_kernel<false, false, 2>, tmk, tmq, a)
+             : cudaLaunchKernelEx(&cfg, score_kernel<false, false>, tmk, tmq, a);
 }
 
 cudaError_t launch_score_select(const CUtensorMap &tmk, const CUtensorMap &tmq, ScoreArgs a,
                                 int grid, cudaStream_t stream) {
+  // (a second producer made the fused scorer slower on the sharded layout)
   grid = grid > kFusedMaxGrid ? kFusedMaxGrid : grid;
   score_kernel<true, false><<<grid, kThreads, smem_bytes_for<true>(a.batch), stream>>>(tmk, tmq,
                                                                                        a);
