@@ -924,8 +924,8 @@ def timed_fused(bench, steps, warmup):
 
 def timed_step_with_scorer_pdl(bench, steps, warmup, local):
     """The decode step with the scorers launched under programmatic dependent
-    launch (early start: set-up and an L2 prefetch of the first pages ahead
-    of griddepcontrol.wait), timed like the step itself: ms per step."""
+    launch (early start: the CTAs' set-up runs ahead of griddepcontrol.wait),
+    timed like the step itself: ms per step."""
     bench.score_pdl = True
     try:
         step_ms, _, _ = timed_graphs(bench, steps, warmup, local)

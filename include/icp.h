@@ -94,12 +94,11 @@ int icp_score_columns(int max_seq_len, int page_size, int world_size);
  *   4 * max_decode_query_len <= 32; 0 <= batch <= ICP_MAX_BATCH.
  *   enable_pdl (parameter enable_pdl of the same page): non-zero launches with
  *   programmatic dependent launch.  Ahead of its griddepcontrol.wait the
- *   kernel only reads seq_lens and block_table and warms L2 with the index_k
- *   pages lying wholly below position seq_len - decode_query_len; no other
- *   load and no store precedes the wait.  The caller guarantees that the
- *   kernel queued just ahead leaves seq_lens, block_table and those pages
- *   alone, and that it is either an ordinary launch or one that waits for its
- *   own predecessor before it signals its dependents.
+ *   kernel only sets itself up (barriers, tensor memory, and the split of
+ *   the work, read from seq_lens); no other load and no store precedes the
+ *   wait.  The caller guarantees that the kernel queued just ahead leaves
+ *   seq_lens alone, and that it is either an ordinary launch or one that
+ *   waits for its own predecessor before it signals its dependents.
  *   0 removes the requirement.
  *   errors: optional int32 [>= 1] counter of timed-out internal waits,
  *           requests with block-table entries outside the pool, and requests

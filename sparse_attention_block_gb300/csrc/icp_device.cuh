@@ -149,14 +149,6 @@ __device__ __forceinline__ uint64_t policy_evict_first() {
   return p;
 }
 
-// L2 prefetch of a 2D tile (no shared memory, no completion to wait for).
-__device__ __forceinline__ void tma_prefetch_l2_2d(const CUtensorMap *map, int x, int y) {
-  asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];" ::"l"(
-                   reinterpret_cast<uint64_t>(map)),
-               "r"(x), "r"(y)
-               : "memory");
-}
-
 // Programmatic dependent launch: wait until the preceding grid's memory
 // operations are visible / allow the next grid to start launching.
 __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }

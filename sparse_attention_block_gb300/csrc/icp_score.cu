@@ -481,37 +481,12 @@ score_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CU
 #ifdef ICP_TIMELINE
     if (lane == 0 && walk.b >= 0) ICP_STAMP(18);
 #endif
-    if (a.pdl && pp == 0) {
-      // Early start: while the preceding kernel finishes, pull the first
-      // tiles of this CTA into L2, only from pages lying wholly below
-      // position seq_len - dql (the newest keys may still be appended by the
-      // preceding kernel); every real load below is issued after the wait.
-      // The first 2 * kStages tiles' columns are spread over the lanes, so
-      // their block-table reads are in flight together.
-      SegmentWalker pw(prefix, nbatch, g0, g1, WIDE ? kWideRequestUnits : 0);
-      int pb, p0, p1, budget = 2 * kStages * g.cpt;  // columns
-      while (budget > 0 && pw.next(pb, p0, p1)) {
-        const ReqView rv = req_view(a, pb);
-        const int nunits = units_of(rv.seq_len, a.page_size, g.split);
-        const int32_t *btrow = a.block_table + (long long)rv.bt_row * a.bt_stride;
-        const long long safe_end = (long long)rv.seq_len - rv.ntok;
-        const int c0 = p0 * g.cpt;
-        const int c1 = min(min(p1 * g.cpt, nunits), c0 + budget);
-        budget -= max(c1 - c0, 1);
-        for (int c = c0 + lane; c < c1; c += 32) {
-          const int slot = page_slot_of(c, g.split);
-          if ((long long)(slot + 1) * a.page_size <= safe_end) {
-            const int pg = btrow[slot];
-            if ((unsigned)pg < (unsigned)a.num_pages)
-              tma_prefetch_l2_2d(&tmk, 0, pg * g.rows_per_page + row_off_of(c, g.split));
-          }
-        }
-      }
-      __syncwarp();
+    if (a.pdl) {
+      // Early start: the set-up above (barriers, TMEM, the tile prefix sums
+      // from seq_lens) ran while the preceding kernel finished; every load
+      // of the step's data comes after the wait.
       pdl_wait();
       if (lane == 0) ICP_STAMP(12);
-    } else if (a.pdl) {
-      pdl_wait();
     }
     while (ok && walk.next(b, t0, t1)) {
 #ifdef ICP_TIMELINE
