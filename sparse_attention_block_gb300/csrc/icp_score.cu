@@ -332,10 +332,20 @@ __device__ __forceinline__ void epilogue_tile_wide(const ScoreArgs &a, uint32_t 
   const long long pfirst = (long long)seq_len - ntok;  // position of token 0
   const long long p_lane = pfirst + (row >> 2);        // position of this row's token
   const bool row_ok = row < 4 * ntok;
-  // the whole tile in registers with one wait, then reductions with the most
-  // independent work first
+  // the whole tile in registers with one wait; the load also returns each
+  // column's maximum over its R keys, which is the plane value of every
+  // column that no row's causal limit cuts
   float v[128];
-  tmem_ld128(ta, v);
+  float mx[CPT];
+  if constexpr (R == 128) {
+    tmem_ld_max128(ta, v, mx[0]);
+  } else {
+#pragma unroll
+    for (int cc = 0; cc < CPT; ++cc) {
+      if constexpr (R == 64) tmem_ld_max64(ta + cc * R, v + cc * R, mx[cc]);
+      else tmem_ld_max32(ta + cc * R, v + cc * R, mx[cc]);
+    }
+  }
   tmem_wait_ld();
   if (release) {
     tc_fence_before();
@@ -349,6 +359,7 @@ __device__ __forceinline__ void epilogue_tile_wide(const ScoreArgs &a, uint32_t 
     const long long pos0 = g.split ? (long long)c * 128
                                    : (long long)c * a.page_size +
                                          (long long)a.rank * g.rows_per_page;
+    float val = mx[cc];
     if (pos0 + R - 1 > pfirst) {
       // keys i <= lim of the column are at or before the row's token
       const long long d = p_lane - pos0;
@@ -356,10 +367,11 @@ __device__ __forceinline__ void epilogue_tile_wide(const ScoreArgs &a, uint32_t 
 #pragma unroll
       for (int i = 0; i < R; ++i)
         if (i > lim) vc[i] = -INFINITY;
+      max_tree3<R>(vc);
+      val = vc[0];
     }
-    max_tree3<R>(vc);
     if (c < nunits && c < a.cols && row_ok)
-      a.score_out[((long long)tok0 * 4 + row) * a.cols + c] = vc[0] + 0.0f;  // + 0 folds -0
+      a.score_out[((long long)tok0 * 4 + row) * a.cols + c] = val + 0.0f;  // + 0 folds -0
   }
 }
 
