@@ -332,34 +332,14 @@ __device__ __forceinline__ void epilogue_tile_wide(const ScoreArgs &a, uint32_t 
   const long long pfirst = (long long)seq_len - ntok;  // position of token 0
   const long long p_lane = pfirst + (row >> 2);        // position of this row's token
   const bool row_ok = row < 4 * ntok;
-  // the whole tile in registers with one wait; the load also returns each
-  // column's maximum over its R keys, which is the plane value of every
-  // column that no row's causal limit cuts
-  float v[128];
-  float mx[CPT];
-  if constexpr (R == 128) {
-    tmem_ld_max128(ta, v, mx[0]);
-  } else {
-#pragma unroll
-    for (int cc = 0; cc < CPT; ++cc) {
-      if constexpr (R == 64) tmem_ld_max64(ta + cc * R, v + cc * R, mx[cc]);
-      else tmem_ld_max32(ta + cc * R, v + cc * R, mx[cc]);
-    }
-  }
-  tmem_wait_ld();
-  if (release) {
-    tc_fence_before();
-    __syncwarp();
-    if (lane == 0) mbar_arrive(tempty);
-  }
-#pragma unroll
-  for (int cc = 0; cc < CPT; ++cc) {
+  // The load also returns each column's maximum over its R keys: the plane
+  // value of every column that no row's causal limit cuts.  A cut column
+  // masks its keys in registers and folds them with a max tree.
+  auto column = [&](int cc, float *vc, float mx) {
     const int c = tl * CPT + cc;
-    float *vc = v + cc * R;
     const long long pos0 = g.split ? (long long)c * 128
                                    : (long long)c * a.page_size +
                                          (long long)a.rank * g.rows_per_page;
-    float val = mx[cc];
     if (pos0 + R - 1 > pfirst) {
       // keys i <= lim of the column are at or before the row's token
       const long long d = p_lane - pos0;
@@ -368,11 +348,35 @@ __device__ __forceinline__ void epilogue_tile_wide(const ScoreArgs &a, uint32_t 
       for (int i = 0; i < R; ++i)
         if (i > lim) vc[i] = -INFINITY;
       max_tree3<R>(vc);
-      val = vc[0];
+      mx = vc[0];
     }
+    return mx;
+  };
+  auto store = [&](int cc, float val) {
+    const int c = tl * CPT + cc;
     if (c < nunits && c < a.cols && row_ok)
       a.score_out[((long long)tok0 * 4 + row) * a.cols + c] = val + 0.0f;  // + 0 folds -0
+  };
+  auto hand_back = [&]() {
+    if (release) {
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(tempty);
+    }
+  };
+  // the whole tile in registers with one wait
+  float v[128];
+  float mx[CPT];
+#pragma unroll
+  for (int cc = 0; cc < CPT; ++cc) {
+    if constexpr (R == 128) tmem_ld_max128(ta, v, mx[0]);
+    else if constexpr (R == 64) tmem_ld_max64(ta + cc * R, v + cc * R, mx[cc]);
+    else tmem_ld_max32(ta + cc * R, v + cc * R, mx[cc]);
   }
+  tmem_wait_ld();
+  hand_back();
+#pragma unroll
+  for (int cc = 0; cc < CPT; ++cc) store(cc, column(cc, v + cc * R, mx[cc]));
 }
 
 // WIDE: the prefill scorer.  A request (a plan record of up to 64 tokens)
@@ -386,7 +390,7 @@ __device__ __forceinline__ void epilogue_tile_wide(const ScoreArgs &a, uint32_t 
 // set s finishing tile s of every item for the half's rows; each warp takes
 // its lane quarter (8 of the half's 32 tokens) and the accumulator is free
 // again after all eight warps have arrived.
-template <bool FUSED, bool WIDE, int NPROD = 1>
+template <bool FUSED, bool WIDE, int NPROD = 1, int RW = 0>
 __global__ void __launch_bounds__(BlockThreads<WIDE, NPROD>::value, 1)
 score_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmq,
              const ScoreArgs a) {
@@ -398,6 +402,7 @@ score_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CU
   constexpr int NT = BlockThreads<WIDE, NPROD>::value;
   constexpr int kEpiThreads = WIDE ? 128 * kEpiSetsWide : 128;
   static_assert(NPROD == 1 || (!WIDE && !FUSED), "a second producer only for the plane scorer");
+  static_assert(!WIDE || RW == 128 || RW == 64 || RW == 32, "prefill: RW = g.R, one kernel each");
   using L = Layout<FUSED, WIDE, NPROD>;
   constexpr int NS = RingStages<FUSED, WIDE, NPROD>::value;
   const int warp = threadIdx.x >> 5;
@@ -831,15 +836,9 @@ score_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CU
               const uint32_t tj = tmem_base + ((uint32_t)(q * 32) << 16) +
                                   (uint32_t)acc * (2 * kAccCols) + (uint32_t)set * kAccCols;
               const int rowq = h * 128 + q * 32;
-              if (g.R == 128)
-                epilogue_tile_wide<128>(a, tj, lane, rowq, rv.tok0, rv.ntok, tl + set, nunits,
-                                        seq_len, bar_tempty(acc), true);
-              else if (g.R == 64)
-                epilogue_tile_wide<64>(a, tj, lane, rowq, rv.tok0, rv.ntok, tl + set, nunits,
-                                       seq_len, bar_tempty(acc), true);
-              else
-                epilogue_tile_wide<32>(a, tj, lane, rowq, rv.tok0, rv.ntok, tl + set, nunits,
-                                       seq_len, bar_tempty(acc), true);
+              epilogue_tile_wide<(WIDE ? RW : 128)>(a, tj, lane, rowq, rv.tok0, rv.ntok,
+                                                    tl + set, nunits, seq_len, bar_tempty(acc),
+                                                    true);
             } else {
               // a segment's odd last tile: nothing for this set to read
               tc_fence_before();
@@ -933,9 +932,14 @@ cudaError_t score_prepare(int device) {
                                        cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        (int)smem_bytes_for<false>(kMaxBatchDevice));
   if (e != cudaSuccess) return e;
-  e = cudaFuncSetAttribute(score_kernel<false, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           (int)smem_bytes_for<false, true>(kMaxBatchDevice));
-  if (e != cudaSuccess) return e;
+  // the prefill scorer: one kernel per page-slice height, each with a
+  // single epilogue (a run-time choice among three raised its register peak)
+  for (auto k : {score_kernel<false, true, 1, 128>, score_kernel<false, true, 1, 64>,
+                 score_kernel<false, true, 1, 32>}) {
+    e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)smem_bytes_for<false, true>(kMaxBatchDevice));
+    if (e != cudaSuccess) return e;
+  }
   e = cudaFuncSetAttribute(score_kernel<false, false, 2>,
                            cudaFuncAttributeMaxDynamicSharedMemorySize,
                            (int)smem_bytes_for<false, false, 2>(kMaxBatchDevice));
@@ -948,8 +952,13 @@ cudaError_t score_prepare(int device) {
 cudaError_t launch_score(const CUtensorMap &tmk, const CUtensorMap &tmq, const ScoreArgs &a,
                          int grid, cudaStream_t stream) {
   if (a.wide) {
-    score_kernel<false, true><<<grid, kThreadsWide, smem_bytes_for<false, true>(a.batch), stream>>>(
-        tmk, tmq, a);
+    const size_t smem = smem_bytes_for<false, true>(a.batch);
+    if (a.g.R == 128)
+      score_kernel<false, true, 1, 128><<<grid, kThreadsWide, smem, stream>>>(tmk, tmq, a);
+    else if (a.g.R == 64)
+      score_kernel<false, true, 1, 64><<<grid, kThreadsWide, smem, stream>>>(tmk, tmq, a);
+    else
+      score_kernel<false, true, 1, 32><<<grid, kThreadsWide, smem, stream>>>(tmk, tmq, a);
     return cudaGetLastError();
   }
   // a tile of two or four page slices is as many TMA boxes: two producer
