@@ -680,7 +680,9 @@ score_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CU
             const uint32_t kaddr = sb + kOffStages + stage * 2 * kTileBytes;
             const uint32_t id = np == 2 ? idesc_f8_f32(128, 2 * (int)kAccCols) : idesc;
             for (int h = 0; h < nh; ++h) {
-              ICP_TIMED(21, ok = mbar_wait(bar_tempty(acc), aphase ^ 1u, abort_flag));
+              // the hand-back of an accumulator is on the MMA's critical
+              // path: poll rather than sleep
+              ICP_TIMED(21, ok = mbar_wait_spin(bar_tempty(acc), aphase ^ 1u, abort_flag));
               if (!ok) break;
               tc_fence_after();
               const uint32_t d = tmem_base + (uint32_t)acc * (2 * kAccCols);
@@ -825,11 +827,14 @@ score_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CU
           for (int h = 0; ok && h < nh; ++h, ++pi) {
             const int acc = pi & 1;
             const uint32_t wph = (uint32_t)(pi >> 1) & 1u;
-            if (lane == 0) {
-              if (warp == 2) ICP_TIMED(22, ok = mbar_wait(bar_tfull(acc), wph, abort_flag));
-              else ok = mbar_wait(bar_tfull(acc), wph, abort_flag);
-            }
-            ok = __shfl_sync(0xFFFFFFFFu, ok, 0) != 0;
+            // every lane waits (no lane-0 branch and broadcast)
+#ifdef ICP_TIMELINE
+            if (warp == 2 && lane == 0) ICP_TIMED(22, ok = mbar_wait(bar_tfull(acc), wph, abort_flag));
+            else ok = mbar_wait(bar_tfull(acc), wph, abort_flag);
+#else
+            ok = mbar_wait(bar_tfull(acc), wph, abort_flag);
+#endif
+            ok = __all_sync(0xFFFFFFFFu, ok);
             if (!ok) break;
             tc_fence_after();
             if (set < np) {
