@@ -266,8 +266,16 @@ __device__ __forceinline__ void epilogue_tile(const ScoreArgs &a, uint32_t taddr
                                               LaneTop &lt, unsigned long long *lk, int *lfid,
                                               float *lfsc) {
   constexpr int CPT = 128 / R;
+  // the tile in registers, and each column's maximum over its R keys from
+  // the reducing load
   float v[128];
-  tmem_ld128(taddr, v);
+  float mx[CPT];
+#pragma unroll
+  for (int cc = 0; cc < CPT; ++cc) {
+    if constexpr (R == 128) tmem_ld_max128(taddr, v, mx[0]);
+    else if constexpr (R == 64) tmem_ld_max64(taddr + cc * R, v + cc * R, mx[cc]);
+    else tmem_ld_max32(taddr + cc * R, v + cc * R, mx[cc]);
+  }
   tmem_wait_ld();
   // the accumulator is in registers: hand it back to the MMA warp
   tc_fence_before();
@@ -287,13 +295,16 @@ __device__ __forceinline__ void epilogue_tile(const ScoreArgs &a, uint32_t taddr
     const long long pos0 = g.split ? (long long)c * 128
                                    : (long long)c * a.page_size +
                                          (long long)a.rank * g.rows_per_page;
+    float val = mx[cc];
     if (pos0 + R - 1 > pfirst) {
+      // the column reaches past the first token: mask, then fold
 #pragma unroll
       for (int i = 0; i < R; ++i)
         if (pos0 + i > p_lane) vc[i] = -INFINITY;
+      max_tree3<R>(vc);
+      val = vc[0];
     }
-    max_tree3<R>(vc);
-    const float val = vc[0] + 0.0f;  // + 0 folds -0 onto +0
+    val += 0.0f;  // + 0 folds -0 onto +0
     if (row_ok && c < a.cols) {
       if constexpr (!FUSED) {
         const long long prow = (long long)tok0 * 4 + row;
@@ -364,19 +375,31 @@ __device__ __forceinline__ void epilogue_tile_wide(const ScoreArgs &a, uint32_t 
       if (lane == 0) mbar_arrive(tempty);
     }
   };
-  // the whole tile in registers with one wait
-  float v[128];
-  float mx[CPT];
+  if constexpr (R == 128) {
+    // the whole tile in registers with one wait
+    float v[128];
+    float mx;
+    tmem_ld_max128(ta, v, mx);
+    tmem_wait_ld();
+    hand_back();
+    store(0, column(0, v, mx));
+  } else {
+    // one column at a time (a wait each): the kernel's registers then stay
+    // below the ten-warp limit without spills
+    float val[CPT];
 #pragma unroll
-  for (int cc = 0; cc < CPT; ++cc) {
-    if constexpr (R == 128) tmem_ld_max128(ta, v, mx[0]);
-    else if constexpr (R == 64) tmem_ld_max64(ta + cc * R, v + cc * R, mx[cc]);
-    else tmem_ld_max32(ta + cc * R, v + cc * R, mx[cc]);
+    for (int cc = 0; cc < CPT; ++cc) {
+      float v[R];
+      float mx;
+      if constexpr (R == 64) tmem_ld_max64(ta + cc * R, v, mx);
+      else tmem_ld_max32(ta + cc * R, v, mx);
+      tmem_wait_ld();
+      val[cc] = column(cc, v, mx);
+    }
+    hand_back();
+#pragma unroll
+    for (int cc = 0; cc < CPT; ++cc) store(cc, val[cc]);
   }
-  tmem_wait_ld();
-  hand_back();
-#pragma unroll
-  for (int cc = 0; cc < CPT; ++cc) store(cc, column(cc, v + cc * R, mx[cc]));
 }
 
 // WIDE: the prefill scorer.  A request (a plan record of up to 64 tokens)
