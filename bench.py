@@ -47,10 +47,10 @@ FALLBACK_HBM_GBS = 6800.0
 # not part of it).  When the code changes the digest no longer matches and
 # `traffic` is reported null.
 NCU_TRAFFIC = {
-    # dram__bytes_read.sum + dram__bytes_write.sum = 278865152 + 3031552 bytes for
+    # dram__bytes_read.sum + dram__bytes_write.sum = 278827776 + 3077888 bytes for
     # 278330624 bytes of index-K: one ncu capture of a launch over the first 32
     # requests of the multitoken workload
-    ("multitoken", "8087223e9fbf7e96"): (278865152 + 3031552) / 278330624,
+    ("multitoken", "e2c828233b81d928"): (278827776 + 3077888) / 278330624,
 }
 
 
