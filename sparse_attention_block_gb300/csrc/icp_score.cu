@@ -410,9 +410,11 @@ __device__ __forceinline__ void epilogue_tile_wide(const ScoreArgs &a, uint32_t 
 // the record has more than 32 tokens) into one of two 256-column
 // accumulators, items alternating, so each key byte read serves 256 query
 // rows at the N = 256 MMA rate.  The epilogue warps form two sets of four,
-// set s finishing tile s of every item for the half's rows; each warp takes
-// its lane quarter (8 of the half's 32 tokens) and the accumulator is free
-// again after all eight warps have arrived.
+// set s owning accumulator s: it finishes every item of parity s, one tile
+// after the other, each warp its lane quarter (8 of the half's 32 tokens),
+// and the accumulator is free again after the set's four warps have read
+// both tiles.  The two warps that share a scheduler thus work on different
+// items.
 template <bool FUSED, bool WIDE, int NPROD = 1, int RW = 0>
 __global__ void __launch_bounds__(BlockThreads<WIDE, NPROD>::value, 1)
 score_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmq,
@@ -456,7 +458,7 @@ score_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CU
     }
     for (int i = 0; i < kAcc; ++i) {
       mbar_init(bar_tfull(i), 1);
-      mbar_init(bar_tempty(i), WIDE ? 4 * kEpiSetsWide : 1);
+      mbar_init(bar_tempty(i), WIDE ? 4 : 1);
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(bar_qfull(i), 1);
@@ -839,16 +841,17 @@ score_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CU
         for (int j = 0; j < kTopK; ++j) lk[j * 32 + lane] = 0ull;
       }
       if constexpr (WIDE) {
-        // every (tile pair, row half) item: set s finishes the pair's tile s
-        // for the half's rows, this warp's lane quarter (tokens 32 h + 8 q
-        // .. 32 h + 8 q + 7); pi counts the CTA's items as the MMA thread
-        // does, item pi sits in accumulator pi & 1
+        // every (tile pair, row half) item: pi counts the CTA's items as the
+        // MMA thread does, item pi sits in accumulator pi & 1, and set s
+        // takes the items of accumulator s, the pair's tiles in turn, for
+        // this warp's lane quarter (tokens 32 h + 8 q .. 32 h + 8 q + 7)
         const int set = (warp - 2) >> 2;
         const int nh = rv.ntok > kPlanTokens / 2 ? 2 : 1;
         for (int tl = t0; ok && tl < t1; tl += 2) {
           const int np = min(2, t1 - tl);
           for (int h = 0; ok && h < nh; ++h, ++pi) {
-            const int acc = pi & 1;
+            if ((pi & 1) != set) continue;
+            const int acc = set;
             const uint32_t wph = (uint32_t)(pi >> 1) & 1u;
             // every lane waits (no lane-0 branch and broadcast)
 #ifdef ICP_TIMELINE
@@ -860,19 +863,14 @@ score_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CU
             ok = __all_sync(0xFFFFFFFFu, ok);
             if (!ok) break;
             tc_fence_after();
-            if (set < np) {
-              const uint32_t tj = tmem_base + ((uint32_t)(q * 32) << 16) +
-                                  (uint32_t)acc * (2 * kAccCols) + (uint32_t)set * kAccCols;
-              const int rowq = h * 128 + q * 32;
-              epilogue_tile_wide<(WIDE ? RW : 128)>(a, tj, lane, rowq, rv.tok0, rv.ntok,
-                                                    tl + set, nunits, seq_len, bar_tempty(acc),
-                                                    true);
-            } else {
-              // a segment's odd last tile: nothing for this set to read
-              tc_fence_before();
-              __syncwarp();
-              if (lane == 0) mbar_arrive(bar_tempty(acc));
-            }
+            const uint32_t tj = tmem_base + ((uint32_t)(q * 32) << 16) +
+                                (uint32_t)acc * (2 * kAccCols);
+            const int rowq = h * 128 + q * 32;
+            // the second tile (if any) hands the accumulator back
+            for (int j = 0; j < np; ++j)
+              epilogue_tile_wide<(WIDE ? RW : 128)>(a, tj + (uint32_t)j * kAccCols, lane, rowq,
+                                                    rv.tok0, rv.ntok, tl + j, nunits, seq_len,
+                                                    bar_tempty(acc), j == np - 1);
 #ifdef ICP_TIMELINE
             if (warp == 2 && lane == 0) {
               if (pi == 0) ICP_STAMP(6);
