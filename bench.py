@@ -47,10 +47,10 @@ FALLBACK_HBM_GBS = 6800.0
 # not part of it).  When the code changes the digest no longer matches and
 # `traffic` is reported null.
 NCU_TRAFFIC = {
-    # dram__bytes_read.sum + dram__bytes_write.sum = 278827776 + 3077888 bytes for
+    # dram__bytes_read.sum + dram__bytes_write.sum = 278836992 + 3306240 bytes for
     # 278330624 bytes of index-K: one ncu capture of a launch over the first 32
     # requests of the multitoken workload
-    ("multitoken", "e2c828233b81d928"): (278827776 + 3077888) / 278330624,
+    ("multitoken", "a9ef42467d3b3efc"): (278836992 + 3306240) / 278330624,
 }
 
 
