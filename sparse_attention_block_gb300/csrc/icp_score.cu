@@ -27,8 +27,10 @@
 //              All 4 heads and all dql tokens share one K tile.
 //   warps 2-5  epilogue: tile i belongs to epilogue warp i % 4, which reads
 //              its lane quarter of the accumulator (thread = query row,
-//              registers = the tile's 128 key scores), applies the causal
-//              mask and folds each column's keys with a register max tree.
+//              registers = the tile's 128 key scores) with the reducing TMEM
+//              load: it also returns each column's maximum over its keys,
+//              the column value unless the causal limit cuts the column,
+//              whose keys are then masked and folded by a register max tree.
 //              Scorer: one plane store per (query row, column).
 //              Fused: the column value goes into the row's running Top16
 //              (forced ids kept aside); at the end of each request segment
@@ -87,7 +89,7 @@ constexpr int kQBytes = 4 * kQRows * 128;  // four copies -> the 128-row A opera
 constexpr int kQBytesWide = 4 * kPlanTokens * 128;
 static_assert(4 * kPlanTokens == 256, "a record's query rows are two 128-row operands");
 constexpr int kThreads = 192;
-// prefill scorer: two sets of four epilogue warps take alternate tiles
+// prefill scorer: two sets of four epilogue warps, one per accumulator
 constexpr int kEpiSetsWide = 2;
 constexpr int kThreadsWide = 64 + 128 * kEpiSetsWide;
 // NPROD 2: a second producer warp (warp 6) takes every other tile; used when
@@ -170,7 +172,7 @@ __device__ __forceinline__ int page_slot_of(int c, int split) { return split ? (
 
 // What the kernel needs of request b: a decode request (token rows
 // b * dql .. + dql, its own block-table row and seq_len), or a record of a
-// prefill plan (up to 8 consecutive tokens of a request's chunk).
+// prefill plan (up to kPlanTokens = 64 consecutive tokens of a request's chunk).
 struct ReqView {
   int seq_len;   // positions seen by the tokens: the last one is seq_len - 1
   int tok0;      // first token (index_q / plane rows tok0 * 4 ...)
