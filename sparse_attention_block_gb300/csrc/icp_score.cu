@@ -63,9 +63,18 @@ __device__ unsigned long long g_timeline[kTimelineCtas * kTimelineSlots];
     wait;                                                                  \
     g_timeline[blockIdx.x * kTimelineSlots + (slot)] += globaltimer_ns() - icp_t0_; \
   } while (0)
+// the same inside a loop that the whole warp runs: lane 0 keeps the sum
+#define ICP_TIMED_WARP(slot, wait)                                         \
+  do {                                                                     \
+    const unsigned long long icp_t0_ = globaltimer_ns();                   \
+    wait;                                                                  \
+    if ((threadIdx.x & 31) == 0)                                           \
+      g_timeline[blockIdx.x * kTimelineSlots + (slot)] += globaltimer_ns() - icp_t0_; \
+  } while (0)
 #else
 #define ICP_STAMP(slot) ((void)0)
 #define ICP_TIMED(slot, wait) wait
+#define ICP_TIMED_WARP(slot, wait) wait
 #endif
 
 namespace {
@@ -676,9 +685,13 @@ score_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CU
     }
   } else if (warp == 1) {
     // ---------------------------------------------------------- MMA issuer
-    // One thread issues every MMA and runs the loop alone: no per-tile
-    // reconvergence of the warp.
-    if (lane == 0) {
+    // Decode: one thread issues every MMA and runs the loop alone (no
+    // per-tile reconvergence of the warp).  Prefill, where the issue rate
+    // sets the pace: the whole warp runs the loop, every lane waits, and the
+    // lane elect.sync picks issues each MMA and commit; the warp-uniform
+    // descriptors then stay in uniform registers (a lone issuing thread
+    // took 54.6 us on the benched window, the warp 52.0 us).
+    if (WIDE || lane == 0) {
       const uint32_t idesc = idesc_f8_f32(128, (int)kAccCols);
 #ifdef ICP_TIMELINE
       long long mma_tiles = 0;
@@ -692,6 +705,7 @@ score_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CU
       bool ok = true;
       while (ok && walk.next(b, t0, t1)) {
         ok = mbar_wait(bar_qfull(qslot), qslot ? qph1 : qph0, abort_flag);
+        if constexpr (WIDE) ok = __all_sync(0xFFFFFFFFu, ok);  // the lanes leave together
         if (!ok) break;
         const uint32_t qaddr = sb + L::off_q + qslot * L::q_bytes;
         if constexpr (WIDE) {
@@ -702,33 +716,36 @@ score_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CU
           const int nh = req_view(a, b).ntok > kPlanTokens / 2 ? 2 : 1;
           for (int tl = t0; ok && tl < t1; tl += 2) {
             const int np = min(2, t1 - tl);
-            ICP_TIMED(20, ok = mbar_wait(bar_full(stage), sphase, abort_flag));
+            ICP_TIMED_WARP(20, ok = mbar_wait(bar_full(stage), sphase, abort_flag));
+            ok = __all_sync(0xFFFFFFFFu, ok);
             if (!ok) break;
             const uint32_t kaddr = sb + kOffStages + stage * 2 * kTileBytes;
             const uint32_t id = np == 2 ? idesc_f8_f32(128, 2 * (int)kAccCols) : idesc;
             for (int h = 0; h < nh; ++h) {
               // the hand-back of an accumulator is on the MMA's critical
               // path: poll rather than sleep
-              ICP_TIMED(21, ok = mbar_wait_spin(bar_tempty(acc), aphase ^ 1u, abort_flag));
+              ICP_TIMED_WARP(21, ok = mbar_wait_spin(bar_tempty(acc), aphase ^ 1u, abort_flag));
+              ok = __all_sync(0xFFFFFFFFu, ok);
               if (!ok) break;
               tc_fence_after();
               const uint32_t d = tmem_base + (uint32_t)acc * (2 * kAccCols);
               const uint32_t qh = qaddr + (uint32_t)h * (128 * 128);
+              // K steps of 32 bytes advance both start addresses by 2 (16-byte units)
+              const uint64_t da = smem_desc_sw128(qh), db = smem_desc_sw128(kaddr);
 #pragma unroll
               for (int k = 0; k < 4; ++k)
-                mma_f8(d, smem_desc_sw128(qh + 32 * k), smem_desc_sw128(kaddr + 32 * k), id,
-                       k > 0 ? 1u : 0u);
-              mma_commit(bar_tfull(acc));
+                mma_f8_elect(d, da + 2u * k, db + 2u * k, id, k > 0 ? 1u : 0u);
+              mma_commit_elect(bar_tfull(acc));
               if (++acc == 2) {
                 acc = 0;
                 aphase ^= 1u;
               }
             }
             if (!ok) break;
-            mma_commit(bar_empty(stage));
+            mma_commit_elect(bar_empty(stage));
 #ifdef ICP_TIMELINE
-            if (mma_tiles++ == 0) ICP_STAMP(4);
-            ICP_STAMP(5);
+            if (mma_tiles++ == 0 && lane == 0) ICP_STAMP(4);
+            if (lane == 0) ICP_STAMP(5);
 #endif
             if (++stage == NS / 2) {
               stage = 0;
@@ -764,13 +781,15 @@ score_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CU
           }
         }
         if (!ok) break;
-        mma_commit(bar_qempty(qslot));
+        if constexpr (WIDE) mma_commit_elect(bar_qempty(qslot));
+        else mma_commit(bar_qempty(qslot));
         if (qslot) qph1 ^= 1u; else qph0 ^= 1u;
         qslot ^= 1;
       }
       if (*abort_flag) {
         // every MMA issued so far must finish before TMEM is released
-        mma_commit(bar_done);
+        if constexpr (WIDE) mma_commit_elect(bar_done);
+        else mma_commit(bar_done);
         mbar_wait_drain(bar_done, 0);
       }
     }
