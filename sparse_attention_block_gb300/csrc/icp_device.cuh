@@ -100,40 +100,6 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatil
   }
 }
 
-// Non-blocking probe of a phase (mbarrier.test_wait never suspends).
-__device__ __forceinline__ bool mbar_test_wait(uint32_t bar, uint32_t parity) {
-  uint32_t ok;
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
-      "selp.u32 %0, 1, 0, p;\n\t}"
-      : "=r"(ok)
-      : "r"(bar), "r"(parity)
-      : "memory");
-  return ok != 0;
-}
-
-// As mbar_wait, but the thread polls instead of sleeping in the barrier: it
-// resumes a few cycles after the phase completes, at the price of issue
-// slots.  For a lone thread whose wake-up latency is on the critical path.
-__device__ __forceinline__ bool mbar_wait_spin(uint32_t bar, uint32_t parity,
-                                               volatile int *abort) {
-  unsigned long long t0 = 0;
-  for (uint32_t it = 1;; ++it) {
-    if (mbar_test_wait(bar, parity)) return true;
-    if ((it & 1023u) == 0u) {
-      if (*abort) return false;
-      const unsigned long long now = globaltimer_ns();
-      if (t0 == 0) {
-        t0 = now;
-      } else if (now - t0 > kWaitTimeoutNs) {
-        *abort = 1;
-        return false;
-      }
-    }
-  }
-}
-
 // Same, with a short private limit, for draining copies after an abort.
 __device__ __forceinline__ bool mbar_wait_drain(uint32_t bar, uint32_t parity) {
   const unsigned long long t0 = globaltimer_ns();

@@ -722,9 +722,9 @@ score_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CU
             const uint32_t kaddr = sb + kOffStages + stage * 2 * kTileBytes;
             const uint32_t id = np == 2 ? idesc_f8_f32(128, 2 * (int)kAccCols) : idesc;
             for (int h = 0; h < nh; ++h) {
-              // the hand-back of an accumulator is on the MMA's critical
-              // path: poll rather than sleep
-              ICP_TIMED_WARP(21, ok = mbar_wait_spin(bar_tempty(acc), aphase ^ 1u, abort_flag));
+              // a sleeping wait: a warp polling here took issue slots from
+              // the epilogue warps on its scheduler (51.4 against 49.3 us)
+              ICP_TIMED_WARP(21, ok = mbar_wait(bar_tempty(acc), aphase ^ 1u, abort_flag));
               ok = __all_sync(0xFFFFFFFFu, ok);
               if (!ok) break;
               tc_fence_after();
