@@ -182,27 +182,11 @@ __device__ __forceinline__ void tc_fence_after() {
   asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
 }
 
-// D[tmem] (+)= A[smem] * B[smem]^T, fp8 e4m3 x e4m3 -> fp32, one CTA.
-__device__ __forceinline__ void mma_f8(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
-                                       uint32_t idesc, uint32_t accumulate) {
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "setp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
-      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
-      : "memory");
-}
-
-// Arrive on an mbarrier once all tcgen05 ops issued so far by this thread complete.
-__device__ __forceinline__ void mma_commit(uint32_t bar) {
-  asm volatile(
-      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
-      : "memory");
-}
-
-// Whole-warp forms of mma_f8 and mma_commit: every lane of the warp executes
-// them (its operands warp-uniform) and the one lane elect.sync picks issues,
-// so the warp stays converged and the operands stay in uniform registers.
+// D[tmem] (+)= A[smem] * B[smem]^T, fp8 e4m3 x e4m3 -> fp32, one CTA, and
+// the commit that arrives on an mbarrier once every tcgen05 op issued before
+// it completes.  Every lane of the warp executes them (the operands
+// warp-uniform) and the one lane elect.sync picks issues, so the warp stays
+// converged and the operands stay in uniform registers.
 __device__ __forceinline__ void mma_f8_elect(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
                                              uint32_t idesc, uint32_t accumulate) {
   asm volatile(

@@ -685,13 +685,12 @@ score_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CU
     }
   } else if (warp == 1) {
     // ---------------------------------------------------------- MMA issuer
-    // Decode: one thread issues every MMA and runs the loop alone (no
-    // per-tile reconvergence of the warp).  Prefill, where the issue rate
-    // sets the pace: the whole warp runs the loop, every lane waits, and the
-    // lane elect.sync picks issues each MMA and commit; the warp-uniform
-    // descriptors then stay in uniform registers (a lone issuing thread
-    // took 54.6 us on the benched window, the warp 52.0 us).
-    if (WIDE || lane == 0) {
+    // The whole warp runs the loop, every lane waits, and the lane
+    // elect.sync picks issues each MMA and commit; the warp-uniform
+    // descriptors then stay in uniform registers.  A lone issuing thread
+    // was slower everywhere: the prefill window 54.6 against 52.0 us, the
+    // batched decode scorer 0.785 against 0.825 of the copy peak.
+    {
       const uint32_t idesc = idesc_f8_f32(128, (int)kAccCols);
 #ifdef ICP_TIMELINE
       long long mma_tiles = 0;
@@ -705,7 +704,7 @@ score_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CU
       bool ok = true;
       while (ok && walk.next(b, t0, t1)) {
         ok = mbar_wait(bar_qfull(qslot), qslot ? qph1 : qph0, abort_flag);
-        if constexpr (WIDE) ok = __all_sync(0xFFFFFFFFu, ok);  // the lanes leave together
+        ok = __all_sync(0xFFFFFFFFu, ok);  // the lanes leave together
         if (!ok) break;
         const uint32_t qaddr = sb + L::off_q + qslot * L::q_bytes;
         if constexpr (WIDE) {
@@ -756,19 +755,21 @@ score_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CU
           for (int tl = t0; tl < t1; ++tl) {
             ok = mbar_wait(bar_full(stage), sphase, abort_flag) &&
                  mbar_wait(bar_tempty(acc), aphase ^ 1u, abort_flag);
+            ok = __all_sync(0xFFFFFFFFu, ok);
             if (!ok) break;
             tc_fence_after();
             const uint32_t kaddr = sb + kOffStages + stage * kTileBytes;
             const uint32_t d = tmem_base + (uint32_t)acc * kAccCols;
+            // K steps of 32 bytes advance both start addresses by 2 (16-byte units)
+            const uint64_t da = smem_desc_sw128(qaddr), db = smem_desc_sw128(kaddr);
 #pragma unroll
             for (int k = 0; k < 4; ++k)
-              mma_f8(d, smem_desc_sw128(qaddr + 32 * k), smem_desc_sw128(kaddr + 32 * k), idesc,
-                     k > 0 ? 1u : 0u);
-            mma_commit(bar_empty(stage));
-            mma_commit(bar_tfull(acc));
+              mma_f8_elect(d, da + 2u * k, db + 2u * k, idesc, k > 0 ? 1u : 0u);
+            mma_commit_elect(bar_empty(stage));
+            mma_commit_elect(bar_tfull(acc));
 #ifdef ICP_TIMELINE
-            if (mma_tiles++ == 0) ICP_STAMP(4);
-            ICP_STAMP(5);
+            if (mma_tiles++ == 0 && lane == 0) ICP_STAMP(4);
+            if (lane == 0) ICP_STAMP(5);
 #endif
             if (++stage == NS) {
               stage = 0;
@@ -781,15 +782,13 @@ score_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CU
           }
         }
         if (!ok) break;
-        if constexpr (WIDE) mma_commit_elect(bar_qempty(qslot));
-        else mma_commit(bar_qempty(qslot));
+        mma_commit_elect(bar_qempty(qslot));
         if (qslot) qph1 ^= 1u; else qph0 ^= 1u;
         qslot ^= 1;
       }
       if (*abort_flag) {
         // every MMA issued so far must finish before TMEM is released
-        if constexpr (WIDE) mma_commit_elect(bar_done);
-        else mma_commit(bar_done);
+        mma_commit_elect(bar_done);
         mbar_wait_drain(bar_done, 0);
       }
     }
@@ -906,8 +905,10 @@ score_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CU
         const int seg_tiles = t1 - t0;
         idx += seg_tiles;
         for (; ok && tl < t1; tl += 4) {
-          if (lane == 0) ok = mbar_wait(bar_tfull(e), aphase, abort_flag);
-          ok = __shfl_sync(0xFFFFFFFFu, ok, 0) != 0;
+          // every lane waits (a lane-0 wait and broadcast was slower: the
+          // batched decode scorer 0.763 against 0.785 of the copy peak)
+          ok = mbar_wait(bar_tfull(e), aphase, abort_flag);
+          ok = __all_sync(0xFFFFFFFFu, ok);
           if (!ok) break;
           tc_fence_after();
           if (g.R == 128)
