@@ -21,9 +21,10 @@
 //              slices (world size 2 or 4), warp 6, a second producer, issues
 //              every other tile: one warp alone cannot issue that many boxes
 //              fast enough.
-//   warp 1     MMA issuer: per tile, 4 x tcgen05.mma kind::f8f6f4 with
-//              A = the replicated queries (M = 128), B = the 128 keys of the
-//              tile (N = 128), K = 32, into one of 4 fp32 TMEM accumulators.
+//   warp 1     MMA issuer (the whole warp waits; an elected lane issues):
+//              per tile, 4 x tcgen05.mma kind::f8f6f4 with A = the
+//              replicated queries (M = 128), B = the 128 keys of the tile
+//              (N = 128), K = 32, into one of 4 fp32 TMEM accumulators.
 //              All 4 heads and all dql tokens share one K tile.
 //   warps 2-5  epilogue: tile i belongs to epilogue warp i % 4, which reads
 //              its lane quarter of the accumulator (thread = query row,
