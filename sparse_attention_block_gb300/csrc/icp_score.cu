@@ -633,8 +633,17 @@ score_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CU
         // adjacent stages, one barrier per slot; j is the tile in its pair
         const int j = WIDE ? ((tl - t0) & 1) : 0;
         if (j == 0) {
-          if (lane == 0) ICP_TIMED(19, ok = mbar_wait(bar_empty(stage), sphase ^ 1u, abort_flag));
-          ok = __shfl_sync(0xFFFFFFFFu, ok, 0) != 0;
+          if constexpr (NPROD == 2) {
+            // the two-producer kernel (launches of 4 KB page slices): every
+            // lane waits, 0.823 against 0.798 of the copy peak on the sharded
+            // workload; the long single-producer streams were slower so
+            // (multitoken 0.968 against 0.999)
+            ICP_TIMED_WARP(19, ok = mbar_wait(bar_empty(stage), sphase ^ 1u, abort_flag));
+            ok = __all_sync(0xFFFFFFFFu, ok);
+          } else {
+            if (lane == 0) ICP_TIMED(19, ok = mbar_wait(bar_empty(stage), sphase ^ 1u, abort_flag));
+            ok = __shfl_sync(0xFFFFFFFFu, ok, 0) != 0;
+          }
           if (!ok) break;
         }
         const int p0 = __shfl_sync(0xFFFFFFFFu, pg_cur, (c0 - grp) & 31);
