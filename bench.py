@@ -47,10 +47,10 @@ FALLBACK_HBM_GBS = 6800.0
 # not part of it).  When the code changes the digest no longer matches and
 # `traffic` is reported null.
 NCU_TRAFFIC = {
-    # dram__bytes_read.sum + dram__bytes_write.sum = 278843392 + 3153408 bytes for
+    # dram__bytes_read.sum + dram__bytes_write.sum = 278825216 + 3099136 bytes for
     # 278330624 bytes of index-K: one ncu capture of a launch over the first 32
     # requests of the multitoken workload
-    ("multitoken", "dc3f39ae1d31cd4f"): (278843392 + 3153408) / 278330624,
+    ("multitoken", "45ef5d0af562f584"): (278825216 + 3099136) / 278330624,
 }
 
 
