@@ -633,11 +633,12 @@ score_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CU
         // adjacent stages, one barrier per slot; j is the tile in its pair
         const int j = WIDE ? ((tl - t0) & 1) : 0;
         if (j == 0) {
-          if constexpr (NPROD == 2) {
-            // the two-producer kernel (launches of 4 KB page slices): every
-            // lane waits, 0.823 against 0.798 of the copy peak on the sharded
-            // workload; the long single-producer streams were slower so
-            // (multitoken 0.968 against 0.999)
+          if constexpr (NPROD == 2 || WIDE) {
+            // the two-producer kernel (launches of 4 KB page slices) and the
+            // prefill scorer: every lane waits, 0.823 against 0.798 of the
+            // copy peak on the sharded workload, 0.744 against 0.738 of the
+            // fp8 peak on the prefill window; the long single-producer
+            // decode streams were slower so (multitoken 0.968 against 0.999)
             ICP_TIMED_WARP(19, ok = mbar_wait(bar_empty(stage), sphase ^ 1u, abort_flag));
             ok = __all_sync(0xFFFFFFFFu, ok);
           } else {
