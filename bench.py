@@ -47,10 +47,10 @@ FALLBACK_HBM_GBS = 6800.0
 # not part of it).  When the code changes the digest no longer matches and
 # `traffic` is reported null.
 NCU_TRAFFIC = {
-    # dram__bytes_read.sum + dram__bytes_write.sum = 278825216 + 3099136 bytes for
+    # dram__bytes_read.sum + dram__bytes_write.sum = 278823424 + 3031552 bytes for
     # 278330624 bytes of index-K: one ncu capture of a launch over the first 32
     # requests of the multitoken workload
-    ("multitoken", "45ef5d0af562f584"): (278825216 + 3099136) / 278330624,
+    ("multitoken", "2dbc8c222f6299f4"): (278823424 + 3031552) / 278330624,
 }
 
 
